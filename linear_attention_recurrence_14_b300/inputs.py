@@ -1,0 +1,121 @@
+"""Seeded synthetic inputs for the Gated DeltaNet core.
+
+This module holds the input recipe only -- no arithmetic of the recurrence.
+Both the tests (for the CUDA path and for the fp64 oracle) and the benchmark
+draw their inputs from here, so the two sides always see the same values.
+
+Recipe (the five workloads below):
+  * q, k ~ N(0, 1) per element, then L2-normalised per (token, head) in fp32
+    and stored in the workload dtype.  The Qwen3.8-Next reading notes
+    (jianyuh.github.io, section 2.1, "Feature parameterization") normalise q
+    and k before the recurrence and call the normalisation load-bearing; the
+    core does not re-normalise.
+  * v ~ N(0, 1), stored in the workload dtype.
+  * alpha = exp(-softplus(a) * s), a ~ N(0, 1), fp32: the decay gate lies in
+    (0, 1) (section 2.1, "Gating dynamics" -- a double-exponential gate with a
+    per-head time constant; here exp(A) is folded into the scale s).
+  * beta = sigmoid(N(0, 1)), fp32 (section 2.1, beta = sigma(W_beta x)).
+  * S0 ~ N(0, s0_std^2) fp32, or absent (zero state) when s0_std == 0.
+Every tensor has its own generator seeded from (seed, tensor name), drawn in
+the fixed order a, b, q, k, v, S0.
+"""
+from __future__ import annotations
+
+import zlib
+from dataclasses import dataclass
+
+import torch
+
+# Named workloads: shapes and gate scales of the five reference workloads.
+WORKLOADS = {
+    # B=1, H=2, T=256, d=64, fp32, gate scale 0.1, zero initial state.
+    "tiny": dict(kind="prefill", B=1, T=256, Hqk=2, Hv=2, d=64, dtype="f32", decay_scale=0.1, s0_std=0.0),
+    # B=2, H=16, T=4096, d=128, bf16, gate scale 0.05, zero initial state.
+    "train": dict(kind="prefill", B=2, T=4096, Hqk=16, Hv=16, d=128, dtype="bf16", decay_scale=0.05, s0_std=0.0),
+    # B=1, 16 q/k heads shared by 32 v heads, T=65536, d=128, S0 ~ N(0, 0.02^2).
+    "grouped": dict(kind="prefill", B=1, T=65536, Hqk=16, Hv=32, d=128, dtype="bf16", decay_scale=0.05, s0_std=0.02),
+    # B=256 sequences, 32 v heads over 16 q/k heads, d=128, 128 single-token steps.
+    "decode": dict(kind="decode", B=256, steps=128, Hqk=16, Hv=32, d=128, dtype="bf16", decay_scale=0.05, s0_std=0.02),
+    # B=1, H=16, T=2^20, d=128, bf16, gate scale 0.01, zero initial state.
+    "long": dict(kind="prefill", B=1, T=1 << 20, Hqk=16, Hv=16, d=128, dtype="bf16", decay_scale=0.01, s0_std=0.0),
+}
+
+_DTYPES = {"f32": torch.float32, "bf16": torch.bfloat16}
+
+
+def torch_dtype(name: str) -> torch.dtype:
+    return _DTYPES[name]
+
+
+def _gen(seed: int, name: str, device) -> torch.Generator:
+    g = torch.Generator(device=device)
+    g.manual_seed((seed * 1_000_003 + zlib.crc32(name.encode())) & 0x7FFF_FFFF_FFFF_FFFF)
+    return g
+
+
+def _randn(shape, seed, name, device):
+    return torch.randn(shape, generator=_gen(seed, name, device), device=device, dtype=torch.float32)
+
+
+def _unit_rows(x: torch.Tensor) -> torch.Tensor:
+    return x / torch.linalg.vector_norm(x, dim=-1, keepdim=True)
+
+
+@dataclass
+class PrefillInputs:
+    q: torch.Tensor        # [B, T, Hqk, dk]
+    k: torch.Tensor        # [B, T, Hqk, dk]
+    v: torch.Tensor        # [B, T, Hv, dv]
+    alpha: torch.Tensor    # [B, T, Hv] fp32
+    beta: torch.Tensor     # [B, T, Hv] fp32
+    S0: torch.Tensor | None  # [B, Hv, dk, dv] fp32
+
+
+def make_prefill_inputs(B, T, Hqk, Hv, d, dtype="bf16", decay_scale=0.05, s0_std=0.0,
+                        seed=0, device="cpu", dv=None) -> PrefillInputs:
+    dk = d
+    dv = d if dv is None else dv
+    td = torch_dtype(dtype)
+    a = _randn((B, T, Hv), seed, "a", device)
+    b = _randn((B, T, Hv), seed, "b", device)
+    alpha = torch.exp(-torch.nn.functional.softplus(a) * decay_scale)
+    beta = torch.sigmoid(b)
+    del a, b
+    q = _unit_rows(_randn((B, T, Hqk, dk), seed, "q", device)).to(td)
+    k = _unit_rows(_randn((B, T, Hqk, dk), seed, "k", device)).to(td)
+    v = _randn((B, T, Hv, dv), seed, "v", device).to(td)
+    S0 = None
+    if s0_std > 0:
+        S0 = _randn((B, Hv, dk, dv), seed, "S0", device) * s0_std
+    return PrefillInputs(q.contiguous(), k.contiguous(), v.contiguous(), alpha.contiguous(), beta.contiguous(), S0)
+
+
+@dataclass
+class DecodeInputs:
+    q: torch.Tensor        # [steps, B, 1, Hqk, dk]
+    k: torch.Tensor        # [steps, B, 1, Hqk, dk]
+    v: torch.Tensor        # [steps, B, 1, Hv, dv]
+    alpha: torch.Tensor    # [steps, B, 1, Hv] fp32
+    beta: torch.Tensor     # [steps, B, 1, Hv] fp32
+    S0: torch.Tensor       # [B, Hv, dk, dv] fp32
+
+
+def make_decode_inputs(B, steps, Hqk, Hv, d, dtype="bf16", decay_scale=0.05, s0_std=0.02,
+                       seed=0, device="cpu") -> DecodeInputs:
+    """Fresh q, k, v, alpha, beta for every step; one initial state."""
+    x = make_prefill_inputs(steps * B, 1, Hqk, Hv, d, dtype, decay_scale, 0.0, seed, device)
+    S0 = _randn((B, Hv, d, d), seed, "S0", device) * s0_std
+    sh = lambda t: t.reshape(steps, B, *t.shape[1:])  # noqa: E731
+    return DecodeInputs(sh(x.q), sh(x.k), sh(x.v), sh(x.alpha), sh(x.beta), S0.contiguous())
+
+
+def workload_inputs(name: str, seed: int = 0, device="cpu", **overrides):
+    """Inputs of a named workload (optionally with some fields overridden)."""
+    w = dict(WORKLOADS[name])
+    w.update(overrides)
+    kind = w.pop("kind")
+    if kind == "decode":
+        return make_decode_inputs(w["B"], w["steps"], w["Hqk"], w["Hv"], w["d"], w["dtype"],
+                                  w["decay_scale"], w["s0_std"], seed, device)
+    return make_prefill_inputs(w["B"], w["T"], w["Hqk"], w["Hv"], w["d"], w["dtype"],
+                               w["decay_scale"], w["s0_std"], seed, device)

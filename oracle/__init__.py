@@ -1,0 +1,6 @@
+"""fp64 CPU oracle for the Gated DeltaNet recurrence.
+
+Test infrastructure: only the test suite, the smoke check and the CPU-baseline
+leg of the benchmark use this package.  The library never imports it.
+"""
+from .oracle import build, recurrence, recurrence_head, library_path  # noqa: F401
