@@ -1,0 +1,172 @@
+/*
+ * gdn.h -- C ABI of the Gated DeltaNet (GDN) token-mixing core on NVIDIA B300
+ * (sm_103a).
+ *
+ * The operation (Qwen3.8-Next reading notes, jianyuh.github.io, section 2.1
+ * "Gated DeltaNet", the four-line gated delta recurrence): per head, with a
+ * matrix state S in R^{dk x dv} stored key-dimension-major ("transposed
+ * convention", dv contiguous), for each token t in order
+ *
+ *     S~  = alpha_t * S_{t-1}
+ *     e_t = v_t - S~^T k_t
+ *     S_t = S~ + beta_t * k_t e_t^T
+ *     y_t = S_t^T q_t
+ *
+ * alpha_t in (0,1] is the decay gate and beta_t in [0,1] the write strength
+ * (same section, "where alpha_t ... beta_t ..."; alpha = 1 and beta in {0,1}
+ * are accepted as boundary values).  q and k are expected L2-normalised per
+ * token (same section, "Feature parameterization": the normalisation keeps the
+ * rank-one transition I - beta k k^T well conditioned); the core does not
+ * re-normalise.
+ *
+ * Tensor layouts (dense, row-major, no padding):
+ *   q, k          [B, T, Hqk, dk]   dtype of gdn_shape.dtype
+ *   v, y          [B, T, Hv,  dv]   dtype of gdn_shape.dtype
+ *   alpha, beta   [B, T, Hv]        fp32
+ *   S0, S_T,
+ *   S_inout       [B, Hv, dk, dv]   fp32, dv contiguous
+ * Value head h reads query/key head h / (Hv / Hqk) (contiguous grouping);
+ * alpha, beta and the state are per value head.
+ *
+ * Supported: dk == dv in {64, 128}; Hv a multiple of Hqk; q, k, v, y, S0,
+ * S_T, S_inout 16-byte aligned; alpha, beta 4-byte aligned.  bf16 prefill runs
+ * the chunked tensor-core kernel (tcgen05/TMEM/TMA); fp32 prefill runs the
+ * token-sequential fp32 kernel; decode runs the HBM-streaming kernel.
+ *
+ * Ownership and execution: the caller owns every buffer (device memory for
+ * all tensors and the workspace).  Calls validate their arguments on the host,
+ * enqueue kernels on `stream` (a cudaStream_t passed as void*, NULL = legacy
+ * default stream) and return without synchronising.  They keep no device
+ * allocation between calls except the TMA descriptors, which are rebuilt per
+ * call and passed by value.  Calls are reentrant; two calls that share an
+ * output buffer or a workspace must be ordered by the caller.
+ *
+ * Errors: argument errors are returned before anything is launched; a failed
+ * launch returns GDN_ERR_CUDA; errors detected on the device are recorded in
+ * the workspace status word and read by gdn_read_device_status.
+ */
+#ifndef GDN_H
+#define GDN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    GDN_OK = 0,
+    GDN_ERR_INVALID_ARG = 1,   /* null pointer, negative size, inconsistent shape */
+    GDN_ERR_UNSUPPORTED = 2,   /* valid but not implemented: head dims, dtype, no sm_103 device */
+    GDN_ERR_ALIGNMENT = 3,     /* a pointer violates the alignment above */
+    GDN_ERR_WORKSPACE = 4,     /* workspace missing or smaller than gdn_prefill_workspace_bytes */
+    GDN_ERR_CUDA = 5,          /* a CUDA runtime/driver call or a launch failed */
+    GDN_ERR_TIMEOUT = 6,       /* a bounded device-side wait gave up (status word) */
+    GDN_ERR_DEVICE = 7,        /* another device-detected inconsistency (status word) */
+    GDN_ERR_ALIASING = 8       /* y overlaps an input, or an output overlaps another output */
+} gdn_status;
+
+typedef enum { GDN_F32 = 0, GDN_BF16 = 1 } gdn_dtype;
+
+/* Problem shape.  T is the number of tokens per sequence (1 for decode). */
+typedef struct {
+    int64_t B, T;
+    int32_t Hqk, Hv, dk, dv;
+    int32_t dtype;              /* gdn_dtype of q, k, v and y */
+} gdn_shape;
+
+/*
+ * Optional prefill controls (pass NULL for the defaults).
+ *
+ * segments: each head's sequence is split into this many contiguous runs of
+ *   chunks that are processed in parallel (0 = chosen from the shape and the
+ *   SM count; 1 = one sequential pass per head).  A run that does not start
+ *   at token 0 rebuilds its entering state from a zero state over a window of
+ *   preceding tokens, the shortest window (at most max_warmup_chunks chunks of
+ *   64 tokens) over which sum(log alpha) <= log_eps.  With unit keys and
+ *   beta in [0,1] every step is a contraction of norm <= alpha_t, so the state
+ *   so rebuilt differs from the exact one by at most exp(log_eps) times the
+ *   state norm at the window start.  When no such window exists the run
+ *   restarts from token 0 and the initial state (exact).
+ * log_eps: natural log of that bound (0 = default, -20 ln 2); must be <= 0.
+ * max_warmup_chunks: window limit (0 = default, 64).
+ * algorithm: GDN_ALGO_AUTO (bf16 -> chunked, fp32 -> sequential),
+ *   GDN_ALGO_CHUNKED (tensor-core chunked kernel; bf16 only, else
+ *   GDN_ERR_UNSUPPORTED) or GDN_ALGO_SEQUENTIAL (token-sequential fp32-math
+ *   kernel, one CTA per head; segments/log_eps do not apply).
+ */
+typedef enum { GDN_ALGO_AUTO = 0, GDN_ALGO_CHUNKED = 1, GDN_ALGO_SEQUENTIAL = 2 } gdn_algorithm;
+
+typedef struct {
+    int32_t segments;
+    float log_eps;
+    int32_t max_warmup_chunks;
+    int32_t algorithm;          /* gdn_algorithm */
+} gdn_prefill_options;
+
+/* Text for a status code (static storage, never NULL). */
+const char *gdn_status_string(gdn_status status);
+
+/*
+ * Bytes of device workspace gdn_prefill needs for this shape: a 256-byte
+ * status area plus B*Hv*dk*dv fp32 values used to stage S_T when it aliases
+ * S0.  Returns 0 for an invalid shape.
+ */
+size_t gdn_prefill_workspace_bytes(const gdn_shape *shape);
+
+/*
+ * Prefill: run the recurrence over T tokens of each (batch, value head) from
+ * the initial state S0 (NULL = zero state), writing every y_t and the final
+ * state S_T.  S_T may equal S0 (in-place update, staged through the
+ * workspace); y must not overlap any input.  ws must be device memory of at
+ * least gdn_prefill_workspace_bytes(shape) bytes, 256-byte aligned; its first
+ * 256 bytes must be zero before the first call (the calls leave them zero
+ * unless a device error was recorded).  T == 0 copies S0 (or zeros) to S_T.
+ * The chunked algebra this computes is the recurrence unrolled over chunks of
+ * 64 tokens: identical up to rounding in exact arithmetic.
+ */
+gdn_status gdn_prefill(const gdn_shape *shape,
+                       const void *q, const void *k, const void *v,
+                       const float *alpha, const float *beta,
+                       const float *S0, void *y, float *S_T,
+                       void *ws, size_t ws_bytes, void *stream);
+
+/* gdn_prefill with explicit options (NULL = defaults). */
+gdn_status gdn_prefill_ex(const gdn_shape *shape, const gdn_prefill_options *options,
+                          const void *q, const void *k, const void *v,
+                          const float *alpha, const float *beta,
+                          const float *S0, void *y, float *S_T,
+                          void *ws, size_t ws_bytes, void *stream);
+
+/*
+ * Decode: one recurrence step (shape->T must be 1) for every (batch, value
+ * head), updating S_inout in place and writing y [B, 1, Hv, dv].  Each head's
+ * fp32 state is streamed once from HBM and written back once.  y must not
+ * overlap any input or S_inout.
+ */
+gdn_status gdn_decode_step(const gdn_shape *shape,
+                           const void *q, const void *k, const void *v,
+                           const float *alpha, const float *beta,
+                           float *S_inout, void *y, void *stream);
+
+/*
+ * Synchronise `stream`, read the status word that gdn_prefill kernels write
+ * into `ws` when they detect an error on the device, clear it, and return
+ * GDN_OK, GDN_ERR_TIMEOUT or GDN_ERR_DEVICE (GDN_ERR_CUDA if the sync fails).
+ */
+gdn_status gdn_read_device_status(void *ws, void *stream);
+
+/* 1 if the current CUDA device can run these kernels (compute capability 10.3). */
+int gdn_device_supported(void);
+
+/* ABI version of this header: major * 10000 + minor * 100 + patch. */
+int gdn_abi_version(void);
+
+#define GDN_ABI_VERSION 10000
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDN_H */

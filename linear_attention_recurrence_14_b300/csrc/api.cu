@@ -1,0 +1,255 @@
+// Host side of the C ABI declared in include/gdn.h: argument validation,
+// aliasing and workspace checks, dispatch to the kernels.  Nothing here
+// computes any part of the recurrence.
+#include <cstdint>
+#include <cstring>
+
+#include "gdn.h"
+#include "gdn_internal.h"
+
+namespace {
+
+constexpr size_t kStatusBytes = 256;
+constexpr float kDefaultLogEps = -13.862943611198906f;  // -20 ln 2
+constexpr int kDefaultMaxWarmupChunks = 64;
+
+bool mul_ok(int64_t a, int64_t b, int64_t *out) {
+    if (a < 0 || b < 0) return false;
+    if (a != 0 && b > INT64_MAX / a) return false;
+    *out = a * b;
+    return true;
+}
+
+// Validates the shape and returns element counts (0 on failure).
+gdn_status check_shape(const gdn_shape *s, int64_t *n_qk, int64_t *n_v, int64_t *n_gate, int64_t *n_state) {
+    if (!s) return GDN_ERR_INVALID_ARG;
+    if (s->B < 0 || s->T < 0 || s->Hqk <= 0 || s->Hv <= 0 || s->dk <= 0 || s->dv <= 0)
+        return GDN_ERR_INVALID_ARG;
+    if (s->Hv % s->Hqk != 0) return GDN_ERR_INVALID_ARG;
+    if (s->dtype != GDN_F32 && s->dtype != GDN_BF16) return GDN_ERR_INVALID_ARG;
+    int64_t bt = 0, tmp = 0;
+    if (!mul_ok(s->B, s->T, &bt)) return GDN_ERR_INVALID_ARG;
+    if (!mul_ok(bt, s->Hqk, &tmp) || !mul_ok(tmp, s->dk, n_qk)) return GDN_ERR_INVALID_ARG;
+    if (!mul_ok(bt, s->Hv, n_gate) || !mul_ok(*n_gate, s->dv, n_v)) return GDN_ERR_INVALID_ARG;
+    if (!mul_ok(s->B, s->Hv, &tmp) || !mul_ok(tmp, static_cast<int64_t>(s->dk) * s->dv, n_state))
+        return GDN_ERR_INVALID_ARG;
+    if (*n_qk > (INT64_MAX >> 3) || *n_v > (INT64_MAX >> 3) || *n_state > (INT64_MAX >> 3))
+        return GDN_ERR_INVALID_ARG;
+    if (!(s->dk == s->dv && (s->dk == 64 || s->dk == 128))) return GDN_ERR_UNSUPPORTED;
+    return GDN_OK;
+}
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+struct Range {
+    const void *p;
+    size_t n;
+};
+
+bool overlap(Range a, Range b) {
+    if (!a.p || !b.p || a.n == 0 || b.n == 0) return false;
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(a.p), b0 = reinterpret_cast<uintptr_t>(b.p);
+    return a0 < b0 + b.n && b0 < a0 + a.n;
+}
+
+gdn_status check_device(int *num_sms) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return GDN_ERR_CUDA;
+    }
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+        cudaGetLastError();
+        return GDN_ERR_CUDA;
+    }
+    if (major != 10 || minor != 3) return GDN_ERR_UNSUPPORTED;
+    return GDN_OK;
+}
+
+gdn_status from_cuda(cudaError_t e) {
+    if (e == cudaSuccess) return GDN_OK;
+    cudaGetLastError();
+    return GDN_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *gdn_status_string(gdn_status status) {
+    switch (status) {
+        case GDN_OK: return "ok";
+        case GDN_ERR_INVALID_ARG: return "invalid argument";
+        case GDN_ERR_UNSUPPORTED: return "unsupported configuration or device";
+        case GDN_ERR_ALIGNMENT: return "misaligned pointer";
+        case GDN_ERR_WORKSPACE: return "workspace missing or too small";
+        case GDN_ERR_CUDA: return "CUDA error";
+        case GDN_ERR_TIMEOUT: return "device-side wait timed out";
+        case GDN_ERR_DEVICE: return "device-detected error";
+        case GDN_ERR_ALIASING: return "overlapping buffers";
+    }
+    return "unknown status";
+}
+
+int gdn_abi_version(void) { return GDN_ABI_VERSION; }
+
+int gdn_device_supported(void) {
+    int sms = 0;
+    return check_device(&sms) == GDN_OK ? 1 : 0;
+}
+
+size_t gdn_prefill_workspace_bytes(const gdn_shape *shape) {
+    int64_t n_qk, n_v, n_gate, n_state;
+    if (check_shape(shape, &n_qk, &n_v, &n_gate, &n_state) != GDN_OK) return 0;
+    return kStatusBytes + static_cast<size_t>(n_state) * sizeof(float);
+}
+
+gdn_status gdn_prefill_ex(const gdn_shape *shape, const gdn_prefill_options *options,
+                          const void *q, const void *k, const void *v,
+                          const float *alpha, const float *beta,
+                          const float *S0, void *y, float *S_T,
+                          void *ws, size_t ws_bytes, void *stream_) {
+    int64_t n_qk, n_v, n_gate, n_state;
+    gdn_status st = check_shape(shape, &n_qk, &n_v, &n_gate, &n_state);
+    if (st != GDN_OK) return st;
+    const gdn_shape &s = *shape;
+    const size_t esz = s.dtype == GDN_BF16 ? 2 : 4;
+    const bool has_tokens = s.B * s.T > 0;
+
+    gdn_prefill_options opt{0, 0.f, 0, GDN_ALGO_AUTO};
+    if (options) opt = *options;
+    if (opt.segments < 0 || opt.max_warmup_chunks < 0 || !(opt.log_eps <= 0.f)) return GDN_ERR_INVALID_ARG;
+    if (opt.algorithm < GDN_ALGO_AUTO || opt.algorithm > GDN_ALGO_SEQUENTIAL) return GDN_ERR_INVALID_ARG;
+    const int algorithm = opt.algorithm;
+    const int segments = opt.segments;
+
+    if (has_tokens && (!q || !k || !v || !alpha || !beta || !y)) return GDN_ERR_INVALID_ARG;
+    if (!ws) return GDN_ERR_WORKSPACE;
+    if (ws_bytes < kStatusBytes + static_cast<size_t>(n_state) * sizeof(float)) return GDN_ERR_WORKSPACE;
+
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(y, 16) || !aligned(S0, 16) ||
+        !aligned(S_T, 16) || !aligned(alpha, 4) || !aligned(beta, 4) || !aligned(ws, 256))
+        return GDN_ERR_ALIGNMENT;
+
+    const Range rq{q, static_cast<size_t>(n_qk) * esz}, rk{k, static_cast<size_t>(n_qk) * esz};
+    const Range rv{v, static_cast<size_t>(n_v) * esz}, ry{y, static_cast<size_t>(n_v) * esz};
+    const Range ra{alpha, static_cast<size_t>(n_gate) * 4}, rb{beta, static_cast<size_t>(n_gate) * 4};
+    const Range rs0{S0, static_cast<size_t>(n_state) * 4}, rst{S_T, static_cast<size_t>(n_state) * 4};
+    const Range rws{ws, ws_bytes};
+    for (const Range &in : {rq, rk, rv, ra, rb, rs0, rst, rws})
+        if (overlap(ry, in)) return GDN_ERR_ALIASING;
+    for (const Range &in : {rq, rk, rv, ra, rb, rws})
+        if (overlap(rst, in)) return GDN_ERR_ALIASING;
+    for (const Range &in : {rq, rk, rv, ra, rb, rs0})
+        if (overlap(rws, in)) return GDN_ERR_ALIASING;
+    const bool in_place = S0 && S_T && S0 == S_T;
+    if (!in_place && overlap(rst, rs0)) return GDN_ERR_ALIASING;
+
+    int num_sms = 0;
+    st = check_device(&num_sms);
+    if (st != GDN_OK) return st;
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+
+    if (s.B * s.Hv == 0) return GDN_OK;
+    if (!has_tokens) {
+        // Empty sequences: the final state is the initial state.
+        if (S_T && !in_place) {
+            if (S0)
+                return from_cuda(cudaMemcpyAsync(S_T, S0, rst.n, cudaMemcpyDeviceToDevice, stream));
+            return from_cuda(cudaMemsetAsync(S_T, 0, rst.n, stream));
+        }
+        return GDN_OK;
+    }
+
+    const bool chunked = algorithm == GDN_ALGO_CHUNKED || (algorithm == GDN_ALGO_AUTO && s.dtype == GDN_BF16);
+    if (chunked && s.dtype != GDN_BF16) return GDN_ERR_UNSUPPORTED;
+
+    if (!chunked) {
+        // Token-sequential path: each CTA reads its own head's S0 before it
+        // writes that head's S_T, so in-place needs no staging.
+        gdn::RecurrentParams p{};
+        p.B = s.B; p.T = s.T; p.Hqk = s.Hqk; p.Hv = s.Hv; p.group = s.Hv / s.Hqk;
+        p.q = q; p.k = k; p.v = v; p.alpha = alpha; p.beta = beta;
+        p.S_in = S0; p.S_out = S_T; p.y = y;
+        return from_cuda(gdn::launch_recurrent(p, s.dk, s.dv, static_cast<gdn_dtype>(s.dtype), stream));
+    }
+
+    gdn::ChunkedParams p{};
+    p.B = s.B; p.T = s.T; p.Hqk = s.Hqk; p.Hv = s.Hv; p.group = s.Hv / s.Hqk; p.d = s.dk;
+    p.q = q; p.k = k; p.v = v; p.alpha = alpha; p.beta = beta; p.S0 = S0; p.y = y;
+    p.status = static_cast<uint32_t *>(ws);
+    float *staging = reinterpret_cast<float *>(static_cast<char *>(ws) + kStatusBytes);
+    // Runs of one head are processed by different CTAs, so a run that reads S0
+    // may start after the head's last run wrote S_T: stage in-place results.
+    p.S_T = in_place ? staging : S_T;
+    p.segments = segments;
+    p.log_eps = opt.log_eps < 0.f ? opt.log_eps : kDefaultLogEps;
+    p.max_warmup_chunks = opt.max_warmup_chunks > 0 ? opt.max_warmup_chunks : kDefaultMaxWarmupChunks;
+    st = from_cuda(gdn::launch_chunked(p, stream, num_sms));
+    if (st != GDN_OK) return st;
+    if (in_place) return from_cuda(cudaMemcpyAsync(S_T, staging, rst.n, cudaMemcpyDeviceToDevice, stream));
+    return GDN_OK;
+}
+
+gdn_status gdn_prefill(const gdn_shape *shape, const void *q, const void *k, const void *v,
+                       const float *alpha, const float *beta, const float *S0, void *y, float *S_T,
+                       void *ws, size_t ws_bytes, void *stream) {
+    return gdn_prefill_ex(shape, nullptr, q, k, v, alpha, beta, S0, y, S_T, ws, ws_bytes, stream);
+}
+
+gdn_status gdn_decode_step(const gdn_shape *shape, const void *q, const void *k, const void *v,
+                           const float *alpha, const float *beta, float *S_inout, void *y, void *stream_) {
+    int64_t n_qk, n_v, n_gate, n_state;
+    gdn_status st = check_shape(shape, &n_qk, &n_v, &n_gate, &n_state);
+    if (st != GDN_OK) return st;
+    const gdn_shape &s = *shape;
+    if (s.T != 1) return GDN_ERR_INVALID_ARG;
+    if (s.B == 0) return GDN_OK;
+    if (!q || !k || !v || !alpha || !beta || !S_inout || !y) return GDN_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(y, 16) || !aligned(S_inout, 16) ||
+        !aligned(alpha, 4) || !aligned(beta, 4))
+        return GDN_ERR_ALIGNMENT;
+    const size_t esz = s.dtype == GDN_BF16 ? 2 : 4;
+    const Range rq{q, static_cast<size_t>(n_qk) * esz}, rk{k, static_cast<size_t>(n_qk) * esz};
+    const Range rv{v, static_cast<size_t>(n_v) * esz}, ry{y, static_cast<size_t>(n_v) * esz};
+    const Range ra{alpha, static_cast<size_t>(n_gate) * 4}, rb{beta, static_cast<size_t>(n_gate) * 4};
+    const Range rs{S_inout, static_cast<size_t>(n_state) * 4};
+    for (const Range &in : {rq, rk, rv, ra, rb, rs})
+        if (overlap(ry, in)) return GDN_ERR_ALIASING;
+    for (const Range &in : {rq, rk, rv, ra, rb})
+        if (overlap(rs, in)) return GDN_ERR_ALIASING;
+    int num_sms = 0;
+    st = check_device(&num_sms);
+    if (st != GDN_OK) return st;
+    gdn::RecurrentParams p{};
+    p.B = s.B; p.T = 1; p.Hqk = s.Hqk; p.Hv = s.Hv; p.group = s.Hv / s.Hqk;
+    p.q = q; p.k = k; p.v = v; p.alpha = alpha; p.beta = beta;
+    p.S_in = S_inout; p.S_out = S_inout; p.y = y;
+    return from_cuda(gdn::launch_recurrent(p, s.dk, s.dv, static_cast<gdn_dtype>(s.dtype),
+                                           static_cast<cudaStream_t>(stream_)));
+}
+
+gdn_status gdn_read_device_status(void *ws, void *stream_) {
+    if (!ws) return GDN_ERR_INVALID_ARG;
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+    if (cudaStreamSynchronize(stream) != cudaSuccess) {
+        cudaGetLastError();
+        return GDN_ERR_CUDA;
+    }
+    uint32_t word = 0;
+    if (cudaMemcpy(&word, ws, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess) {
+        cudaGetLastError();
+        return GDN_ERR_CUDA;
+    }
+    if (word == 0) return GDN_OK;
+    if (cudaMemset(ws, 0, sizeof(word)) != cudaSuccess) {
+        cudaGetLastError();
+        return GDN_ERR_CUDA;
+    }
+    return (word & gdn::kDevTimeout) ? GDN_ERR_TIMEOUT : GDN_ERR_DEVICE;
+}
+
+}  // extern "C"

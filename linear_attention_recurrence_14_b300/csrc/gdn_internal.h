@@ -1,0 +1,48 @@
+// Internal declarations shared by the host-side entry points and the kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "gdn.h"
+
+namespace gdn {
+
+// Status word written by kernels into the first bytes of the prefill workspace.
+// Bit flags; 0 means no error.
+enum DeviceStatusBits : uint32_t {
+    kDevTimeout = 1u << 0,   // a bounded mbarrier wait gave up
+    kDevBadShape = 1u << 1,  // a kernel saw parameters it cannot handle
+};
+
+struct RecurrentParams {
+    int64_t B, T;
+    int Hqk, Hv, group;          // group = Hv / Hqk
+    const void *q, *k, *v;       // [B, T, Hqk, dk] / [B, T, Hv, dv]
+    const float *alpha, *beta;   // [B, T, Hv]
+    const float *S_in;           // [B, Hv, dk, dv] or nullptr (zero state)
+    float *S_out;                // [B, Hv, dk, dv] or nullptr
+    void *y;                     // [B, T, Hv, dv]
+};
+
+// Token-sequential kernel: decode (T == 1, S_in == S_out) and the fp32 prefill.
+cudaError_t launch_recurrent(const RecurrentParams &p, int dk, int dv, gdn_dtype dtype, cudaStream_t stream);
+
+struct ChunkedParams {
+    int64_t B, T;
+    int Hqk, Hv, group, d;       // d = dk = dv (64 runs as zero-padded 128)
+    const void *q, *k, *v;
+    const float *alpha, *beta;
+    const float *S0;             // nullptr = zero state
+    void *y;
+    float *S_T;                  // final states (possibly the workspace staging area)
+    uint32_t *status;            // device status word
+    int segments;                // runs per head
+    float log_eps;
+    int max_warmup_chunks;
+};
+
+// Chunked tensor-core prefill (bf16).  Builds the TMA descriptors and launches.
+cudaError_t launch_chunked(const ChunkedParams &p, cudaStream_t stream, int num_sms);
+
+}  // namespace gdn

@@ -1,0 +1,159 @@
+"""Thin ctypes binding over ``libgdn.so`` (C ABI of ``include/gdn.h``).
+
+Argument marshalling only: shapes are read from the tensors, raw device
+pointers and the current CUDA stream are handed to the C entry points, and
+every step of the computation runs in the library's kernels.  There is no
+fallback: a missing library or a failed call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libgdn.so")
+
+GDN_OK = 0
+STATUS_NAMES = {0: "GDN_OK", 1: "GDN_ERR_INVALID_ARG", 2: "GDN_ERR_UNSUPPORTED", 3: "GDN_ERR_ALIGNMENT",
+                4: "GDN_ERR_WORKSPACE", 5: "GDN_ERR_CUDA", 6: "GDN_ERR_TIMEOUT", 7: "GDN_ERR_DEVICE",
+                8: "GDN_ERR_ALIASING"}
+GDN_F32, GDN_BF16 = 0, 1
+ALGO_AUTO, ALGO_CHUNKED, ALGO_SEQUENTIAL = 0, 1, 2
+
+# Every symbol include/gdn.h declares.
+EXPORTS = ("gdn_status_string", "gdn_prefill_workspace_bytes", "gdn_prefill", "gdn_prefill_ex",
+           "gdn_decode_step", "gdn_read_device_status", "gdn_device_supported", "gdn_abi_version")
+
+
+class GdnShape(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int64), ("T", ctypes.c_int64), ("Hqk", ctypes.c_int32), ("Hv", ctypes.c_int32),
+                ("dk", ctypes.c_int32), ("dv", ctypes.c_int32), ("dtype", ctypes.c_int32)]
+
+
+class GdnPrefillOptions(ctypes.Structure):
+    _fields_ = [("segments", ctypes.c_int32), ("log_eps", ctypes.c_float), ("max_warmup_chunks", ctypes.c_int32),
+                ("algorithm", ctypes.c_int32)]
+
+
+class GdnError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        super().__init__(f"{what}: {STATUS_NAMES.get(code, code)} ({_status_text(code)})")
+        self.code = code
+
+
+_lib = None
+_lock = threading.Lock()
+
+
+def lib() -> ctypes.CDLL:
+    """Load libgdn.so (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(f"{LIB_PATH} is missing: build it with linear_attention_recurrence_14_b300.build")
+            L = ctypes.CDLL(LIB_PATH)
+            vp, fp, c_size = ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t
+            sp = ctypes.POINTER(GdnShape)
+            L.gdn_status_string.restype = ctypes.c_char_p
+            L.gdn_status_string.argtypes = [ctypes.c_int]
+            L.gdn_prefill_workspace_bytes.restype = c_size
+            L.gdn_prefill_workspace_bytes.argtypes = [sp]
+            L.gdn_prefill.restype = ctypes.c_int
+            L.gdn_prefill.argtypes = [sp, vp, vp, vp, fp, fp, fp, vp, fp, vp, c_size, vp]
+            L.gdn_prefill_ex.restype = ctypes.c_int
+            L.gdn_prefill_ex.argtypes = [sp, ctypes.POINTER(GdnPrefillOptions), vp, vp, vp, fp, fp, fp, vp, fp, vp,
+                                         c_size, vp]
+            L.gdn_decode_step.restype = ctypes.c_int
+            L.gdn_decode_step.argtypes = [sp, vp, vp, vp, fp, fp, fp, vp, vp]
+            L.gdn_read_device_status.restype = ctypes.c_int
+            L.gdn_read_device_status.argtypes = [vp, vp]
+            L.gdn_device_supported.restype = ctypes.c_int
+            L.gdn_abi_version.restype = ctypes.c_int
+            _lib = L
+    return _lib
+
+
+def _status_text(code: int) -> str:
+    try:
+        return lib().gdn_status_string(code).decode()
+    except Exception:  # pragma: no cover
+        return "?"
+
+
+def _check(code: int, what: str):
+    if code != GDN_OK:
+        raise GdnError(code, what)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return GDN_BF16
+    if t.dtype == torch.float32:
+        return GDN_F32
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def shape_of(q: torch.Tensor, v: torch.Tensor) -> GdnShape:
+    B, T, Hqk, dk = q.shape
+    Hv, dv = v.shape[2], v.shape[3]
+    return GdnShape(B, T, Hqk, Hv, dk, dv, _dtype_code(q))
+
+
+def workspace_bytes(shape: GdnShape) -> int:
+    return int(lib().gdn_prefill_workspace_bytes(ctypes.byref(shape)))
+
+
+def new_workspace(shape: GdnShape, device) -> torch.Tensor:
+    """A zeroed workspace of the size gdn_prefill needs (uint8, 256-byte aligned by the allocator)."""
+    return torch.zeros(max(workspace_bytes(shape), 256), dtype=torch.uint8, device=device)
+
+
+def prefill(q, k, v, alpha, beta, S0=None, *, y=None, S_T=None, workspace=None, segments=0, log_eps=0.0,
+            max_warmup_chunks=0, algorithm=ALGO_AUTO, stream=None):
+    """Run gdn_prefill_ex on device tensors; returns (y, S_T).
+
+    q, k [B,T,Hqk,d]; v [B,T,Hv,d]; alpha, beta [B,T,Hv] fp32; S0 [B,Hv,d,d] fp32 or None.
+    """
+    shape = shape_of(q, v)
+    if y is None:
+        y = torch.empty_like(v)
+    if S_T is None:
+        S_T = torch.empty((shape.B, shape.Hv, shape.dk, shape.dv), dtype=torch.float32, device=v.device)
+    if workspace is None:
+        workspace = new_workspace(shape, v.device)
+    opts = GdnPrefillOptions(segments, log_eps, max_warmup_chunks, algorithm)
+    rc = lib().gdn_prefill_ex(ctypes.byref(shape), ctypes.byref(opts), _ptr(q), _ptr(k), _ptr(v), _ptr(alpha),
+                              _ptr(beta), _ptr(S0), _ptr(y), _ptr(S_T), _ptr(workspace),
+                              workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(rc, "gdn_prefill_ex")
+    return y, S_T
+
+
+def decode_step(q, k, v, alpha, beta, S, *, y=None, stream=None):
+    """Run gdn_decode_step: one token per sequence, S [B,Hv,d,d] fp32 updated in place; returns y."""
+    shape = shape_of(q, v)
+    if y is None:
+        y = torch.empty_like(v)
+    rc = lib().gdn_decode_step(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(beta), _ptr(S),
+                               _ptr(y), _stream(stream))
+    _check(rc, "gdn_decode_step")
+    return y
+
+
+def read_device_status(workspace, stream=None) -> int:
+    """Synchronise and return (and clear) the device status recorded in the workspace."""
+    return int(lib().gdn_read_device_status(_ptr(workspace), _stream(stream)))

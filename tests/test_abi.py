@@ -1,0 +1,107 @@
+"""C-ABI checks that need no GPU: the library loads, exports every symbol
+include/gdn.h declares, and rejects bad arguments on the host before any CUDA
+call (the pointers below are never dereferenced)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from linear_attention_recurrence_14_b300 import build as gbuild
+from linear_attention_recurrence_14_b300 import gdn
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    gbuild.build()
+    return gdn.lib()
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "gdn.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(gdn_[a-z_]+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol(L):
+    names = declared_functions()
+    assert set(names) == set(gdn.EXPORTS)
+    for n in names:
+        assert hasattr(L, n), n
+
+
+def test_status_strings_and_version(L):
+    for code in range(9):
+        assert L.gdn_status_string(code)
+    assert L.gdn_status_string(1234) == b"unknown status"
+    assert L.gdn_abi_version() == 10000
+
+
+def shape(B=1, T=64, Hqk=2, Hv=4, d=128, dtype=gdn.GDN_BF16):
+    return gdn.GdnShape(B, T, Hqk, Hv, d, d, dtype)
+
+
+def test_workspace_bytes(L):
+    s = shape(B=2, Hv=4, d=128)
+    assert gdn.workspace_bytes(s) == 256 + 2 * 4 * 128 * 128 * 4
+    assert gdn.workspace_bytes(shape(Hqk=3, Hv=4)) == 0
+    assert L.gdn_prefill_workspace_bytes(None) == 0
+
+
+BASE = 1 << 32  # fake, 256-byte aligned device addresses; never dereferenced
+MB = 1 << 20
+
+
+def call_prefill(L, s, q=BASE, k=BASE + 64 * MB, v=BASE + 128 * MB, a=BASE + 192 * MB, b=BASE + 200 * MB,
+                 S0=None, y=BASE + 256 * MB, S_T=BASE + 320 * MB, ws=BASE + 384 * MB, ws_bytes=None, opts=None):
+    if ws_bytes is None:
+        ws_bytes = max(gdn.workspace_bytes(s), 256) if s is not None else 256
+    vp = lambda x: None if x is None else ctypes.c_void_p(x)  # noqa: E731
+    o = None if opts is None else ctypes.byref(opts)
+    return L.gdn_prefill_ex(ctypes.byref(s) if s is not None else None, o, vp(q), vp(k), vp(v), vp(a), vp(b),
+                            vp(S0), vp(y), vp(S_T), vp(ws), ws_bytes, None)
+
+
+def test_prefill_rejects_bad_arguments(L):
+    E = {v: k for k, v in gdn.STATUS_NAMES.items()}
+    assert call_prefill(L, None) == E["GDN_ERR_INVALID_ARG"]
+    assert call_prefill(L, shape(Hqk=3, Hv=4)) == E["GDN_ERR_INVALID_ARG"]
+    assert call_prefill(L, shape(T=-1)) == E["GDN_ERR_INVALID_ARG"]
+    assert call_prefill(L, gdn.GdnShape(1, 64, 1, 1, 128, 128, 7)) == E["GDN_ERR_INVALID_ARG"]
+    assert call_prefill(L, gdn.GdnShape(1, 64, 1, 1, 96, 96, 1)) == E["GDN_ERR_UNSUPPORTED"]
+    assert call_prefill(L, gdn.GdnShape(1, 64, 1, 1, 128, 64, 1)) == E["GDN_ERR_UNSUPPORTED"]
+    assert call_prefill(L, shape(), q=None) == E["GDN_ERR_INVALID_ARG"]
+    assert call_prefill(L, shape(), ws=None) == E["GDN_ERR_WORKSPACE"]
+    assert call_prefill(L, shape(), ws_bytes=255) == E["GDN_ERR_WORKSPACE"]
+    assert call_prefill(L, shape(), q=BASE + 8) == E["GDN_ERR_ALIGNMENT"]
+    assert call_prefill(L, shape(), a=BASE + 192 * MB + 2) == E["GDN_ERR_ALIGNMENT"]
+    assert call_prefill(L, shape(), ws=BASE + 384 * MB + 16) == E["GDN_ERR_ALIGNMENT"]
+    assert call_prefill(L, shape(), y=BASE) == E["GDN_ERR_ALIASING"]              # y == q
+    assert call_prefill(L, shape(), S_T=BASE + 128 * MB) == E["GDN_ERR_ALIASING"]  # S_T inside v
+    assert call_prefill(L, shape(), S0=BASE + 320 * MB + 256) == E["GDN_ERR_ALIASING"]  # partial S0/S_T overlap
+    bad = gdn.GdnPrefillOptions(-1, 0.0, 0, 0)
+    assert call_prefill(L, shape(), opts=bad) == E["GDN_ERR_INVALID_ARG"]
+    bad = gdn.GdnPrefillOptions(0, 0.5, 0, 0)
+    assert call_prefill(L, shape(), opts=bad) == E["GDN_ERR_INVALID_ARG"]
+    bad = gdn.GdnPrefillOptions(0, 0.0, 0, 3)
+    assert call_prefill(L, shape(), opts=bad) == E["GDN_ERR_INVALID_ARG"]
+
+
+def test_decode_rejects_bad_arguments(L):
+    E = {v: k for k, v in gdn.STATUS_NAMES.items()}
+    vp = ctypes.c_void_p
+    s = shape(T=1)
+    args = [vp(BASE), vp(BASE + MB), vp(BASE + 2 * MB), vp(BASE + 3 * MB), vp(BASE + 4 * MB), vp(BASE + 5 * MB),
+            vp(BASE + 9 * MB)]
+    assert L.gdn_decode_step(ctypes.byref(shape(T=2)), *args, None) == E["GDN_ERR_INVALID_ARG"]
+    bad = list(args)
+    bad[6] = vp(BASE + 5 * MB)  # y == S_inout
+    assert L.gdn_decode_step(ctypes.byref(s), *bad, None) == E["GDN_ERR_ALIASING"]
+    bad = list(args)
+    bad[5] = None
+    assert L.gdn_decode_step(ctypes.byref(s), *bad, None) == E["GDN_ERR_INVALID_ARG"]
+    bad = list(args)
+    bad[5] = vp(BASE + 5 * MB + 4)
+    assert L.gdn_decode_step(ctypes.byref(s), *bad, None) == E["GDN_ERR_ALIGNMENT"]
