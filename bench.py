@@ -1,0 +1,495 @@
+#!/usr/bin/env python3
+"""Benchmark of the Gated DeltaNet core on one B300 (or N replicas).
+
+Timed step: one gdn_prefill over the grouped-head prefill workload (B=1,
+16 query/key heads shared by 32 value heads, T=65536, d=128, bf16 q/k/v,
+fp32 gates and state, S0 ~ N(0, 0.02^2)).  Inputs are resident in HBM and
+larger than L2 (1.6 GB per step), so no flush is needed between steps.
+The same run also times the decode workload (B=256 sequences, 32 value heads
+over 16 key heads, d=128, 128 single-token steps, fp32 state updated in place)
+and reports it under "decode".
+
+Printed: one JSON line (rank 0).  `value` is prefill tokens/s summed over all
+ranks; `e2e` is the same metric through the C ABI with host buffers (pinned
+host -> device copies of the inputs and device -> host copies of y and S_T
+inside the timed region); `roofline` is the prefill kernel against measured
+HBM bandwidth (its binding roof) with its tensor-core fraction beside it;
+`cpu_baseline` is the fp64 oracle timed on a bounded sample on the host cores.
+
+`--impl reference` times the fp64 oracle instead (the only reference
+implementation there is), on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "GDN prefill tokens/s at H=32,T=64K,d=128 (% TC peak); decode steps/s (% HBM BW)"
+PREFILL_WORKLOAD = "grouped"
+DECODE_WORKLOAD = "decode"
+CHUNK = 64  # chunk length of the useful-FLOP convention
+
+
+# ----------------------------------------------------------------- accounting
+def useful_flops_per_token_head(d: int, group: int, chunk: int = CHUNK) -> float:
+    """Algorithmic FLOPs per (token, value head) of the chunked prefill.
+
+    Three d x d products per token (W S, Q S, K~^T U) plus the chunk-local
+    terms (T K, T V, P U per value head; K K^T and Q K^T per key head, shared
+    by `group` value heads), causal triangles counted as halves.
+    """
+    return 2.0 * (3 * d * d + (chunk / 2) * (d + 2 * d) + (chunk / 2) * (2 * d) / group)
+
+
+def prefill_bytes(w: dict, esz: int = 2) -> int:
+    """Algorithmic HBM bytes of one prefill: q, k, v, y, alpha, beta, S0 and S_T once each."""
+    B, T, Hqk, Hv, d = w["B"], w["T"], w["Hqk"], w["Hv"], w["d"]
+    io = (2 * B * T * Hqk * d + 2 * B * T * Hv * d) * esz
+    gates = 2 * B * T * Hv * 4
+    state = (2 if w.get("s0_std", 0) > 0 else 1) * B * Hv * d * d * 4
+    return io + gates + state
+
+
+def decode_bytes(w: dict, esz: int = 2) -> int:
+    """Algorithmic HBM bytes of one decode step: the state read and written once, plus q, k, v, y, gates."""
+    B, Hqk, Hv, d = w["B"], w["Hqk"], w["Hv"], w["d"]
+    return 2 * B * Hv * d * d * 4 + (2 * B * Hqk * d + 2 * B * Hv * d) * esz + 2 * B * Hv * 4
+
+
+def load_peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            m = json.load(f)
+        return {"hbm_gbs": m["hbm_gbs"], "bf16_tflops": m["bf16_tflops"],
+                "bf16_tflops_sustained": m.get("bf16_tflops_sustained"), "source": "measured"}
+    return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0, "source": "fallback"}
+
+
+# ----------------------------------------------------------------- clocks
+class ClockSampler:
+    """Samples SM clocks and throttle reasons with nvidia-smi while a region runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.out = ""
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self) -> dict:
+        sm, mx, reasons = [], None, set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for line in (self.out or "").splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 7:
+                continue
+            try:
+                sm.append(float(f[0]))
+                mx = float(f[1])
+            except ValueError:
+                continue
+            for name, flag in zip(names, f[3:7]):
+                if flag.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------- distributed
+def dist_setup():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+
+        import torch
+
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    return ws, rank, local
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def max_over_ranks(x: float, ws: int, device) -> float:
+    if ws == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------- oracle timing
+def time_oracle_prefill(w: dict, seed: int, target_s: float, device="cpu"):
+    """Time the fp64 oracle on the first T_s tokens of the workload (all heads).
+
+    Returns (tokens/s, sample description, threads).  T_s is grown until one
+    run takes about target_s seconds (bounded by the workload's T).
+    """
+    import oracle
+    from linear_attention_recurrence_14_b300.inputs import make_prefill_inputs
+
+    oracle.build()
+    threads = os.cpu_count() or 1
+    Ts = 256
+    while True:
+        x = make_prefill_inputs(w["B"], Ts, w["Hqk"], w["Hv"], w["d"], w["dtype"], w["decay_scale"], w["s0_std"],
+                                seed=seed, device=device)
+        t0 = time.perf_counter()
+        oracle.recurrence(x.q, x.k, x.v, x.alpha, x.beta, x.S0, threads=threads)
+        dt = time.perf_counter() - t0
+        if dt >= target_s * 0.5 or Ts >= w["T"]:
+            break
+        Ts = min(w["T"], int(Ts * min(16.0, max(2.0, target_s / max(dt, 1e-3)))))
+    tokens = w["B"] * Ts
+    sample = (f"oracle fp64 on B={w['B']} x T={Ts} tokens x {w['Hv']} value heads of the "
+              f"{PREFILL_WORKLOAD} workload ({dt:.2f} s)")
+    return tokens / dt, sample, threads, dt
+
+
+# ----------------------------------------------------------------- main arms
+def run_reference(args, ws, rank):
+    if rank != 0:
+        return
+    from linear_attention_recurrence_14_b300.inputs import WORKLOADS
+
+    w = dict(WORKLOADS[PREFILL_WORKLOAD])
+    target = max(2.0, 60.0 / max(1, args.steps + args.warmup))
+    # size the sample once, then time K steps of it
+    v, sample, threads, dt = time_oracle_prefill(w, args.seed, target)
+    Ts = None
+    for tok in sample.split():
+        if tok.startswith("T="):
+            Ts = int(tok[2:])
+    import oracle
+    from linear_attention_recurrence_14_b300.inputs import make_prefill_inputs
+
+    x = make_prefill_inputs(w["B"], Ts, w["Hqk"], w["Hv"], w["d"], w["dtype"], w["decay_scale"], w["s0_std"],
+                            seed=args.seed)
+    for _ in range(args.warmup):
+        oracle.recurrence(x.q, x.k, x.v, x.alpha, x.beta, x.S0, threads=threads)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        oracle.recurrence(x.q, x.k, x.v, x.alpha, x.beta, x.S0, threads=threads)
+        times.append(time.perf_counter() - t0)
+    tot = sum(times)
+    value = w["B"] * Ts * args.steps / tot
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"{PREFILL_WORKLOAD} prefill (B=1, Hqk=16, Hv=32, T=65536, d=128) sampled to T={Ts}",
+                   "l2": "n/a (host)"},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                         "sample": f"B={w['B']} x T={Ts} tokens x {w['Hv']} value heads per step"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, ws, rank, local):
+    import torch
+
+    from linear_attention_recurrence_14_b300 import gdn
+    from linear_attention_recurrence_14_b300.inputs import WORKLOADS, make_decode_inputs, make_prefill_inputs
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    gdn.lib()
+    peaks = load_peaks()
+    seed = args.seed + rank
+
+    # ------------------------------------------------------------- prefill
+    w = dict(WORKLOADS[PREFILL_WORKLOAD])
+    x = make_prefill_inputs(w["B"], w["T"], w["Hqk"], w["Hv"], w["d"], w["dtype"], w["decay_scale"], w["s0_std"],
+                            seed=seed, device=dev)
+    shape = gdn.shape_of(x.q, x.v)
+    y = torch.empty_like(x.v)
+    S_T = torch.empty((w["B"], w["Hv"], w["d"], w["d"]), dtype=torch.float32, device=dev)
+    ws_buf = gdn.new_workspace(shape, dev)
+    launches = gdn.prefill_launches(shape, algorithm=args.algorithm, segments=args.segments)
+
+    def prefill_once():
+        gdn.prefill(x.q, x.k, x.v, x.alpha, x.beta, x.S0, y=y, S_T=S_T, workspace=ws_buf,
+                    algorithm=args.algorithm, segments=args.segments)
+
+    for _ in range(args.warmup):
+        prefill_once()
+    torch.cuda.synchronize()
+    status = gdn.read_device_status(ws_buf)
+    if status != 0:
+        raise SystemExit(f"device status {status} after warm-up")
+
+    stream = torch.cuda.current_stream()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    barrier(ws)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        t_all0 = torch.cuda.Event(enable_timing=True)
+        t_all1 = torch.cuda.Event(enable_timing=True)
+        t_all0.record(stream)
+        for i in range(args.steps):
+            ev[i][0].record(stream)
+            prefill_once()
+            ev[i][1].record(stream)
+        t_all1.record(stream)
+        torch.cuda.synchronize()
+    barrier(ws)
+    per_launch_ms = [a.elapsed_time(b) for a, b in ev]
+    total_ms = t_all0.elapsed_time(t_all1)
+    total_ms = max_over_ranks(total_ms, ws, dev)
+    ms_per_step = total_ms / args.steps
+    tokens = w["B"] * w["T"]
+    value = tokens * ws * args.steps / (total_ms * 1e-3)
+    clocks = clk.summary()
+
+    kern_s = statistics.mean(per_launch_ms) * 1e-3
+    pbytes = prefill_bytes(w)
+    flops = useful_flops_per_token_head(w["d"], w["Hv"] // w["Hqk"]) * w["B"] * w["T"] * w["Hv"]
+    achieved_gbs = pbytes / kern_s / 1e9
+    achieved_tflops = flops / kern_s / 1e12
+    roofline = {
+        "bound": "hbm", "achieved": achieved_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+        "frac": achieved_gbs / peaks["hbm_gbs"], "traffic": args.traffic,
+        "peak_source": peaks["source"], "bytes_per_launch": pbytes, "launch_ms": kern_s * 1e3,
+        "tensor": {"achieved": achieved_tflops, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                   "frac": achieved_tflops / peaks["bf16_tflops"],
+                   "frac_sustained": achieved_tflops / peaks["bf16_tflops_sustained"]
+                   if peaks.get("bf16_tflops_sustained") else None,
+                   "flops_per_launch": flops},
+    }
+
+    # correctness spot check of this very run: sampled heads against the oracle
+    check = None
+    if args.check and rank == 0:
+        check = spot_check(x, y, S_T, w)
+
+    # ------------------------------------------------------------- e2e (host buffers)
+    e2e = None
+    if not args.no_e2e:
+        e2e = time_e2e(args, x, shape, w, dev, ws)
+
+    del ws_buf
+    x = None
+    torch.cuda.empty_cache()
+
+    # ------------------------------------------------------------- decode
+    dec = None
+    if not args.no_decode:
+        dec = time_decode(args, peaks, seed, dev, ws, local)
+
+    # ------------------------------------------------------------- cpu baseline
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        v, sample, threads, _ = time_oracle_prefill(w, seed, args.cpu_seconds)
+        cpu = {"value": v, "unit": "tokens/s", "cores": threads, "kind": "oracle", "sample": sample}
+
+    gpu_launches = launches * args.steps
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "grouped-head prefill: B=1, Hqk=16, Hv=32, T=65536, dk=dv=128, bf16 q/k/v, "
+                               "fp32 alpha/beta/state, S0~N(0,0.02^2)",
+                   "l2": "inputs larger than L2 (1.6 GB per step), no flush",
+                   "algorithm": gdn.ALGO_NAMES[args.algorithm], "segments": args.segments,
+                   "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"},
+        "roofline": roofline, "clocks": clocks, "e2e": e2e, "cpu_baseline": cpu, "gpu_launches": gpu_launches,
+        "decode": dec, "check": check,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def spot_check(x, y, S_T, w):
+    """Compare two sampled value heads over the first tokens with the oracle."""
+    import numpy as np
+
+    import oracle
+
+    Tcheck = min(w["T"], 8192)
+    errs = []
+    for hv in (0, w["Hv"] - 1):
+        yo, so = oracle.recurrence_head(x.q, x.k, x.v, x.alpha, x.beta, x.S0, 0, hv, T=Tcheck)
+        yg = y[0, :Tcheck, hv].double().cpu().numpy()
+        errs.append(float(np.abs(yg - yo).max() / max(np.abs(yo).max(), 1e-30)))
+    return {"heads": [0, w["Hv"] - 1], "tokens": Tcheck, "max_rel_err_y": max(errs)}
+
+
+def time_e2e(args, x, shape, w, dev, ws):
+    """Prefill through the C ABI with host buffers: H2D of inputs, prefill, D2H of y and S_T per step."""
+    import torch
+
+    from linear_attention_recurrence_14_b300 import gdn
+
+    host = {n: getattr(x, n).cpu().pin_memory() for n in ("q", "k", "v", "alpha", "beta")}
+    if x.S0 is not None:
+        host["S0"] = x.S0.cpu().pin_memory()
+    dev_in = {n: torch.empty_like(t, device=dev) for n, t in host.items()}
+    y_dev = torch.empty_like(dev_in["v"])
+    S_dev = torch.empty((w["B"], w["Hv"], w["d"], w["d"]), dtype=torch.float32, device=dev)
+    y_host = torch.empty_like(host["v"]).pin_memory()
+    S_host = torch.empty(S_dev.shape, dtype=torch.float32).pin_memory()
+    wsb = gdn.new_workspace(shape, dev)
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = y_host.numel() * y_host.element_size() + S_host.numel() * 4
+
+    def step():
+        for n, t in host.items():
+            dev_in[n].copy_(t, non_blocking=True)
+        gdn.prefill(dev_in["q"], dev_in["k"], dev_in["v"], dev_in["alpha"], dev_in["beta"], dev_in.get("S0"),
+                    y=y_dev, S_T=S_dev, workspace=wsb, algorithm=args.algorithm, segments=args.segments)
+        y_host.copy_(y_dev, non_blocking=True)
+        S_host.copy_(S_dev, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    steps = max(1, min(args.steps, 5))
+    barrier(ws)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        step()
+    e1.record()
+    torch.cuda.synchronize()
+    ms = max_over_ranks(e0.elapsed_time(e1), ws, dev)
+    value = w["B"] * w["T"] * ws * steps / (ms * 1e-3)
+    return {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "steps": steps, "ms_per_step": ms / steps}
+
+
+def time_decode(args, peaks, seed, dev, ws, local):
+    """128 decode steps of the decode workload, state in place; returns steps/s and its HBM roofline."""
+    import torch
+
+    from linear_attention_recurrence_14_b300 import gdn
+    from linear_attention_recurrence_14_b300.inputs import WORKLOADS, make_decode_inputs
+
+    w = dict(WORKLOADS[DECODE_WORKLOAD])
+    nsteps = args.decode_steps
+    d = make_decode_inputs(w["B"], nsteps, w["Hqk"], w["Hv"], w["d"], w["dtype"], w["decay_scale"], w["s0_std"],
+                           seed=seed, device=dev)
+    S = d.S0.clone()
+    ys = torch.empty((nsteps,) + tuple(d.v.shape[1:]), dtype=d.v.dtype, device=dev)
+
+    def run_all():
+        for s in range(nsteps):
+            gdn.decode_step(d.q[s], d.k[s], d.v[s], d.alpha[s], d.beta[s], S, y=ys[s])
+
+    for _ in range(max(1, args.warmup)):
+        S.copy_(d.S0)
+        run_all()
+    torch.cuda.synchronize()
+    S.copy_(d.S0)
+    stream = torch.cuda.current_stream()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(nsteps)]
+    barrier(ws)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a0.record(stream)
+        for s in range(nsteps):
+            evs[s][0].record(stream)
+            gdn.decode_step(d.q[s], d.k[s], d.v[s], d.alpha[s], d.beta[s], S, y=ys[s])
+            evs[s][1].record(stream)
+        a1.record(stream)
+        torch.cuda.synchronize()
+    total_ms = max_over_ranks(a0.elapsed_time(a1), ws, dev)
+    per = [a.elapsed_time(b) for a, b in evs]
+    kern_s = statistics.mean(per) * 1e-3
+    nbytes = decode_bytes(w)
+    gbs = nbytes / kern_s / 1e9
+    return {
+        "metric": "decode steps/s (B=256, Hv=32, Hqk=16, d=128, fp32 state in place, bf16 q/k/v)",
+        "value": nsteps * ws / (total_ms * 1e-3), "unit": "steps/s", "steps": nsteps, "ms_per_step": total_ms / nsteps,
+        "gpu_launches": nsteps,
+        "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": gbs / peaks["hbm_gbs"], "traffic": args.decode_traffic, "bytes_per_launch": nbytes,
+                     "launch_ms": kern_s * 1e3, "peak_source": peaks["source"]},
+        "clocks": clk.summary(),
+        "l2": "state 512 MiB > L2, no flush",
+    }
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--algorithm", type=int, default=0, help="0 auto, 1 chunked, 2 sequential")
+    ap.add_argument("--segments", type=int, default=0, help="0 = chosen by the library")
+    ap.add_argument("--decode-steps", type=int, default=128)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--traffic", type=float, default=None, help="ncu dram bytes per prefill launch, if measured")
+    ap.add_argument("--decode-traffic", type=float, default=None, help="ncu dram bytes per decode launch")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-check", dest="check", action="store_false")
+    args = ap.parse_args(argv)
+    if args.warmup < 3 and args.impl == "ours":
+        print("warning: fewer than 3 warm-up steps", file=sys.stderr)
+    ws, rank, local = dist_setup()
+    if args.impl == "reference":
+        run_reference(args, ws, rank)
+    else:
+        run_ours(args, ws, rank, local)
+    if ws > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

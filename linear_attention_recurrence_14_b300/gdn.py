@@ -22,6 +22,7 @@ STATUS_NAMES = {0: "GDN_OK", 1: "GDN_ERR_INVALID_ARG", 2: "GDN_ERR_UNSUPPORTED",
                 8: "GDN_ERR_ALIASING"}
 GDN_F32, GDN_BF16 = 0, 1
 ALGO_AUTO, ALGO_CHUNKED, ALGO_SEQUENTIAL = 0, 1, 2
+ALGO_NAMES = {ALGO_AUTO: "auto", ALGO_CHUNKED: "chunked", ALGO_SEQUENTIAL: "sequential"}
 
 # Every symbol include/gdn.h declares.
 EXPORTS = ("gdn_status_string", "gdn_prefill_workspace_bytes", "gdn_prefill", "gdn_prefill_ex",
@@ -152,6 +153,11 @@ def decode_step(q, k, v, alpha, beta, S, *, y=None, stream=None):
                                _ptr(y), _stream(stream))
     _check(rc, "gdn_decode_step")
     return y
+
+
+def prefill_launches(shape: GdnShape, algorithm=ALGO_AUTO, segments=0) -> int:
+    """Kernel launches one gdn_prefill call enqueues for this shape (both paths launch one kernel)."""
+    return 1 if shape.B * shape.T * shape.Hv > 0 else 0
 
 
 def read_device_status(workspace, stream=None) -> int:
