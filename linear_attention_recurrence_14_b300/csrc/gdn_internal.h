@@ -42,6 +42,10 @@ struct ChunkedParams {
     int max_warmup_chunks;
 };
 
+// Number of sequence segments per (batch, value head) the chunked prefill uses
+// (requested > 0 is taken as is, capped at the chunk count).
+int plan_segments(int64_t pairs, int64_t nchunks, int num_sms, int requested);
+
 // Chunked tensor-core prefill (bf16).  Builds the TMA descriptors and launches.
 cudaError_t launch_chunked(const ChunkedParams &p, cudaStream_t stream, int num_sms);
 

@@ -94,6 +94,22 @@ def _ptr(t):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
 
 
+def _require(tensors: dict):
+    """The C ABI takes dense row-major device buffers: reject views it cannot address."""
+    dev = None
+    for name, t in tensors.items():
+        if t is None:
+            continue
+        if not t.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+        if dev is None:
+            dev = t.device
+        elif t.device != dev:
+            raise ValueError(f"{name} is on {t.device}, expected {dev}")
+
+
 def _dtype_code(t: torch.Tensor) -> int:
     if t.dtype == torch.bfloat16:
         return GDN_BF16
@@ -129,6 +145,7 @@ def prefill(q, k, v, alpha, beta, S0=None, *, y=None, S_T=None, workspace=None, 
 
     q, k [B,T,Hqk,d]; v [B,T,Hv,d]; alpha, beta [B,T,Hv] fp32; S0 [B,Hv,d,d] fp32 or None.
     """
+    _require(dict(q=q, k=k, v=v, alpha=alpha, beta=beta, S0=S0, y=y, S_T=S_T, workspace=workspace))
     shape = shape_of(q, v)
     if y is None:
         y = torch.empty_like(v)
@@ -146,6 +163,7 @@ def prefill(q, k, v, alpha, beta, S0=None, *, y=None, S_T=None, workspace=None, 
 
 def decode_step(q, k, v, alpha, beta, S, *, y=None, stream=None):
     """Run gdn_decode_step: one token per sequence, S [B,Hv,d,d] fp32 updated in place; returns y."""
+    _require(dict(q=q, k=k, v=v, alpha=alpha, beta=beta, S=S, y=y))
     shape = shape_of(q, v)
     if y is None:
         y = torch.empty_like(v)

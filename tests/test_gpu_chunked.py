@@ -1,0 +1,159 @@
+"""GPU parity of the chunked tensor-core prefill (bf16 q/k/v, fp32 gates and
+state) against the fp64 oracle, through the C ABI.
+
+Tolerance: max|gpu - oracle| / max|oracle| <= 2e-2 over each compared tensor
+(bf16 inputs with an fp32 state)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from linear_attention_recurrence_14_b300 import build as gbuild
+from linear_attention_recurrence_14_b300 import gdn
+from linear_attention_recurrence_14_b300.inputs import make_prefill_inputs, workload_inputs
+
+from .helpers import TOL, rel_err
+
+pytestmark = pytest.mark.gpu
+BF16_TOL = TOL[torch.bfloat16]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    gbuild.build()
+    oracle.build()
+
+
+def _chunked(x, **kw):
+    return gdn.prefill(x.q, x.k, x.v, x.alpha, x.beta, x.S0, algorithm=gdn.ALGO_CHUNKED, **kw)
+
+
+@pytest.mark.parametrize(
+    "B,T,Hqk,Hv,d,s0,segments",
+    [
+        (1, 64, 1, 1, 128, 0.0, 1),      # one full chunk
+        (1, 1, 1, 1, 128, 0.02, 1),      # a single token
+        (1, 65, 1, 2, 128, 0.02, 1),     # ragged tail
+        (2, 200, 2, 4, 128, 0.02, 1),    # grouped heads, several chunks
+        (1, 300, 2, 2, 64, 0.05, 1),     # d = 64 (zero-padded to the 128 tile)
+        (2, 777, 1, 2, 128, 0.02, 3),    # segments with warm-up windows
+        (1, 1024, 2, 2, 128, 0.0, 7),
+    ],
+)
+def test_chunked_small_matches_oracle(B, T, Hqk, Hv, d, s0, segments):
+    x = make_prefill_inputs(B, T, Hqk, Hv, d, "bf16", decay_scale=0.1, s0_std=s0, seed=T + d, device="cuda")
+    y, S_T = _chunked(x, segments=segments)
+    yo, So = oracle.recurrence(x.q, x.k, x.v, x.alpha, x.beta, x.S0)
+    assert rel_err(y, yo) <= BF16_TOL
+    assert rel_err(S_T, So) <= BF16_TOL
+
+
+def test_chunked_train_workload_matches_oracle():
+    # B=2, H=16, T=4096, d=128, S0 = 0: whole y and S_T, in the launch
+    # configuration the library picks.
+    x = workload_inputs("train", device="cuda")
+    y, S_T = _chunked(x)
+    yo, So = oracle.recurrence(x.q, x.k, x.v, x.alpha, x.beta, x.S0)
+    assert rel_err(y, yo) <= BF16_TOL
+    assert rel_err(S_T, So) <= BF16_TOL
+
+
+def test_chunked_grouped_workload_matches_oracle():
+    # B=1, Hqk=16, Hv=32, T=65536, d=128, S0 ~ N(0, 0.02^2): whole y and S_T.
+    x = workload_inputs("grouped", device="cuda")
+    y, S_T = _chunked(x)
+    yo, So = oracle.recurrence(x.q, x.k, x.v, x.alpha, x.beta, x.S0)
+    assert rel_err(y, yo) <= BF16_TOL
+    assert rel_err(S_T, So) <= BF16_TOL
+
+
+def _window_oracle(x, hv, t0, t1, warm):
+    """Oracle y over tokens [t0, t1) of (batch 0, value head hv) and the state
+    at t1, started from a zero state `warm` tokens before t0 (from S0 at token 0
+    if the window reaches it).  With unit keys and beta in [0, 1] every step is
+    a contraction of norm <= alpha_t, so the start-state difference is damped
+    by the product of the gates over the warm-up, far below the tolerance for
+    the warm-up lengths used here."""
+    Hqk, Hv = x.q.shape[2], x.v.shape[2]
+    hk = hv // (Hv // Hqk)
+    s = max(0, t0 - warm)
+    sl = lambda t, h: t[0:1, s:t1, h:h + 1]  # noqa: E731
+    S0 = x.S0[0:1, hv:hv + 1] if (s == 0 and x.S0 is not None) else None
+    y, St = oracle.recurrence(sl(x.q, hk), sl(x.k, hk), sl(x.v, hv), sl(x.alpha, hv), sl(x.beta, hv), S0, threads=1)
+    a = x.alpha[0, s:t0, hv].double()
+    damp = float(torch.exp(torch.log(a).sum())) if t0 > s else 0.0
+    assert s == 0 or damp < 1e-6, "warm-up too short for an exact window"
+    return y[0, t0 - s:, 0], St[0, 0]
+
+
+@pytest.mark.slow
+def test_chunked_long_workload_windows_match_oracle():
+    # B=1, H=16, T=2^20, d=128, gate scale 0.01: sampled windows of two heads
+    # (start, across segment boundaries, end) and their final states.
+    x = workload_inputs("long", device="cuda")
+    T = x.q.shape[1]
+    y, S_T = _chunked(x)
+    errs = []
+    for hv in (0, 15):
+        for t0, t1 in ((0, 4096), (T // 2 - 3000, T // 2 + 3000), (T - 4096, T)):
+            yo, So = _window_oracle(x, hv, t0, t1, warm=8192)
+            errs.append(rel_err(y[0, t0:t1, hv], yo))
+            if t1 == T:
+                errs.append(rel_err(S_T[0, hv], So))
+    assert max(errs) <= BF16_TOL, errs
+
+
+def test_chunked_segments_agree_with_single_pass():
+    x = make_prefill_inputs(1, 4096, 2, 4, 128, "bf16", decay_scale=0.05, s0_std=0.02, seed=11, device="cuda")
+    y1, S1 = _chunked(x, segments=1)
+    for P in (2, 5, 16):
+        yP, SP = _chunked(x, segments=P)
+        assert rel_err(yP, y1.double().cpu().numpy()) <= 1e-2
+        assert rel_err(SP, S1.double().cpu().numpy()) <= 1e-2
+
+
+def test_chunked_in_place_state_and_empty():
+    x = make_prefill_inputs(1, 500, 1, 2, 128, "bf16", decay_scale=0.1, s0_std=0.05, seed=12, device="cuda")
+    yo, So = oracle.recurrence(x.q, x.k, x.v, x.alpha, x.beta, x.S0)
+    S = x.S0.clone()
+    y, _ = _chunked(x, S_T=S, segments=3)
+    assert rel_err(y, yo) <= BF16_TOL
+    assert rel_err(S, So) <= BF16_TOL
+    e = make_prefill_inputs(1, 0, 1, 2, 128, "bf16", s0_std=0.05, seed=13, device="cuda")
+    y, S_T = _chunked(e)
+    assert y.numel() == 0 and torch.equal(S_T, e.S0)
+
+
+def test_chunked_identity_gates_keep_state():
+    # alpha = 1, beta = 0: S_T = S0 and y_t = S0^T q_t (up to bf16 operand rounding).
+    x = make_prefill_inputs(1, 256, 1, 2, 128, "bf16", s0_std=0.05, seed=14, device="cuda")
+    x.alpha.fill_(1.0)
+    x.beta.zero_()
+    y, S_T = _chunked(x, segments=1)
+    assert torch.equal(S_T, x.S0)
+    yo, _ = oracle.recurrence(x.q, x.k, x.v, x.alpha, x.beta, x.S0)
+    assert rel_err(y, yo) <= BF16_TOL
+
+
+def test_chunked_is_deterministic():
+    x = make_prefill_inputs(1, 3000, 2, 4, 128, "bf16", s0_std=0.02, seed=15, device="cuda")
+    y1, S1 = _chunked(x)
+    y2, S2 = _chunked(x)
+    assert torch.equal(y1, y2) and torch.equal(S1, S2)
+
+
+def test_chunked_matches_sequential_kernel_and_decode():
+    # Three independent paths of the library agree: chunked prefill,
+    # token-sequential prefill, and T decode steps.
+    x = make_prefill_inputs(2, 96, 1, 2, 128, "bf16", decay_scale=0.05, s0_std=0.02, seed=16, device="cuda")
+    yc, Sc = _chunked(x)
+    ys, Ss = gdn.prefill(x.q, x.k, x.v, x.alpha, x.beta, x.S0, algorithm=gdn.ALGO_SEQUENTIAL)
+    S = x.S0.clone()
+    tok = lambda a, t: a[:, t:t + 1].contiguous()  # noqa: E731
+    yd = torch.stack([gdn.decode_step(tok(x.q, t), tok(x.k, t), tok(x.v, t), tok(x.alpha, t), tok(x.beta, t), S)
+                      for t in range(96)], 1)[:, :, 0]
+    ref = ys.double().cpu().numpy()
+    assert rel_err(yc, ref) <= BF16_TOL
+    assert rel_err(yd, ref) <= 1e-2
+    assert rel_err(Sc, Ss.double().cpu().numpy()) <= BF16_TOL
+    assert rel_err(S, Ss.double().cpu().numpy()) <= 1e-3
