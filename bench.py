@@ -282,6 +282,9 @@ def run_ours(args, ws, rank, local):
         t_all1.record(stream)
         torch.cuda.synchronize()
     barrier(ws)
+    status = gdn.read_device_status(ws_buf)
+    if status != 0:
+        raise SystemExit(f"device status {status} in the timed region")
     per_launch_ms = [a.elapsed_time(b) for a, b in ev]
     total_ms = t_all0.elapsed_time(t_all1)
     total_ms = max_over_ranks(total_ms, ws, dev)

@@ -25,23 +25,44 @@ def _built():
 
 
 def _chunked(x, **kw):
-    return gdn.prefill(x.q, x.k, x.v, x.alpha, x.beta, x.S0, algorithm=gdn.ALGO_CHUNKED, **kw)
+    """Chunked prefill through the C ABI; also checks that no bounded device-side
+    wait timed out (the kernel records that in the workspace status word)."""
+    ws = gdn.new_workspace(gdn.shape_of(x.q, x.v), x.v.device)
+    out = gdn.prefill(x.q, x.k, x.v, x.alpha, x.beta, x.S0, algorithm=gdn.ALGO_CHUNKED, workspace=ws, **kw)
+    assert gdn.read_device_status(ws) == 0, "device-side wait timed out"
+    return out
+
+
+def test_chunked_repeated_launches_report_no_device_error():
+    # Many launches of a multi-segment shape: a scheduling hazard in the
+    # warp-specialised pipeline shows up as a timed-out bounded wait.
+    x = make_prefill_inputs(1, 8192, 2, 4, 128, "bf16", decay_scale=0.05, s0_std=0.02, seed=21, device="cuda")
+    ws = gdn.new_workspace(gdn.shape_of(x.q, x.v), "cuda")
+    y = torch.empty_like(x.v)
+    S = torch.empty_like(x.S0)
+    for P in (1, 2, 3, 9, 16):
+        for _ in range(20):
+            gdn.prefill(x.q, x.k, x.v, x.alpha, x.beta, x.S0, y=y, S_T=S, workspace=ws, algorithm=gdn.ALGO_CHUNKED,
+                        segments=P)
+        assert gdn.read_device_status(ws) == 0, f"device-side wait timed out with {P} segments"
 
 
 @pytest.mark.parametrize(
-    "B,T,Hqk,Hv,d,s0,segments",
+    "B,T,Hqk,Hv,d,s0,segments,decay",
     [
-        (1, 64, 1, 1, 128, 0.0, 1),      # one full chunk
-        (1, 1, 1, 1, 128, 0.02, 1),      # a single token
-        (1, 65, 1, 2, 128, 0.02, 1),     # ragged tail
-        (2, 200, 2, 4, 128, 0.02, 1),    # grouped heads, several chunks
-        (1, 300, 2, 2, 64, 0.05, 1),     # d = 64 (zero-padded to the 128 tile)
-        (2, 777, 1, 2, 128, 0.02, 3),    # segments with warm-up windows
-        (1, 1024, 2, 2, 128, 0.0, 7),
+        (1, 64, 1, 1, 128, 0.0, 1, 0.1),      # one full chunk
+        (1, 1, 1, 1, 128, 0.02, 1, 0.1),      # a single token
+        (1, 65, 1, 2, 128, 0.02, 1, 0.1),     # ragged tail
+        (2, 200, 2, 4, 128, 0.02, 1, 0.1),    # grouped heads, several chunks
+        (1, 300, 2, 2, 64, 0.05, 1, 0.1),     # d = 64 (zero-padded to the 128 tile)
+        (2, 777, 1, 2, 128, 0.02, 3, 0.1),    # segments with warm-up windows
+        (1, 1024, 2, 2, 128, 0.0, 7, 0.1),
+        (1, 640, 1, 2, 128, 0.02, 2, 1.5),    # strong decay: every chunk below e^-40 (exact gate path)
+        (1, 1280, 1, 2, 128, 0.02, 1, 0.6),   # chunks on both sides of the e^-40 switch
     ],
 )
-def test_chunked_small_matches_oracle(B, T, Hqk, Hv, d, s0, segments):
-    x = make_prefill_inputs(B, T, Hqk, Hv, d, "bf16", decay_scale=0.1, s0_std=s0, seed=T + d, device="cuda")
+def test_chunked_small_matches_oracle(B, T, Hqk, Hv, d, s0, segments, decay):
+    x = make_prefill_inputs(B, T, Hqk, Hv, d, "bf16", decay_scale=decay, s0_std=s0, seed=T + d, device="cuda")
     y, S_T = _chunked(x, segments=segments)
     yo, So = oracle.recurrence(x.q, x.k, x.v, x.alpha, x.beta, x.S0)
     assert rel_err(y, yo) <= BF16_TOL
