@@ -60,7 +60,7 @@ constexpr uint64_t kWaitLimitNs = 1000000000ull;  // bounded waits: 1 s
 // tiles use the 128-byte swizzle: rows of 128 bytes (64 bf16), 16-byte chunk
 // c of row r stored at chunk position c ^ (r & 7).
 constexpr uint32_t kKQBytes = 2 * 128 * 128;  // [kb][128 rows][64]: K rows 0-63, Q rows 64-127
-constexpr uint32_t kVWBytes = 2 * 64 * 128;   // [kb][64 rows][64]: V, later -W
+constexpr uint32_t kVWBytes = 2 * 64 * 128;   // [kb][64 rows][64]: V; later -W^T as [128 dk][64 tokens]
 constexpr uint32_t kPBytes = 64 * 128;        // [64 rows][64]
 constexpr uint32_t OFF_KQ = 0;
 constexpr uint32_t OFF_VW = OFF_KQ + kStages * kKQBytes;
@@ -75,8 +75,8 @@ constexpr int kBS = 24;
 constexpr int kBlk = 16 * kBS;
 constexpr uint32_t OFF_AT = OFF_T2 + 64 * 128;
 constexpr uint32_t OFF_TM = OFF_AT + 10 * kBlk * 4;
-constexpr uint32_t OFF_R = OFF_TM + 10 * kBlk * 4;      // 3 warps x [16][kBS]
-constexpr uint32_t OFF_GATES = OFF_R + 3 * kBlk * 4;
+constexpr uint32_t OFF_R = OFF_TM + 10 * kBlk * 4;      // 4 warps x [16][kBS]
+constexpr uint32_t OFF_GATES = OFF_R + 4 * kBlk * 4;
 // gates, double-buffered by chunk parity: g, u = gamma, w = 1/gamma, beta,
 // beta gamma (64 floats each), misc (64)
 constexpr int kGateFloats = 6 * 64;
@@ -138,8 +138,8 @@ struct Dev {
     uint32_t *status;
 };
 
-__device__ __forceinline__ bool bwait(uint64_t *bar, uint32_t parity, volatile int *abort, uint32_t *status) {
-    if (mbar_try_wait(bar, parity)) return true;
+// Slow path of a bounded wait (out of line: one copy for every call site).
+__device__ __noinline__ bool bwait_slow(uint64_t *bar, uint32_t parity, volatile int *abort, uint32_t *status) {
     const uint64_t t0 = globaltimer_ns();
     for (;;) {
         if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
@@ -150,6 +150,11 @@ __device__ __forceinline__ bool bwait(uint64_t *bar, uint32_t parity, volatile i
             return false;
         }
     }
+}
+
+__device__ __forceinline__ bool bwait(uint64_t *bar, uint32_t parity, volatile int *abort, uint32_t *status) {
+    if (mbar_try_wait(bar, parity)) return true;
+    return bwait_slow(bar, parity, abort, status);
 }
 
 // Bounded wait that ignores the abort flag (teardown).
@@ -205,51 +210,125 @@ __device__ __forceinline__ float warp_sum(float v) {
     return v;
 }
 
+// One warp: C (+)= X W for 16 x 16 row-major fp32 blocks (row stride kBS) with
+// tf32 m16n8k8 MMAs; c[nt] holds the C fragment of columns 8 nt .. 8 nt + 7.
+__device__ __forceinline__ void mm16(float (&c)[2][4], const float *X, const float *W, int gq, int t4) {
+#pragma unroll
+    for (int ks = 0; ks < 2; ++ks) {
+        const int k0 = 8 * ks;
+        const uint32_t a0 = __float_as_uint(X[gq * kBS + k0 + t4]);
+        const uint32_t a1 = __float_as_uint(X[(gq + 8) * kBS + k0 + t4]);
+        const uint32_t a2 = __float_as_uint(X[gq * kBS + k0 + t4 + 4]);
+        const uint32_t a3 = __float_as_uint(X[(gq + 8) * kBS + k0 + t4 + 4]);
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+            mma_tf32(c[nt], a0, a1, a2, a3, __float_as_uint(W[(k0 + t4) * kBS + 8 * nt + gq]),
+                     __float_as_uint(W[(k0 + t4 + 4) * kBS + 8 * nt + gq]));
+    }
+}
+
+__device__ __forceinline__ void load_cfrag(float (&c)[2][4], const float *M, int gq, int t4) {
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+        const float2 lo = *reinterpret_cast<const float2 *>(M + gq * kBS + 8 * nt + 2 * t4);
+        const float2 hi = *reinterpret_cast<const float2 *>(M + (gq + 8) * kBS + 8 * nt + 2 * t4);
+        c[nt][0] = lo.x; c[nt][1] = lo.y; c[nt][2] = hi.x; c[nt][3] = hi.y;
+    }
+}
+
+__device__ __forceinline__ void store_cfrag(float *M, const float (&c)[2][4], int gq, int t4) {
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+        *reinterpret_cast<float2 *>(M + gq * kBS + 8 * nt + 2 * t4) = make_float2(c[nt][0], c[nt][1]);
+        *reinterpret_cast<float2 *>(M + (gq + 8) * kBS + 8 * nt + 2 * t4) = make_float2(c[nt][2], c[nt][3]);
+    }
+}
+
+// Inverse of a 16 x 16 unit lower-triangular block I + N (one warp), N the
+// strictly lower part of A's diagonal block (column-major within the block,
+// entries on and above the diagonal are not read).  N is nilpotent (N^16 = 0),
+// so (I + N)^{-1} = (I + Z)(I + Z^2)(I + Z^4)(I + Z^8) exactly, Z = -N: four
+// dependent steps of 16 x 16 products.  Writes the inverse row-major to Y;
+// Zb is a scratch block.
+__device__ __forceinline__ void invert_diag_block(const float *Ablk, float *Y, float *Zb, int lane) {
+    const int gq = lane >> 2, t4 = lane & 3;
+    {
+        // Zb = -N, Y = I - N (row r = lane / 2, columns 8 (lane & 1) .. + 7)
+        const int r = lane >> 1, c0 = 8 * (lane & 1);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const int c = c0 + e;
+            const float z = r > c ? -Ablk[c * kBS + r] : 0.f;
+            Zb[r * kBS + c] = z;
+            Y[r * kBS + c] = z + (r == c ? 1.f : 0.f);
+        }
+    }
+    __syncwarp();
+#pragma unroll 1
+    for (int step = 0; step < 4; ++step) {
+        // step 0: Z <- Z^2.  steps 1, 2: Y <- Y + Y Z, Z <- Z^2.  step 3: Y <- Y + Y Z.
+        float yz[2][4], zz[2][4];
+        if (step > 0) {
+            load_cfrag(yz, Y, gq, t4);
+            mm16(yz, Y, Zb, gq, t4);
+        }
+        if (step < 3) {
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) zz[nt][e] = 0.f;
+            mm16(zz, Zb, Zb, gq, t4);
+        }
+        __syncwarp();
+        if (step > 0) store_cfrag(Y, yz, gq, t4);
+        if (step < 3) store_cfrag(Zb, zz, gq, t4);
+        __syncwarp();
+    }
+}
+
 // Off-diagonal blocks of block column J of T = (I + A)^{-1} (one warp):
 // T_IJ = -T_II R, R = sum_{K=J}^{I-1} A_IK T_KJ, for I = J+1..3, with tf32 warp
 // MMAs (m16n8k8, fp32 accumulation; fp32 operands are passed as is, the
 // tensor core reads their tf32 part).  Writes T_IJ as fp32 (row-major block)
-// and as bf16 T1 = T diag(beta gamma), T2 = T diag(beta).
-template <int J>
-__device__ __forceinline__ void merge_column(const float *At, float *Tm, float *Rw, uint8_t *t1b, uint8_t *t2b,
-                                             const float *s_b, const float *s_bu, int lane) {
+// and as bf16 T1 = T diag(beta gamma), T2 = T diag(beta).  Loops are kept
+// rolled: the kernel's hot code has to fit the instruction cache.
+__device__ __forceinline__ void merge_column(int J, const float *At, float *Tm, float *Rw, uint8_t *t1b,
+                                             uint8_t *t2b, const float *s_b, const float *s_bu, int lane) {
     const int gq = lane >> 2, t4 = lane & 3;
-#pragma unroll
+#pragma unroll 1
     for (int I = J + 1; I < 4; ++I) {
-        float acc[3][2][4];
-#pragma unroll
-        for (int K = 0; K < 3; ++K)
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) acc[K][nt][e] = 0.f;
-#pragma unroll
+        float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
+        float e0[4] = {0.f, 0.f, 0.f, 0.f}, e1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 1
         for (int K = J; K < I; ++K) {
             const float *Ab = At + (I * (I + 1) / 2 + K) * kBlk;   // A[r][k] at k*kBS + r
             const float *Bb = Tm + (K * (K + 1) / 2 + J) * kBlk;   // T[k][n] at k*kBS + n
+            // k-steps 0 and 1 into separate accumulators: two independent MMA chains
+            uint32_t a[2][4], b[2][2][2];
 #pragma unroll
             for (int ks = 0; ks < 2; ++ks) {
                 const int k0 = 8 * ks;
-                const uint32_t a0 = __float_as_uint(Ab[(k0 + t4) * kBS + gq]);
-                const uint32_t a1 = __float_as_uint(Ab[(k0 + t4) * kBS + gq + 8]);
-                const uint32_t a2 = __float_as_uint(Ab[(k0 + t4 + 4) * kBS + gq]);
-                const uint32_t a3 = __float_as_uint(Ab[(k0 + t4 + 4) * kBS + gq + 8]);
+                a[ks][0] = __float_as_uint(Ab[(k0 + t4) * kBS + gq]);
+                a[ks][1] = __float_as_uint(Ab[(k0 + t4) * kBS + gq + 8]);
+                a[ks][2] = __float_as_uint(Ab[(k0 + t4 + 4) * kBS + gq]);
+                a[ks][3] = __float_as_uint(Ab[(k0 + t4 + 4) * kBS + gq + 8]);
 #pragma unroll
-                for (int nt = 0; nt < 2; ++nt)
-                    mma_tf32(acc[K - J][nt], a0, a1, a2, a3, __float_as_uint(Bb[(k0 + t4) * kBS + 8 * nt + gq]),
-                             __float_as_uint(Bb[(k0 + t4 + 4) * kBS + 8 * nt + gq]));
+                for (int nt = 0; nt < 2; ++nt) {
+                    b[ks][nt][0] = __float_as_uint(Bb[(k0 + t4) * kBS + 8 * nt + gq]);
+                    b[ks][nt][1] = __float_as_uint(Bb[(k0 + t4 + 4) * kBS + 8 * nt + gq]);
+                }
             }
+            mma_tf32(c0, a[0][0], a[0][1], a[0][2], a[0][3], b[0][0][0], b[0][0][1]);
+            mma_tf32(c1, a[0][0], a[0][1], a[0][2], a[0][3], b[0][1][0], b[0][1][1]);
+            mma_tf32(e0, a[1][0], a[1][1], a[1][2], a[1][3], b[1][0][0], b[1][0][1]);
+            mma_tf32(e1, a[1][0], a[1][1], a[1][2], a[1][3], b[1][1][0], b[1][1][1]);
         }
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
-            float c[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) c[e] = acc[0][nt][e] + acc[1][nt][e] + acc[2][nt][e];
-            *reinterpret_cast<float2 *>(Rw + gq * kBS + 8 * nt + 2 * t4) = make_float2(c[0], c[1]);
-            *reinterpret_cast<float2 *>(Rw + (gq + 8) * kBS + 8 * nt + 2 * t4) = make_float2(c[2], c[3]);
-        }
+        *reinterpret_cast<float2 *>(Rw + gq * kBS + 2 * t4) = make_float2(c0[0] + e0[0], c0[1] + e0[1]);
+        *reinterpret_cast<float2 *>(Rw + (gq + 8) * kBS + 2 * t4) = make_float2(c0[2] + e0[2], c0[3] + e0[3]);
+        *reinterpret_cast<float2 *>(Rw + gq * kBS + 8 + 2 * t4) = make_float2(c1[0] + e1[0], c1[1] + e1[1]);
+        *reinterpret_cast<float2 *>(Rw + (gq + 8) * kBS + 8 + 2 * t4) = make_float2(c1[2] + e1[2], c1[3] + e1[3]);
         __syncwarp();
-        float d[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+        float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
         const float *Td = Tm + (I * (I + 1) / 2 + I) * kBlk;       // T[r][k] at r*kBS + k
 #pragma unroll
         for (int ks = 0; ks < 2; ++ks) {
@@ -258,21 +337,22 @@ __device__ __forceinline__ void merge_column(const float *At, float *Tm, float *
             const uint32_t a1 = __float_as_uint(Td[(gq + 8) * kBS + k0 + t4]);
             const uint32_t a2 = __float_as_uint(Td[gq * kBS + k0 + t4 + 4]);
             const uint32_t a3 = __float_as_uint(Td[(gq + 8) * kBS + k0 + t4 + 4]);
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt)
-                mma_tf32(d[nt], a0, a1, a2, a3, __float_as_uint(Rw[(k0 + t4) * kBS + 8 * nt + gq]),
-                         __float_as_uint(Rw[(k0 + t4 + 4) * kBS + 8 * nt + gq]));
+            mma_tf32(d0, a0, a1, a2, a3, __float_as_uint(Rw[(k0 + t4) * kBS + gq]),
+                     __float_as_uint(Rw[(k0 + t4 + 4) * kBS + gq]));
+            mma_tf32(d1, a0, a1, a2, a3, __float_as_uint(Rw[(k0 + t4) * kBS + 8 + gq]),
+                     __float_as_uint(Rw[(k0 + t4 + 4) * kBS + 8 + gq]));
         }
         float *Tb = Tm + (I * (I + 1) / 2 + J) * kBlk;
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt) {
+            const float *dd = nt ? d1 : d0;
             const int cn = 8 * nt + 2 * t4;
             const int C = 16 * J + cn;
             const float sa0 = s_bu[C], sa1 = s_bu[C + 1], sb0 = s_b[C], sb1 = s_b[C + 1];
 #pragma unroll
             for (int hr = 0; hr < 2; ++hr) {
                 const int r = gq + 8 * hr;
-                const float v0 = -d[nt][2 * hr], v1 = -d[nt][2 * hr + 1];
+                const float v0 = -dd[2 * hr], v1 = -dd[2 * hr + 1];
                 *reinterpret_cast<float2 *>(Tb + r * kBS + cn) = make_float2(v0, v1);
                 const uint32_t off = sw128_elem(16 * I + r, C);
                 *reinterpret_cast<uint32_t *>(t1b + off) = pack_bf16(v0 * sa0, v1 * sa1);
@@ -284,9 +364,9 @@ __device__ __forceinline__ void merge_column(const float *At, float *Tm, float *
 }
 
 // bf16 T1, T2 of the four diagonal blocks from their fp32 copies (one warp).
-__device__ __forceinline__ void diag_to_bf16(const float *Tm, uint8_t *t1b, uint8_t *t2b, const float *s_b,
-                                             const float *s_bu, int lane) {
-#pragma unroll
+__device__ __noinline__ void diag_to_bf16(const float *Tm, uint8_t *t1b, uint8_t *t2b, const float *s_b,
+                                          const float *s_bu, int lane) {
+#pragma unroll 4
     for (int u = 0; u < 16; ++u) {
         const int e = lane + 32 * u;             // 512 column pairs
         const int blk = e >> 7, r = (e >> 3) & 15, cp = e & 7;
@@ -295,6 +375,110 @@ __device__ __forceinline__ void diag_to_bf16(const float *Tm, uint8_t *t1b, uint
         const uint32_t off = sw128_elem(16 * blk + r, C);
         *reinterpret_cast<uint32_t *>(t1b + off) = pack_bf16(v.x * s_bu[C], v.y * s_bu[C + 1]);
         *reinterpret_cast<uint32_t *>(t2b + off) = pack_bf16(v.x * s_b[C], v.y * s_b[C + 1]);
+    }
+}
+
+// nk consecutive K=16 MMAs of one product.  Operand offsets advance as
+// (kk >> shift) * big + (kk & ((1 << shift) - 1)) * small bytes (TMEM A: columns);
+// a start address inside a descriptor moves by adding offset >> 4.
+struct MmaOperand {
+    uint64_t desc;      // shared-memory descriptor (unused for a TMEM A operand)
+    uint32_t tmem;      // TMEM address of A (0: A from shared memory)
+    uint32_t big, small, shift;
+};
+
+__device__ __forceinline__ uint32_t operand_offset(const MmaOperand &o, uint32_t kk) {
+    return (kk >> o.shift) * o.big + (kk & ((1u << o.shift) - 1u)) * o.small;
+}
+
+__device__ __noinline__ void mma_run(uint32_t d, MmaOperand a, MmaOperand b, uint32_t idesc, int nk, uint32_t acc) {
+#pragma unroll 1
+    for (int kk = 0; kk < nk; ++kk) {
+        const uint64_t bd = b.desc + (operand_offset(b, kk) >> 4);
+        const uint32_t accumulate = acc | (kk > 0 ? 1u : 0u);
+        if (a.tmem)
+            mma_bf16_ts(d, a.tmem + operand_offset(a, kk), bd, idesc, accumulate);
+        else
+            mma_bf16(d, a.desc + (operand_offset(a, kk) >> 4), bd, idesc, accumulate);
+    }
+}
+
+// Exact gate path (a chunk whose decay is below e^kFastLogDecay): per-element
+// e^{g_i - g_j} for A and P, and Q~ = diag(gamma) Q in place.  Cold code.
+__device__ __noinline__ void exact_gram_rows(int j, int l, uint32_t q, uint32_t gw, float *At, uint8_t *pbuf,
+                                             uint8_t *kq, const float *s_g, const float *s_u, const float *s_b) {
+    (void)j;
+#pragma unroll 1
+    for (int half = 0; half < 2; ++half) {
+        float gr[32];
+        tmem_ld32(lane_addr(gw, q, 32 * half), gr);
+        tmem_wait_ld();
+        if (l < 64) {
+            const int i = l;
+            const float bi = s_b[i], gi = s_g[i];
+            float *abase = At + (kBlkIdx[i >> 4][0] + 2 * half) * kBlk + (i & 15);
+#pragma unroll
+            for (int cc = 0; cc < 32; ++cc) {
+                const int c = 32 * half + cc;
+                if (c < i) abase[(cc >> 4) * kBlk + (cc & 15) * kBS] = bi * expf(gi - s_g[c]) * gr[cc];
+            }
+        } else {
+            const int i = l - 64;
+            const float gi = s_g[i];
+            uint8_t *prow = pbuf + i * 128;
+#pragma unroll
+            for (int ch4 = 0; ch4 < 4; ++ch4) {
+                uint32_t w4[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int cc = 8 * ch4 + 2 * e, c = 32 * half + cc;
+                    w4[e] = pack_bf16(c <= i ? expf(gi - s_g[c]) * gr[cc] : 0.f,
+                                      c + 1 <= i ? expf(gi - s_g[c + 1]) * gr[cc + 1] : 0.f);
+                }
+                *reinterpret_cast<uint4 *>(prow + (((4 * half + ch4) ^ (i & 7)) << 4)) =
+                    make_uint4(w4[0], w4[1], w4[2], w4[3]);
+            }
+        }
+    }
+    if (l >= 64) {
+        const int i = l - 64;
+        const float gam = s_u[i];
+        uint8_t *qrow = kq + (64 + i) * 128;
+#pragma unroll 1
+        for (int kb = 0; kb < 2; ++kb) {
+#pragma unroll
+            for (int ch = 0; ch < 8; ++ch) {
+                uint4 *ptr = reinterpret_cast<uint4 *>(qrow + kb * 16384 + ch * 16);
+                uint4 raw = *ptr;
+                __nv_bfloat162 *h2 = reinterpret_cast<__nv_bfloat162 *>(&raw);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float2 f = __bfloat1622float2(h2[e]);
+                    h2[e] = __floats2bfloat162_rn(f.x * gam, f.y * gam);
+                }
+                *ptr = raw;
+            }
+        }
+    }
+}
+
+// Exact gate path: K~ = diag(lambda) K in place, lambda_r = e^{g_C - g_r}.  Cold code.
+__device__ __noinline__ void exact_scale_k(int l, uint8_t *kq, const float *s_g) {
+    const float g63 = s_g[63];
+#pragma unroll 1
+    for (int u = 0; u < 8; ++u) {
+        const int idx = l + 128 * u;
+        const int kb = idx >> 9, r = (idx >> 3) & 63, ch = idx & 7;
+        uint4 *ptr = reinterpret_cast<uint4 *>(kq + kb * 16384 + r * 128 + ch * 16);
+        const float lam = expf(g63 - s_g[r]);
+        uint4 raw = *ptr;
+        __nv_bfloat162 *h2 = reinterpret_cast<__nv_bfloat162 *>(&raw);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float2 f = __bfloat1622float2(h2[e]);
+            h2[e] = __floats2bfloat162_rn(f.x * lam, f.y * lam);
+        }
+        *ptr = raw;
     }
 }
 
@@ -442,28 +626,24 @@ __global__ void __launch_bounds__(kThreads, 1)
             constexpr uint32_t ID_MK = idesc_bf16(128, 64, true, false);    // A MN-major
             constexpr uint32_t ID_TS = idesc_bf16(128, 64, false, false);   // A in TMEM, B K-major
             constexpr uint32_t ID_TD = idesc_bf16(128, 128, false, true);   // A in TMEM, B MN-major
+            constexpr uint32_t ID_TSM = idesc_bf16(128, 64, false, true);   // A in TMEM, B MN-major, N = 64
             const uint32_t t1 = smb + OFF_T1, t2 = smb + OFF_T2;
+            // K-major tiles split in two 64-column sub-tiles (16 KB apart for [K;Q]);
+            // MN-major tiles advance 2048 bytes (16 rows) per K step.
+            auto smem_kmajor = [](uint32_t addr, uint32_t subtile) {
+                return MmaOperand{sw128_desc(addr, 16, 1024), 0u, subtile, 32u, 2u};
+            };
+            auto smem_mnmajor = [](uint32_t addr, uint32_t lbo) {
+                return MmaOperand{sw128_desc(addr, lbo, 1024), 0u, 8192u, 2048u, 2u};
+            };
             auto gram = [&](int j) {
-                const uint32_t base = kq_addr(j % kStages);
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {
-                    const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-                    const uint64_t d = sw128_desc(base + off, 16, 1024);
-                    mma_bf16(tb + TM_GW + (j & 1) * 64, d, d, ID_KK, kk > 0);
-                }
+                const MmaOperand kq = smem_kmajor(kq_addr(j % kStages), 16384u);
+                mma_run(tb + TM_GW + (j & 1) * 64, kq, kq, ID_KK, 8, 0u);
             };
             auto wu = [&](int j) {
                 const int s = j % kStages;
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk) {
-                    const uint64_t a = sw128_desc(kq_addr(s) + kk * 2048, 16384, 1024);
-                    mma_bf16(tb + TM_GW + (j & 1) * 64, a, sw128_desc(t1 + kk * 32, 16, 1024), ID_MK, kk > 0);
-                }
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk) {
-                    const uint64_t a = sw128_desc(vw_addr(s) + kk * 2048, 8192, 1024);
-                    mma_bf16(tb + TM_ZU, a, sw128_desc(t2 + kk * 32, 16, 1024), ID_MK, kk > 0);
-                }
+                mma_run(tb + TM_GW + (j & 1) * 64, smem_mnmajor(kq_addr(s), 16384u), smem_kmajor(t1, 0u), ID_MK, 4, 0u);
+                mma_run(tb + TM_ZU, smem_mnmajor(vw_addr(s), 8192u), smem_kmajor(t2, 0u), ID_MK, 4, 0u);
             };
             bool ok = true;
             do {
@@ -488,12 +668,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (!(ok = bwait(&bars[B_OPS], j & 1, abort_flag, p.status))) break;
                     if (!(ok = bwait(&bars[B_SREADY], j & 1, abort_flag, p.status))) break;
                     tc_fence_after();
-                    // U^T = U~^T + S^T (-W)^T
-#pragma unroll
-                    for (int kk = 0; kk < 8; ++kk) {
-                        const uint64_t bd = sw128_desc(vw_addr(s) + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024);
-                        mma_bf16_ts(zu, sb + kk * 8, bd, ID_TS, 1);
-                    }
+                    // U^T = U~^T + S^T (-W)^T   (-W^T stored [dk][tokens], MN-major)
+                    const MmaOperand sa{0ull, sb, 0u, 8u, 3u};          // S^T bf16: 8 columns per K step
+                    const MmaOperand ua{0ull, zu, 32u, 8u, 1u};         // U^T bf16: tokens 0-31 at 0-15, 32-63 at 32-47
+                    mma_run(zu, sa, smem_mnmajor(vw_addr(s), 16u), ID_TSM, 8, 1u);
                     mma_commit(&bars[B_UFULL]);
                     // Gram of chunk j+2 into the GW buffer W^T(j) occupied (read before
                     // OPS(j)); it runs while the chain converts U^T, before MMA2 is issued.
@@ -506,27 +684,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     if (!(ok = bwait(&bars[B_USMEM], j & 1, abort_flag, p.status))) break;
                     tc_fence_after();
-                    // dS^T = U^T K~   (U^T bf16: tokens 0-31 at columns 0-15, 32-63 at 32-47)
-#pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) {
-                        const uint64_t bd = sw128_desc(kq_addr(s) + kk * 2048, 16384, 1024);
-                        mma_bf16_ts(tb + TM_D, zu + kk * 8 + (kk >= 2 ? 16 : 0), bd, ID_TD, kk > 0);
-                    }
+                    // dS^T = U^T K~
+                    mma_run(tb + TM_D, ua, smem_mnmajor(kq_addr(s), 16384u), ID_TD, 4, 0u);
                     mma_commit(&bars[B_DFULL]);
                     if (j > 0 && !(ok = bwait(&bars[B_YFREE], (j - 1) & 1, abort_flag, p.status))) break;
                     tc_fence_after();
                     // Y^T = S^T Q~^T + U^T P^T
-#pragma unroll
-                    for (int kk = 0; kk < 8; ++kk) {
-                        const uint64_t bd =
-                            sw128_desc(kq_addr(s) + (kk >> 2) * 16384 + 8192 + (kk & 3) * 32, 16, 1024);
-                        mma_bf16_ts(tb + TM_Y, sb + kk * 8, bd, ID_TS, kk > 0);
-                    }
-#pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) {
-                        const uint64_t bd = sw128_desc(p_addr(s) + kk * 32, 16, 1024);
-                        mma_bf16_ts(tb + TM_Y, zu + kk * 8 + (kk >= 2 ? 16 : 0), bd, ID_TS, 1);
-                    }
+                    mma_run(tb + TM_Y, sa, smem_kmajor(kq_addr(s) + 8192, 16384u), ID_TS, 8, 0u);
+                    mma_run(tb + TM_Y, ua, smem_kmajor(p_addr(s), 0u), ID_TS, 4, 1u);
                     mma_commit(&bars[B_YFULL]);
                     mma_commit(&bars[B_EMPTY + s]);
                     if (j + 1 < n) {
@@ -621,18 +786,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!warp_ok(ok)) return false;
             const bool fast = s_misc[2] != 0.f;
             tc_fence_after();
-#pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                float gr[32];
-                tmem_ld32(lane_addr(tb + TM_GW + (j & 1) * 64, q, 32 * half), gr);
-                tmem_wait_ld();
-                if (l < 64) {
-                    // A row i = l (beta_i e^{g_i - g_j} k_i.k_j, j < i) into the block-packed,
-                    // column-major-within-block layout: A[i][j] at blk(i/16, j/16) + (j%16)*kBS + i%16.
-                    const int i = l, bi = i >> 4;
-                    float *abase = At + kBlkIdx[bi][0] * kBlk + (i & 15);
-                    if (fast) {
-                        // all loads of the half first: the stores below may alias them
+            if (fast) {
+#pragma unroll 1
+                for (int half = 0; half < 2; ++half) {
+                    float gr[32];
+                    tmem_ld32(lane_addr(tb + TM_GW + (j & 1) * 64, q, 32 * half), gr);
+                    tmem_wait_ld();
+                    if (l < 64) {
+                        // A row i = l: beta_i gamma_i w_j (k_i.k_j), j < i, into the block-packed
+                        // layout (A[i][j] at blk(i/16, j/16) + (j%16)*kBS + i%16); loads before stores.
+                        const int i = l;
+                        float *abase = At + (kBlkIdx[i >> 4][0] + 2 * half) * kBlk + (i & 15);
                         const float ci = s_bu[i];
                         float wv[32];
 #pragma unroll
@@ -643,118 +807,54 @@ __global__ void __launch_bounds__(kThreads, 1)
                             wv[4 * c4 + 2] = f.z * ci;
                             wv[4 * c4 + 3] = f.w * ci;
                         }
+                        const int lim = i - 32 * half;
 #pragma unroll
-                        for (int cc = 0; cc < 32; ++cc) {
-                            const int c = 32 * half + cc;
-                            if (c < i) abase[(c >> 4) * kBlk + (c & 15) * kBS] = gr[cc] * wv[cc];
-                        }
+                        for (int cc = 0; cc < 32; ++cc)
+                            if (cc < lim) abase[(cc >> 4) * kBlk + (cc & 15) * kBS] = gr[cc] * wv[cc];
                     } else {
-                        const float bi_ = s_b[i], gi = s_g[i];
-#pragma unroll
-                        for (int cc = 0; cc < 32; ++cc) {
-                            const int c = 32 * half + cc;
-                            if (c < i) abase[(c >> 4) * kBlk + (c & 15) * kBS] = bi_ * expf(gi - s_g[c]) * gr[cc];
-                        }
-                    }
-                } else {
-                    // P row i = l - 64, bf16: fast path (q_i.k_j) / gamma_C (the gates are
-                    // applied to U and y by the chain), else e^{g_i - g_j} (q_i.k_j).
-                    const int i = l - 64;
-                    uint8_t *prow = sm + OFF_P + s * kPBytes + i * 128;
-                    float v[32];
-                    if (fast) {
+                        // P row i = l - 64, bf16: (q_i.k_j) / gamma_C for j <= i (the gates
+                        // are applied to U and y by the chain).
+                        const int i = l - 64;
                         const float pinv = s_misc[1];
+                        const int lim = i - 32 * half;
+                        uint8_t *prow = sm + OFF_P + s * kPBytes + i * 128;
 #pragma unroll
-                        for (int cc = 0; cc < 32; ++cc) v[cc] = (32 * half + cc <= i) ? gr[cc] * pinv : 0.f;
-                    } else {
-                        const float gi = s_g[i];
+                        for (int ch4 = 0; ch4 < 4; ++ch4) {
+                            uint32_t w4[4];
 #pragma unroll
-                        for (int cc = 0; cc < 32; ++cc) {
-                            const int c = 32 * half + cc;
-                            v[cc] = c <= i ? expf(gi - s_g[c]) * gr[cc] : 0.f;
+                            for (int e = 0; e < 4; ++e) {
+                                const int cc = 8 * ch4 + 2 * e;
+                                w4[e] = pack_bf16(cc <= lim ? gr[cc] * pinv : 0.f, cc + 1 <= lim ? gr[cc + 1] * pinv : 0.f);
+                            }
+                            *reinterpret_cast<uint4 *>(prow + (((4 * half + ch4) ^ (i & 7)) << 4)) =
+                                make_uint4(w4[0], w4[1], w4[2], w4[3]);
                         }
-                    }
-#pragma unroll
-                    for (int ch4 = 0; ch4 < 4; ++ch4) {
-                        const int ch = 4 * half + ch4;
-                        *reinterpret_cast<uint4 *>(prow + ((ch ^ (i & 7)) << 4)) =
-                            make_uint4(pack_bf16(v[8 * ch4], v[8 * ch4 + 1]), pack_bf16(v[8 * ch4 + 2], v[8 * ch4 + 3]),
-                                       pack_bf16(v[8 * ch4 + 4], v[8 * ch4 + 5]),
-                                       pack_bf16(v[8 * ch4 + 6], v[8 * ch4 + 7]));
                     }
                 }
+            } else {
+                exact_gram_rows(j, l, q, tb + TM_GW + (j & 1) * 64, At, sm + OFF_P + s * kPBytes,
+                                sm + OFF_KQ + s * kKQBytes, s_g, s_u, s_b);
             }
             tc_fence_before();
-            if (l < 64) {
-                // Diagonal blocks of T = (I + A)^{-1} by forward substitution, one
-                // column per thread; this warp wrote both blocks' rows.
-                __syncwarp();
-                const int blk = l >> 4, col = l & 15;
-                const float *Ab = At + kBlkIdx[blk][blk] * kBlk;
-                float t[16];
-#pragma unroll
-                for (int r = 0; r < 16; ++r) t[r] = (r == col) ? 1.f : 0.f;
-#pragma unroll
-                for (int mb = 0; mb < 2; ++mb) {
-                    constexpr int kSplit = 5;   // columns 0-4 hold 65 values, 5-14 hold 55
-                    float av[65];
-                    const int m0 = mb ? kSplit : 0, m1 = mb ? 15 : kSplit;
-#pragma unroll
-                    for (int m = m0; m < m1; ++m)
-#pragma unroll
-                        for (int r = m + 1; r < 16; ++r)
-                            av[(m * 16 - (m * (m + 1)) / 2 + (r - m - 1)) - (m0 * 16 - (m0 * (m0 + 1)) / 2)] =
-                                Ab[m * kBS + r];
-#pragma unroll
-                    for (int m = m0; m < m1; ++m)
-#pragma unroll
-                        for (int r = m + 1; r < 16; ++r)
-                            t[r] = fmaf(-av[(m * 16 - (m * (m + 1)) / 2 + (r - m - 1)) - (m0 * 16 - (m0 * (m0 + 1)) / 2)],
-                                        t[m], t[r]);
-                }
-                float *Tb = Tm + kBlkIdx[blk][blk] * kBlk + col;
-#pragma unroll
-                for (int r = 0; r < 16; ++r) Tb[r * kBS] = t[r];
-            } else if (!fast) {
-                // Q~ = diag(gamma) Q in place (exact path)
-                const int i = l - 64;
-                const float gam = s_u[i];
-                uint8_t *qrow = sm + OFF_KQ + s * kKQBytes + (64 + i) * 128;
-#pragma unroll
-                for (int kb = 0; kb < 2; ++kb) {
-#pragma unroll
-                    for (int ch = 0; ch < 8; ++ch) {
-                        uint4 *ptr = reinterpret_cast<uint4 *>(qrow + kb * 16384 + ch * 16);
-                        uint4 raw = *ptr;
-                        __nv_bfloat162 *h2 = reinterpret_cast<__nv_bfloat162 *>(&raw);
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const float2 f = __bfloat1622float2(h2[e]);
-                            h2[e] = __floats2bfloat162_rn(f.x * gam, f.y * gam);
-                        }
-                        *ptr = raw;
-                    }
-                }
-            }
+            named_bar(1, 128);   // all rows of A written
+            // Diagonal block lw of T = (I + A)^{-1}, one block per warp.
+            invert_diag_block(At + kBlkIdx[lw][lw] * kBlk, Tm + kBlkIdx[lw][lw] * kBlk, Rw, lane);
             return true;
         };
 
-        if (ap(0)) {
-            for (int j = 0; j < n; ++j) {
+        // AP(j) of the next chunk runs between chunk j's merges and its W readout.
+#pragma unroll 1
+        for (int j = -1; j < n; ++j) {
+            if (j >= 0) {
                 const int s = j % kStages;
                 const int gbuf = j & 1;
                 const float *sg = reinterpret_cast<const float *>(sm + OFF_GATES) + gbuf * kGateFloats;
                 const float *s_g = sg, *s_b = sg + 192, *s_bu = sg + 256, *s_misc = sg + 320;
                 const bool fast = s_misc[2] != 0.f;
                 named_bar(1, 128);   // A, diagonal T blocks and P of chunk j are written
-                // Off-diagonal blocks T_IJ = -T_II sum_{K=J}^{I-1} A_IK T_KJ (warp J of 0-2),
-                // and the bf16 T1 = T diag(beta gamma), T2 = T diag(beta) of the diagonal blocks (warp 3).
-                if (lw == 0)
-                    merge_column<0>(At, Tm, Rw, t1b, t2b, s_b, s_bu, lane);
-                else if (lw == 1)
-                    merge_column<1>(At, Tm, Rw, t1b, t2b, s_b, s_bu, lane);
-                else if (lw == 2)
-                    merge_column<2>(At, Tm, Rw, t1b, t2b, s_b, s_bu, lane);
+                // Off-diagonal blocks T_IJ (warp J of 0-2), bf16 T1, T2 of the diagonal blocks (warp 3).
+                if (lw < 3)
+                    merge_column(lw, At, Tm, Rw, t1b, t2b, s_b, s_bu, lane);
                 else
                     diag_to_bf16(Tm, t1b, t2b, s_b, s_bu, lane);
                 fence_proxy_async();
@@ -766,43 +866,30 @@ __global__ void __launch_bounds__(kThreads, 1)
                 bool ok = bwait(&bars[B_WU], j & 1, abort_flag, p.status);
                 if (!warp_ok(ok)) break;
                 tc_fence_after();
-#pragma unroll
+                // -W^T row l (key index l, 64 tokens) as one swizzled 128-byte row of the
+                // MN-major operand [dk][tokens]
+                uint8_t *wrow = sm + OFF_VW + s * kVWBytes + l * 128;
+#pragma unroll 1
                 for (int half = 0; half < 2; ++half) {
                     float w[32];
                     tmem_ld32(lane_addr(tb + TM_GW + (j & 1) * 64, q, 32 * half), w);
                     tmem_wait_ld();
-                    const int kb = l >> 6, col = l & 63;
-                    uint8_t *base = sm + OFF_VW + s * kVWBytes + kb * 8192 + (col & 7) * 2;
 #pragma unroll
-                    for (int ii = 0; ii < 32; ++ii) {
-                        const int i = 32 * half + ii;
-                        *reinterpret_cast<__nv_bfloat16 *>(base + i * 128 + (((col >> 3) ^ (i & 7)) << 4)) =
-                            __float2bfloat16_rn(-w[ii]);
+                    for (int c4 = 0; c4 < 4; ++c4) {
+                        const int ch = 4 * half + c4;
+                        *reinterpret_cast<uint4 *>(wrow + ((ch ^ (l & 7)) << 4)) =
+                            make_uint4(pack_bf16(-w[8 * c4], -w[8 * c4 + 1]), pack_bf16(-w[8 * c4 + 2], -w[8 * c4 + 3]),
+                                       pack_bf16(-w[8 * c4 + 4], -w[8 * c4 + 5]),
+                                       pack_bf16(-w[8 * c4 + 6], -w[8 * c4 + 7]));
                     }
                 }
-                if (!fast) {
-                    const float g63 = s_g[63];
-#pragma unroll
-                    for (int u = 0; u < 8; ++u) {
-                        const int idx = l + 128 * u;
-                        const int kb = idx >> 9, r = (idx >> 3) & 63, ch = idx & 7;
-                        uint4 *ptr =
-                            reinterpret_cast<uint4 *>(sm + OFF_KQ + s * kKQBytes + kb * 16384 + r * 128 + ch * 16);
-                        const float lam = expf(g63 - s_g[r]);
-                        uint4 raw = *ptr;
-                        __nv_bfloat162 *h2 = reinterpret_cast<__nv_bfloat162 *>(&raw);
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const float2 f = __bfloat1622float2(h2[e]);
-                            h2[e] = __floats2bfloat162_rn(f.x * lam, f.y * lam);
-                        }
-                        *ptr = raw;
-                    }
-                }
+                if (!fast) exact_scale_k(l, sm + OFF_KQ + s * kKQBytes, s_g);
                 fence_proxy_async();
                 tc_fence_before();
                 mbar_arrive(&bars[B_OPS]);
                 mbar_arrive(&bars[B_GEMPTY + gbuf]);
+            } else if (!ap(0)) {
+                break;
             }
         }
     } else if (warp >= 8) {
@@ -811,105 +898,109 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t q = warp & 3;             // TMEM lane quadrant
         const int x = 32 * q + lane;             // value index (TMEM lane)
         const int d = p.d;
+        // S[m] = S[64 h + m][x] (this thread's value column, this warpgroup's key half)
         float S[64];
-        if (use_s0 && x < d) {
-            const float *src = p.S0 + (static_cast<int64_t>(b) * p.Hv + hv) * d * d + x;
+#pragma unroll
+        for (int m = 0; m < 64; ++m) S[m] = 0.f;
+        if (use_s0 && x < d && 64 * h < d) {
+            const float *src = p.S0 + (static_cast<int64_t>(b) * p.Hv + hv) * d * d + static_cast<int64_t>(64 * h) * d + x;
 #pragma unroll
             for (int m = 0; m < 64; ++m) {
-                const int dk = 64 * h + m;
-                S[m] = dk < d ? __ldg(src + static_cast<int64_t>(dk) * d) : 0.f;
+                S[m] = __ldg(src);
+                src += d;
             }
-        } else {
-#pragma unroll
-            for (int m = 0; m < 64; ++m) S[m] = 0.f;
         }
-        auto write_sb = [&](int buf) {
+        // j = -1 writes the initial state; j >= 0 processes chunk j and writes the next state.
+#pragma unroll 1
+        for (int j = -1; j < n; ++j) {
+            const float *cs = reinterpret_cast<const float *>(sm + OFF_CHAIN) + ((j + kChainSlots) % kChainSlots) * kChainFloats;
+            if (j >= 0) {
+                const uint32_t zu = tb + TM_ZU;
+                bool ok = bwait(&bars[B_UFULL], j & 1, abort_flag, p.status);
+                ok = ok && bwait(&bars[B_OPS], j & 1, abort_flag, p.status);  // per-chunk scales
+                if (!warp_ok(ok)) break;
+                tc_fence_after();
+                {
+                    // U^T scaled by lambda, bf16: this half's 32 tokens packed into 16 columns
+                    float u[32];
+                    tmem_ld32(lane_addr(zu, q, 32 * h), u);
+                    tmem_wait_ld();
+                    uint32_t pk[16];
 #pragma unroll
-            for (int piece = 0; piece < 2; ++piece) {
-                uint32_t u[16];
-#pragma unroll
-                for (int c = 0; c < 16; ++c) u[c] = pack_bf16(S[32 * piece + 2 * c], S[32 * piece + 2 * c + 1]);
-                tmem_st16(lane_addr(tb + TM_SB + 64 * buf + 32 * h + 16 * piece, q, 0), u);
-            }
-            tmem_wait_st();
-            tc_fence_before();
-            mbar_arrive(&bars[B_SREADY]);
-        };
-        write_sb(0);
-        for (int j = 0; j < n; ++j) {
-            const int c = c_w + j;
-            const float *cs = reinterpret_cast<const float *>(sm + OFF_CHAIN) + (j % kChainSlots) * kChainFloats;
-            const uint32_t zu = tb + TM_ZU;
-            bool ok = bwait(&bars[B_UFULL], j & 1, abort_flag, p.status);
-            ok = ok && bwait(&bars[B_OPS], j & 1, abort_flag, p.status);  // per-chunk scales
-            if (!warp_ok(ok)) break;
-            tc_fence_after();
-            {
-                // U^T scaled by lambda, bf16: this half's 32 tokens packed into 16 columns
-                uint32_t pk[16];
+                    for (int e4 = 0; e4 < 8; ++e4) {
+                        const float4 lam = *reinterpret_cast<const float4 *>(cs + 32 * h + 4 * e4);
+                        pk[2 * e4] = pack_bf16(u[4 * e4] * lam.x, u[4 * e4 + 1] * lam.y);
+                        pk[2 * e4 + 1] = pack_bf16(u[4 * e4 + 2] * lam.z, u[4 * e4 + 3] * lam.w);
+                    }
+                    tmem_st16(lane_addr(zu, q, 32 * h), pk);
+                    tmem_wait_st();
+                }
+                tc_fence_before();
+                mbar_arrive(&bars[B_USMEM]);
+                const float gC = cs[128];
+                ok = bwait(&bars[B_DFULL], j & 1, abort_flag, p.status);
+                if (!warp_ok(ok)) break;
+                tc_fence_after();
 #pragma unroll
                 for (int piece = 0; piece < 2; ++piece) {
-                    float u[16];
-                    tmem_ld16(lane_addr(zu, q, 32 * h + 16 * piece), u);
+                    float dd[32];
+                    tmem_ld32(lane_addr(tb + TM_D + 64 * h + 32 * piece, q, 0), dd);
                     tmem_wait_ld();
 #pragma unroll
-                    for (int e = 0; e < 8; ++e)
-                        pk[8 * piece + e] = pack_bf16(u[2 * e] * cs[32 * h + 16 * piece + 2 * e],
-                                                      u[2 * e + 1] * cs[32 * h + 16 * piece + 2 * e + 1]);
+                    for (int e = 0; e < 32; ++e) S[32 * piece + e] = fmaf(gC, S[32 * piece + e], dd[e]);
                 }
-                tmem_st16(lane_addr(zu, q, 32 * h), pk);
+            }
+            {
+                // S^T bf16 for the next chunk's products (double-buffered)
+                const int buf = (j + 1) & 1;
+#pragma unroll
+                for (int piece = 0; piece < 2; ++piece) {
+                    uint32_t u[16];
+#pragma unroll
+                    for (int c2 = 0; c2 < 16; ++c2) u[c2] = pack_bf16(S[32 * piece + 2 * c2], S[32 * piece + 2 * c2 + 1]);
+                    tmem_st16(lane_addr(tb + TM_SB + 64 * buf + 32 * h + 16 * piece, q, 0), u);
+                }
                 tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(&bars[B_SREADY]);
             }
-            tc_fence_before();
-            mbar_arrive(&bars[B_USMEM]);
-            const float gC = cs[128];
-            ok = bwait(&bars[B_DFULL], j & 1, abort_flag, p.status);
-            if (!warp_ok(ok)) break;
-            tc_fence_after();
-#pragma unroll
-            for (int piece = 0; piece < 4; ++piece) {
-                float dd[16];
-                tmem_ld16(lane_addr(tb + TM_D + 64 * h + 16 * piece, q, 0), dd);
-                tmem_wait_ld();
-#pragma unroll
-                for (int e = 0; e < 16; ++e) S[16 * piece + e] = fmaf(gC, S[16 * piece + e], dd[e]);
-            }
-            write_sb((j + 1) & 1);
-            ok = bwait(&bars[B_YFULL], j & 1, abort_flag, p.status);
+            if (j < 0) continue;
+            const int c = c_w + j;
+            bool ok = bwait(&bars[B_YFULL], j & 1, abort_flag, p.status);
             if (!warp_ok(ok)) break;
             tc_fence_after();
             uint32_t yb[16];   // y of this lane's 32 tokens, bf16 pairs
-#pragma unroll
-            for (int piece = 0; piece < 2; ++piece) {
-                float yv[16];
-                tmem_ld16(lane_addr(tb + TM_Y + 32 * h + 16 * piece, q, 0), yv);
+            {
+                float yv[32];
+                tmem_ld32(lane_addr(tb + TM_Y + 32 * h, q, 0), yv);
                 tmem_wait_ld();
 #pragma unroll
-                for (int e = 0; e < 8; ++e)
-                    yb[8 * piece + e] = pack_bf16(yv[2 * e] * cs[64 + 32 * h + 16 * piece + 2 * e],
-                                                  yv[2 * e + 1] * cs[64 + 32 * h + 16 * piece + 2 * e + 1]);
+                for (int e4 = 0; e4 < 8; ++e4) {
+                    const float4 gm = *reinterpret_cast<const float4 *>(cs + 64 + 32 * h + 4 * e4);
+                    yb[2 * e4] = pack_bf16(yv[4 * e4] * gm.x, yv[4 * e4 + 1] * gm.y);
+                    yb[2 * e4 + 1] = pack_bf16(yv[4 * e4 + 2] * gm.z, yv[4 * e4 + 3] * gm.w);
+                }
             }
             tc_fence_before();
             mbar_arrive(&bars[B_YFREE]);
             if (c >= c_begin && x < d) {
-                __nv_bfloat16 *yp = p.y + ((static_cast<int64_t>(b) * p.T + static_cast<int64_t>(c) * kC + 32 * h) *
-                                               p.Hv + hv) * d + x;
                 const int64_t tstart = static_cast<int64_t>(c) * kC + 32 * h;
-                const int64_t ystride = static_cast<int64_t>(p.Hv) * d;
+                uint16_t *yp = reinterpret_cast<uint16_t *>(p.y) + ((static_cast<int64_t>(b) * p.T + tstart) * p.Hv + hv) * d + x;
+                const int ystride = p.Hv * d;
+                const int nvalid = static_cast<int>(min(static_cast<int64_t>(32), p.T - tstart));
 #pragma unroll
                 for (int i = 0; i < 32; ++i) {
                     const uint32_t pr = yb[i >> 1];
-                    const uint16_t bits = (i & 1) ? static_cast<uint16_t>(pr >> 16) : static_cast<uint16_t>(pr & 0xffffu);
-                    if (tstart + i < p.T) *reinterpret_cast<uint16_t *>(yp + i * ystride) = bits;
+                    if (i < nvalid) yp[i * ystride] = (i & 1) ? static_cast<uint16_t>(pr >> 16) : static_cast<uint16_t>(pr);
                 }
             }
         }
-        if (last_seg && !*abort_flag && x < d) {
-            float *dst = p.S_T + (static_cast<int64_t>(b) * p.Hv + hv) * d * d + x;
+        if (last_seg && !*abort_flag && x < d && 64 * h < d) {
+            float *dst = p.S_T + (static_cast<int64_t>(b) * p.Hv + hv) * d * d + static_cast<int64_t>(64 * h) * d + x;
 #pragma unroll
             for (int m = 0; m < 64; ++m) {
-                const int dk = 64 * h + m;
-                if (dk < d) dst[static_cast<int64_t>(dk) * d] = S[m];
+                *dst = S[m];
+                dst += d;
             }
         }
     }
