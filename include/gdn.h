@@ -157,6 +157,37 @@ gdn_status gdn_decode_step(const gdn_shape *shape,
  */
 gdn_status gdn_read_device_status(void *ws, void *stream);
 
+/*
+ * Prefill for callers that cannot allocate device memory: an embedding
+ * runtime, a plugin running inside someone else's process, or code under a
+ * strict memory budget may have no way to call cudaMalloc for the workspace
+ * gdn_prefill asks for.  (The method itself needs no such entry point.)  This
+ * variant takes no workspace and allocates nothing: its scratch is a 256-byte
+ * status area plus a staging area in one fixed array inside this library
+ * (GDN_NOALLOC_SCRATCH_BYTES in total), which every GPU that loads the
+ * library keeps until the process exits.  Inputs, outputs, layouts and
+ * results are those of gdn_prefill.
+ *
+ * Limit: a shape whose gdn_prefill_workspace_bytes exceeds
+ * GDN_NOALLOC_SCRATCH_BYTES (more than 128 (batch, value head) pairs at
+ * d = 128, 512 at d = 64) returns GDN_ERR_WORKSPACE before anything runs.
+ * The first call on a device looks up the array's device address (once per
+ * device, with that device current); make that first call before any stream
+ * capture.  Every call clears the status area with cudaMemsetAsync on
+ * `stream` and then enqueues the prefill.  All calls share the one array, so
+ * calls whose execution overlaps on the GPU (different streams without
+ * ordering between them) race on it and must not be issued.  Bounded waits
+ * on the device still end the kernel if they time out, but the status word
+ * is not readable through this entry point: callers that need
+ * gdn_read_device_status use gdn_prefill with their own workspace.
+ */
+#define GDN_NOALLOC_SCRATCH_BYTES (256u + 8u * 1024u * 1024u)
+
+gdn_status gdn_prefill_noalloc(const gdn_shape *shape,
+                               const void *q, const void *k, const void *v,
+                               const float *alpha, const float *beta,
+                               const float *S0, void *y, float *S_T, void *stream);
+
 /* 1 if the current CUDA device can run these kernels (compute capability 10.3). */
 int gdn_device_supported(void);
 

@@ -3,6 +3,7 @@
 // computes any part of the recurrence.
 #include <cstdint>
 #include <cstring>
+#include <mutex>
 
 #include "gdn.h"
 #include "gdn_internal.h"
@@ -253,3 +254,58 @@ gdn_status gdn_read_device_status(void *ws, void *stream_) {
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Allocation-free prefill: its scratch is this fixed device array.  In host
+// code `g_noalloc_scratch` is only a stand-in for the symbol; its device
+// address comes from cudaGetSymbolAddress, looked up once per device.
+namespace {
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[GDN_NOALLOC_SCRATCH_BYTES];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_lock;
+void *g_noalloc_ptr[kMaxDevices] = {};
+
+gdn_status noalloc_scratch(void **out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return GDN_ERR_CUDA;
+    }
+    if (dev < 0 || dev >= kMaxDevices) return GDN_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> guard(g_noalloc_lock);
+    if (!g_noalloc_ptr[dev]) {
+        void *ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || ptr == nullptr) {
+            cudaGetLastError();
+            return GDN_ERR_CUDA;
+        }
+        g_noalloc_ptr[dev] = ptr;
+    }
+    *out = g_noalloc_ptr[dev];
+    return GDN_OK;
+}
+
+}  // namespace
+
+extern "C" gdn_status gdn_prefill_noalloc(const gdn_shape *shape, const void *q, const void *k, const void *v,
+                                          const float *alpha, const float *beta, const float *S0, void *y,
+                                          float *S_T, void *stream) {
+    const size_t need = gdn_prefill_workspace_bytes(shape);
+    if (need == 0) return GDN_ERR_INVALID_ARG;
+    if (need > GDN_NOALLOC_SCRATCH_BYTES) return GDN_ERR_WORKSPACE;
+    int num_sms = 0;
+    gdn_status st = check_device(&num_sms);
+    if (st != GDN_OK) return st;
+    void *scratch = nullptr;
+    st = noalloc_scratch(&scratch);
+    if (st != GDN_OK) return st;
+    // The status word must start each call at zero; the array keeps the last call's contents.
+    if (cudaMemsetAsync(scratch, 0, 256, static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+        cudaGetLastError();
+        return GDN_ERR_CUDA;
+    }
+    return gdn_prefill_ex(shape, nullptr, q, k, v, alpha, beta, S0, y, S_T, scratch, GDN_NOALLOC_SCRATCH_BYTES,
+                          stream);
+}

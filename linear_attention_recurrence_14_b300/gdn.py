@@ -26,7 +26,9 @@ ALGO_NAMES = {ALGO_AUTO: "auto", ALGO_CHUNKED: "chunked", ALGO_SEQUENTIAL: "sequ
 
 # Every symbol include/gdn.h declares.
 EXPORTS = ("gdn_status_string", "gdn_prefill_workspace_bytes", "gdn_prefill", "gdn_prefill_ex",
-           "gdn_decode_step", "gdn_read_device_status", "gdn_device_supported", "gdn_abi_version")
+           "gdn_decode_step", "gdn_read_device_status", "gdn_device_supported", "gdn_abi_version",
+           "gdn_prefill_noalloc")
+NOALLOC_SCRATCH_BYTES = 256 + 8 * 1024 * 1024
 
 
 class GdnShape(ctypes.Structure):
@@ -68,6 +70,8 @@ def lib() -> ctypes.CDLL:
             L.gdn_prefill_ex.restype = ctypes.c_int
             L.gdn_prefill_ex.argtypes = [sp, ctypes.POINTER(GdnPrefillOptions), vp, vp, vp, fp, fp, fp, vp, fp, vp,
                                          c_size, vp]
+            L.gdn_prefill_noalloc.restype = ctypes.c_int
+            L.gdn_prefill_noalloc.argtypes = [sp, vp, vp, vp, fp, fp, fp, vp, fp, vp]
             L.gdn_decode_step.restype = ctypes.c_int
             L.gdn_decode_step.argtypes = [sp, vp, vp, vp, fp, fp, fp, vp, vp]
             L.gdn_read_device_status.restype = ctypes.c_int
@@ -158,6 +162,20 @@ def prefill(q, k, v, alpha, beta, S0=None, *, y=None, S_T=None, workspace=None, 
                               _ptr(beta), _ptr(S0), _ptr(y), _ptr(S_T), _ptr(workspace),
                               workspace.numel() * workspace.element_size(), _stream(stream))
     _check(rc, "gdn_prefill_ex")
+    return y, S_T
+
+
+def prefill_noalloc(q, k, v, alpha, beta, S0=None, *, y=None, S_T=None, stream=None):
+    """Run gdn_prefill_noalloc (no workspace; the library's fixed scratch array); returns (y, S_T)."""
+    _require(dict(q=q, k=k, v=v, alpha=alpha, beta=beta, S0=S0, y=y, S_T=S_T))
+    shape = shape_of(q, v)
+    if y is None:
+        y = torch.empty_like(v)
+    if S_T is None:
+        S_T = torch.empty((shape.B, shape.Hv, shape.dk, shape.dv), dtype=torch.float32, device=v.device)
+    rc = lib().gdn_prefill_noalloc(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(beta),
+                                   _ptr(S0), _ptr(y), _ptr(S_T), _stream(stream))
+    _check(rc, "gdn_prefill_noalloc")
     return y, S_T
 
 
