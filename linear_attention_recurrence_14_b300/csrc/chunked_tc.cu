@@ -75,8 +75,8 @@ constexpr int kBS = 24;
 constexpr int kBlk = 16 * kBS;
 constexpr uint32_t OFF_AT = OFF_T2 + 64 * 128;
 constexpr uint32_t OFF_TM = OFF_AT + 10 * kBlk * 4;
-constexpr uint32_t OFF_R = OFF_TM + 10 * kBlk * 4;      // 4 warps x [16][kBS]
-constexpr uint32_t OFF_GATES = OFF_R + 4 * kBlk * 4;
+constexpr uint32_t OFF_R = OFF_TM + 10 * kBlk * 4;      // 3 warps x [16][kBS]
+constexpr uint32_t OFF_GATES = OFF_R + 3 * kBlk * 4;
 // gates, double-buffered by chunk parity: g, u = gamma, w = 1/gamma, beta,
 // beta gamma (64 floats each), misc (64)
 constexpr int kGateFloats = 6 * 64;
@@ -188,12 +188,6 @@ __constant__ int kBlkIdx[4][4] = {{0, 0, 0, 0}, {1, 2, 0, 0}, {3, 4, 5, 0}, {6, 
 // Chunks whose total log decay is at least this use the factored gates.
 constexpr float kFastLogDecay = -40.f;
 
-__device__ __forceinline__ uint32_t f2tf32(float x) {
-    uint32_t r;
-    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
-    return r;
-}
-
 // d (16 x 8, fp32) += a (16 x 8, tf32, row) * b (8 x 8, tf32, col): one warp.
 __device__ __forceinline__ void mma_tf32(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                          uint32_t b0, uint32_t b1) {
@@ -208,82 +202,6 @@ __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
     return v;
-}
-
-// One warp: C (+)= X W for 16 x 16 row-major fp32 blocks (row stride kBS) with
-// tf32 m16n8k8 MMAs; c[nt] holds the C fragment of columns 8 nt .. 8 nt + 7.
-__device__ __forceinline__ void mm16(float (&c)[2][4], const float *X, const float *W, int gq, int t4) {
-#pragma unroll
-    for (int ks = 0; ks < 2; ++ks) {
-        const int k0 = 8 * ks;
-        const uint32_t a0 = __float_as_uint(X[gq * kBS + k0 + t4]);
-        const uint32_t a1 = __float_as_uint(X[(gq + 8) * kBS + k0 + t4]);
-        const uint32_t a2 = __float_as_uint(X[gq * kBS + k0 + t4 + 4]);
-        const uint32_t a3 = __float_as_uint(X[(gq + 8) * kBS + k0 + t4 + 4]);
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt)
-            mma_tf32(c[nt], a0, a1, a2, a3, __float_as_uint(W[(k0 + t4) * kBS + 8 * nt + gq]),
-                     __float_as_uint(W[(k0 + t4 + 4) * kBS + 8 * nt + gq]));
-    }
-}
-
-__device__ __forceinline__ void load_cfrag(float (&c)[2][4], const float *M, int gq, int t4) {
-#pragma unroll
-    for (int nt = 0; nt < 2; ++nt) {
-        const float2 lo = *reinterpret_cast<const float2 *>(M + gq * kBS + 8 * nt + 2 * t4);
-        const float2 hi = *reinterpret_cast<const float2 *>(M + (gq + 8) * kBS + 8 * nt + 2 * t4);
-        c[nt][0] = lo.x; c[nt][1] = lo.y; c[nt][2] = hi.x; c[nt][3] = hi.y;
-    }
-}
-
-__device__ __forceinline__ void store_cfrag(float *M, const float (&c)[2][4], int gq, int t4) {
-#pragma unroll
-    for (int nt = 0; nt < 2; ++nt) {
-        *reinterpret_cast<float2 *>(M + gq * kBS + 8 * nt + 2 * t4) = make_float2(c[nt][0], c[nt][1]);
-        *reinterpret_cast<float2 *>(M + (gq + 8) * kBS + 8 * nt + 2 * t4) = make_float2(c[nt][2], c[nt][3]);
-    }
-}
-
-// Inverse of a 16 x 16 unit lower-triangular block I + N (one warp), N the
-// strictly lower part of A's diagonal block (column-major within the block,
-// entries on and above the diagonal are not read).  N is nilpotent (N^16 = 0),
-// so (I + N)^{-1} = (I + Z)(I + Z^2)(I + Z^4)(I + Z^8) exactly, Z = -N: four
-// dependent steps of 16 x 16 products.  Writes the inverse row-major to Y;
-// Zb is a scratch block.
-__device__ __forceinline__ void invert_diag_block(const float *Ablk, float *Y, float *Zb, int lane) {
-    const int gq = lane >> 2, t4 = lane & 3;
-    {
-        // Zb = -N, Y = I - N (row r = lane / 2, columns 8 (lane & 1) .. + 7)
-        const int r = lane >> 1, c0 = 8 * (lane & 1);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            const int c = c0 + e;
-            const float z = r > c ? -Ablk[c * kBS + r] : 0.f;
-            Zb[r * kBS + c] = z;
-            Y[r * kBS + c] = z + (r == c ? 1.f : 0.f);
-        }
-    }
-    __syncwarp();
-#pragma unroll 1
-    for (int step = 0; step < 4; ++step) {
-        // step 0: Z <- Z^2.  steps 1, 2: Y <- Y + Y Z, Z <- Z^2.  step 3: Y <- Y + Y Z.
-        float yz[2][4], zz[2][4];
-        if (step > 0) {
-            load_cfrag(yz, Y, gq, t4);
-            mm16(yz, Y, Zb, gq, t4);
-        }
-        if (step < 3) {
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) zz[nt][e] = 0.f;
-            mm16(zz, Zb, Zb, gq, t4);
-        }
-        __syncwarp();
-        if (step > 0) store_cfrag(Y, yz, gq, t4);
-        if (step < 3) store_cfrag(Zb, zz, gq, t4);
-        __syncwarp();
-    }
 }
 
 // Off-diagonal blocks of block column J of T = (I + A)^{-1} (one warp):
@@ -378,7 +296,7 @@ __device__ __noinline__ void diag_to_bf16(const float *Tm, uint8_t *t1b, uint8_t
     }
 }
 
-// nk consecutive K=16 MMAs of one product.  Operand offsets advance as
+// Operand of a run of K=16 MMAs.  Offsets advance as
 // (kk >> shift) * big + (kk & ((1 << shift) - 1)) * small bytes (TMEM A: columns);
 // a start address inside a descriptor moves by adding offset >> 4.
 struct MmaOperand {
@@ -391,9 +309,12 @@ __device__ __forceinline__ uint32_t operand_offset(const MmaOperand &o, uint32_t
     return (kk >> o.shift) * o.big + (kk & ((1u << o.shift) - 1u)) * o.small;
 }
 
-__device__ __noinline__ void mma_run(uint32_t d, MmaOperand a, MmaOperand b, uint32_t idesc, int nk, uint32_t acc) {
-#pragma unroll 1
-    for (int kk = 0; kk < nk; ++kk) {
+// NK consecutive K=16 MMAs of one product (unrolled; the descriptors are
+// precomputed, each step adds a constant offset).
+template <int NK>
+__device__ __forceinline__ void mma_run_t(uint32_t d, const MmaOperand &a, const MmaOperand &b, uint32_t idesc, uint32_t acc) {
+#pragma unroll
+    for (int kk = 0; kk < NK; ++kk) {
         const uint64_t bd = b.desc + (operand_offset(b, kk) >> 4);
         const uint32_t accumulate = acc | (kk > 0 ? 1u : 0u);
         if (a.tmem)
@@ -638,12 +559,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             };
             auto gram = [&](int j) {
                 const MmaOperand kq = smem_kmajor(kq_addr(j % kStages), 16384u);
-                mma_run(tb + TM_GW + (j & 1) * 64, kq, kq, ID_KK, 8, 0u);
+                mma_run_t<8>(tb + TM_GW + (j & 1) * 64, kq, kq, ID_KK, 0u);
             };
             auto wu = [&](int j) {
                 const int s = j % kStages;
-                mma_run(tb + TM_GW + (j & 1) * 64, smem_mnmajor(kq_addr(s), 16384u), smem_kmajor(t1, 0u), ID_MK, 4, 0u);
-                mma_run(tb + TM_ZU, smem_mnmajor(vw_addr(s), 8192u), smem_kmajor(t2, 0u), ID_MK, 4, 0u);
+                mma_run_t<4>(tb + TM_GW + (j & 1) * 64, smem_mnmajor(kq_addr(s), 16384u), smem_kmajor(t1, 0u), ID_MK, 0u);
+                mma_run_t<4>(tb + TM_ZU, smem_mnmajor(vw_addr(s), 8192u), smem_kmajor(t2, 0u), ID_MK, 0u);
             };
             bool ok = true;
             do {
@@ -671,7 +592,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // U^T = U~^T + S^T (-W)^T   (-W^T stored [dk][tokens], MN-major)
                     const MmaOperand sa{0ull, sb, 0u, 8u, 3u};          // S^T bf16: 8 columns per K step
                     const MmaOperand ua{0ull, zu, 32u, 8u, 1u};         // U^T bf16: tokens 0-31 at 0-15, 32-63 at 32-47
-                    mma_run(zu, sa, smem_mnmajor(vw_addr(s), 16u), ID_TSM, 8, 1u);
+                    mma_run_t<8>(zu, sa, smem_mnmajor(vw_addr(s), 16u), ID_TSM, 1u);
                     mma_commit(&bars[B_UFULL]);
                     // Gram of chunk j+2 into the GW buffer W^T(j) occupied (read before
                     // OPS(j)); it runs while the chain converts U^T, before MMA2 is issued.
@@ -685,13 +606,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (!(ok = bwait(&bars[B_USMEM], j & 1, abort_flag, p.status))) break;
                     tc_fence_after();
                     // dS^T = U^T K~
-                    mma_run(tb + TM_D, ua, smem_mnmajor(kq_addr(s), 16384u), ID_TD, 4, 0u);
+                    mma_run_t<4>(tb + TM_D, ua, smem_mnmajor(kq_addr(s), 16384u), ID_TD, 0u);
                     mma_commit(&bars[B_DFULL]);
                     if (j > 0 && !(ok = bwait(&bars[B_YFREE], (j - 1) & 1, abort_flag, p.status))) break;
                     tc_fence_after();
                     // Y^T = S^T Q~^T + U^T P^T
-                    mma_run(tb + TM_Y, sa, smem_kmajor(kq_addr(s) + 8192, 16384u), ID_TS, 8, 0u);
-                    mma_run(tb + TM_Y, ua, smem_kmajor(p_addr(s), 0u), ID_TS, 4, 1u);
+                    mma_run_t<8>(tb + TM_Y, sa, smem_kmajor(kq_addr(s) + 8192, 16384u), ID_TS, 0u);
+                    mma_run_t<4>(tb + TM_Y, ua, smem_kmajor(p_addr(s), 0u), ID_TS, 1u);
                     mma_commit(&bars[B_YFULL]);
                     mma_commit(&bars[B_EMPTY + s]);
                     if (j + 1 < n) {
@@ -836,9 +757,37 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 sm + OFF_KQ + s * kKQBytes, s_g, s_u, s_b);
             }
             tc_fence_before();
-            named_bar(1, 128);   // all rows of A written
-            // Diagonal block lw of T = (I + A)^{-1}, one block per warp.
-            invert_diag_block(At + kBlkIdx[lw][lw] * kBlk, Tm + kBlkIdx[lw][lw] * kBlk, Rw, lane);
+            if (l < 64) {
+                // Diagonal blocks of T = (I + A)^{-1} by forward substitution, one
+                // column per thread; this warp wrote both blocks' rows.  The block's
+                // strictly lower part (column m: rows m+1..15) is loaded in two
+                // batches ahead of the arithmetic.
+                __syncwarp();
+                const int blk = l >> 4, col = l & 15;
+                const float *Ab = At + kBlkIdx[blk][blk] * kBlk;
+                float t[16];
+#pragma unroll
+                for (int r = 0; r < 16; ++r) t[r] = (r == col) ? 1.f : 0.f;
+#pragma unroll
+                for (int mb = 0; mb < 2; ++mb) {
+                    constexpr int kSplit = 5;
+                    float av[65];
+                    const int m0 = mb ? kSplit : 0, m1 = mb ? 15 : kSplit;
+#pragma unroll
+                    for (int m = m0; m < m1; ++m)
+#pragma unroll
+                        for (int r = m + 1; r < 16; ++r)
+                            av[(m * 16 - (m * (m + 1)) / 2 + (r - m - 1)) - (m0 * 16 - (m0 * (m0 + 1)) / 2)] = Ab[m * kBS + r];
+#pragma unroll
+                    for (int m = m0; m < m1; ++m)
+#pragma unroll
+                        for (int r = m + 1; r < 16; ++r)
+                            t[r] = fmaf(-av[(m * 16 - (m * (m + 1)) / 2 + (r - m - 1)) - (m0 * 16 - (m0 * (m0 + 1)) / 2)], t[m], t[r]);
+                }
+                float *Tb = Tm + kBlkIdx[blk][blk] * kBlk + col;
+#pragma unroll
+                for (int r = 0; r < 16; ++r) Tb[r * kBS] = t[r];
+            }
             return true;
         };
 
