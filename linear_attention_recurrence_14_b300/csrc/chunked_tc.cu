@@ -75,8 +75,8 @@ constexpr int kBS = 24;
 constexpr int kBlk = 16 * kBS;
 constexpr uint32_t OFF_AT = OFF_T2 + 64 * 128;
 constexpr uint32_t OFF_TM = OFF_AT + 10 * kBlk * 4;
-constexpr uint32_t OFF_R = OFF_TM + 10 * kBlk * 4;      // 3 warps x [16][kBS]
-constexpr uint32_t OFF_GATES = OFF_R + 3 * kBlk * 4;
+constexpr uint32_t OFF_R = OFF_TM + 10 * kBlk * 4;      // 4 warps x [16][kBS]
+constexpr uint32_t OFF_GATES = OFF_R + 4 * kBlk * 4;
 // gates, double-buffered by chunk parity: g, u = gamma, w = 1/gamma, beta,
 // beta gamma (64 floats each), misc (64)
 constexpr int kGateFloats = 6 * 64;
@@ -210,7 +210,12 @@ __device__ __forceinline__ float warp_sum(float v) {
 // tensor core reads their tf32 part).  Writes T_IJ as fp32 (row-major block)
 // and as bf16 T1 = T diag(beta gamma), T2 = T diag(beta).  Loops are kept
 // rolled: the kernel's hot code has to fit the instruction cache.
-__device__ __forceinline__ void merge_column(int J, const float *At, float *Tm, float *Rw, uint8_t *t1b,
+//
+// NNT = 2 does the whole 16-column block column; NNT = 1 only its 8-column
+// tile nt0 (the two tiles are independent through every level, so block
+// column 0, the longest chain, is split over two warps).
+template <int NNT>
+__device__ __forceinline__ void merge_column(int J, int nt0, const float *At, float *Tm, float *Rw, uint8_t *t1b,
                                              uint8_t *t2b, const float *s_b, const float *s_bu, int lane) {
     const int gq = lane >> 2, t4 = lane & 3;
 #pragma unroll 1
@@ -231,20 +236,27 @@ __device__ __forceinline__ void merge_column(int J, const float *At, float *Tm, 
                 a[ks][2] = __float_as_uint(Ab[(k0 + t4 + 4) * kBS + gq]);
                 a[ks][3] = __float_as_uint(Ab[(k0 + t4 + 4) * kBS + gq + 8]);
 #pragma unroll
-                for (int nt = 0; nt < 2; ++nt) {
-                    b[ks][nt][0] = __float_as_uint(Bb[(k0 + t4) * kBS + 8 * nt + gq]);
-                    b[ks][nt][1] = __float_as_uint(Bb[(k0 + t4 + 4) * kBS + 8 * nt + gq]);
+                for (int nt = 0; nt < NNT; ++nt) {
+                    b[ks][nt][0] = __float_as_uint(Bb[(k0 + t4) * kBS + 8 * (nt0 + nt) + gq]);
+                    b[ks][nt][1] = __float_as_uint(Bb[(k0 + t4 + 4) * kBS + 8 * (nt0 + nt) + gq]);
                 }
             }
             mma_tf32(c0, a[0][0], a[0][1], a[0][2], a[0][3], b[0][0][0], b[0][0][1]);
-            mma_tf32(c1, a[0][0], a[0][1], a[0][2], a[0][3], b[0][1][0], b[0][1][1]);
             mma_tf32(e0, a[1][0], a[1][1], a[1][2], a[1][3], b[1][0][0], b[1][0][1]);
-            mma_tf32(e1, a[1][0], a[1][1], a[1][2], a[1][3], b[1][1][0], b[1][1][1]);
+            if (NNT == 2) {
+                mma_tf32(c1, a[0][0], a[0][1], a[0][2], a[0][3], b[0][NNT - 1][0], b[0][NNT - 1][1]);
+                mma_tf32(e1, a[1][0], a[1][1], a[1][2], a[1][3], b[1][NNT - 1][0], b[1][NNT - 1][1]);
+            }
         }
-        *reinterpret_cast<float2 *>(Rw + gq * kBS + 2 * t4) = make_float2(c0[0] + e0[0], c0[1] + e0[1]);
-        *reinterpret_cast<float2 *>(Rw + (gq + 8) * kBS + 2 * t4) = make_float2(c0[2] + e0[2], c0[3] + e0[3]);
-        *reinterpret_cast<float2 *>(Rw + gq * kBS + 8 + 2 * t4) = make_float2(c1[0] + e1[0], c1[1] + e1[1]);
-        *reinterpret_cast<float2 *>(Rw + (gq + 8) * kBS + 8 + 2 * t4) = make_float2(c1[2] + e1[2], c1[3] + e1[3]);
+        {
+            const int cb = 8 * nt0 + 2 * t4;
+            *reinterpret_cast<float2 *>(Rw + gq * kBS + cb) = make_float2(c0[0] + e0[0], c0[1] + e0[1]);
+            *reinterpret_cast<float2 *>(Rw + (gq + 8) * kBS + cb) = make_float2(c0[2] + e0[2], c0[3] + e0[3]);
+            if (NNT == 2) {
+                *reinterpret_cast<float2 *>(Rw + gq * kBS + 8 + cb) = make_float2(c1[0] + e1[0], c1[1] + e1[1]);
+                *reinterpret_cast<float2 *>(Rw + (gq + 8) * kBS + 8 + cb) = make_float2(c1[2] + e1[2], c1[3] + e1[3]);
+            }
+        }
         __syncwarp();
         float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
         const float *Td = Tm + (I * (I + 1) / 2 + I) * kBlk;       // T[r][k] at r*kBS + k
@@ -255,16 +267,17 @@ __device__ __forceinline__ void merge_column(int J, const float *At, float *Tm, 
             const uint32_t a1 = __float_as_uint(Td[(gq + 8) * kBS + k0 + t4]);
             const uint32_t a2 = __float_as_uint(Td[gq * kBS + k0 + t4 + 4]);
             const uint32_t a3 = __float_as_uint(Td[(gq + 8) * kBS + k0 + t4 + 4]);
-            mma_tf32(d0, a0, a1, a2, a3, __float_as_uint(Rw[(k0 + t4) * kBS + gq]),
-                     __float_as_uint(Rw[(k0 + t4 + 4) * kBS + gq]));
-            mma_tf32(d1, a0, a1, a2, a3, __float_as_uint(Rw[(k0 + t4) * kBS + 8 + gq]),
-                     __float_as_uint(Rw[(k0 + t4 + 4) * kBS + 8 + gq]));
+            mma_tf32(d0, a0, a1, a2, a3, __float_as_uint(Rw[(k0 + t4) * kBS + 8 * nt0 + gq]),
+                     __float_as_uint(Rw[(k0 + t4 + 4) * kBS + 8 * nt0 + gq]));
+            if (NNT == 2)
+                mma_tf32(d1, a0, a1, a2, a3, __float_as_uint(Rw[(k0 + t4) * kBS + 8 + gq]),
+                         __float_as_uint(Rw[(k0 + t4 + 4) * kBS + 8 + gq]));
         }
         float *Tb = Tm + (I * (I + 1) / 2 + J) * kBlk;
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
+        for (int nt = 0; nt < NNT; ++nt) {
             const float *dd = nt ? d1 : d0;
-            const int cn = 8 * nt + 2 * t4;
+            const int cn = 8 * (nt0 + nt) + 2 * t4;
             const int C = 16 * J + cn;
             const float sa0 = s_bu[C], sa1 = s_bu[C + 1], sb0 = s_b[C], sb1 = s_b[C + 1];
 #pragma unroll
@@ -281,13 +294,13 @@ __device__ __forceinline__ void merge_column(int J, const float *At, float *Tm, 
     }
 }
 
-// bf16 T1, T2 of the four diagonal blocks from their fp32 copies (one warp).
-__device__ __noinline__ void diag_to_bf16(const float *Tm, uint8_t *t1b, uint8_t *t2b, const float *s_b,
-                                          const float *s_bu, int lane) {
-#pragma unroll 4
-    for (int u = 0; u < 16; ++u) {
-        const int e = lane + 32 * u;             // 512 column pairs
-        const int blk = e >> 7, r = (e >> 3) & 15, cp = e & 7;
+// bf16 T1, T2 of diagonal block blk from its fp32 copy (one warp).
+__device__ __forceinline__ void diag_block_to_bf16(int blk, const float *Tm, uint8_t *t1b, uint8_t *t2b,
+                                                   const float *s_b, const float *s_bu, int lane) {
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        const int e = lane + 32 * u;             // 128 column pairs of the block
+        const int r = e >> 3, cp = e & 7;
         const int C = 16 * blk + 2 * cp;
         const float2 v = *reinterpret_cast<const float2 *>(Tm + (blk * (blk + 1) / 2 + blk) * kBlk + r * kBS + 2 * cp);
         const uint32_t off = sw128_elem(16 * blk + r, C);
@@ -447,6 +460,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&bars[B_GFULL + e], 64);
             mbar_init(&bars[B_GEMPTY + e], 128);
         }
+
         misc->abort = 0;
         fence_mbarrier_init();
         prefetch_tensormap(&tm_q);
@@ -801,35 +815,43 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float *s_g = sg, *s_b = sg + 192, *s_bu = sg + 256, *s_misc = sg + 320;
                 const bool fast = s_misc[2] != 0.f;
                 named_bar(1, 128);   // A, diagonal T blocks and P of chunk j are written
-                // Off-diagonal blocks T_IJ (warp J of 0-2), bf16 T1, T2 of the diagonal blocks (warp 3).
-                if (lw < 3)
-                    merge_column(lw, At, Tm, Rw, t1b, t2b, s_b, s_bu, lane);
+                // bf16 T1, T2 of diagonal block lw, then the off-diagonal blocks T_IJ:
+                // block column 0 split over warps 0 and 3 (one 8-column tile each),
+                // column 1 on warp 1, column 2 on warp 2.
+                diag_block_to_bf16(lw, Tm, t1b, t2b, s_b, s_bu, lane);
+                if (lw == 0 || lw == 3)
+                    merge_column<1>(0, lw == 3 ? 1 : 0, At, Tm, Rw, t1b, t2b, s_b, s_bu, lane);
                 else
-                    diag_to_bf16(Tm, t1b, t2b, s_b, s_bu, lane);
+                    merge_column<2>(lw, 0, At, Tm, Rw, t1b, t2b, s_b, s_bu, lane);
                 fence_proxy_async();
                 mbar_arrive(&bars[B_TREADY]);
                 named_bar(1, 128);   // A and T of chunk j are no longer read
                 if (j + 1 < n && !ap(j + 1)) break;
 
-                // ---- -W (token-major, K-major operand) into the V slot (exact path: K~ in place)
-                bool ok = bwait(&bars[B_WU], j & 1, abort_flag, p.status);
-                if (!warp_ok(ok)) break;
+                // The W^T, U~^T MMAs of chunk j have read T1, T2 (rewritten by the next
+                // merges) and K (exact path: K~ = diag(lambda) K in place).  Waiting here
+                // also keeps this warpgroup at most one TREADY phase ahead of the MMA thread.
+                {
+                    const bool ok = bwait(&bars[B_WU], j & 1, abort_flag, p.status);
+                    if (!warp_ok(ok)) break;
+                }
                 tc_fence_after();
-                // -W^T row l (key index l, 64 tokens) as one swizzled 128-byte row of the
-                // MN-major operand [dk][tokens]
-                uint8_t *wrow = sm + OFF_VW + s * kVWBytes + l * 128;
+                {
+                    // -W^T row l (key index l, 64 tokens) as one swizzled 128-byte row of
+                    // the MN-major operand [dk][tokens] in the V slot
+                    uint8_t *wrow = sm + OFF_VW + s * kVWBytes + l * 128;
 #pragma unroll 1
-                for (int half = 0; half < 2; ++half) {
-                    float w[32];
-                    tmem_ld32(lane_addr(tb + TM_GW + (j & 1) * 64, q, 32 * half), w);
-                    tmem_wait_ld();
+                    for (int half = 0; half < 2; ++half) {
+                        float w[32];
+                        tmem_ld32(lane_addr(tb + TM_GW + (j & 1) * 64, q, 32 * half), w);
+                        tmem_wait_ld();
 #pragma unroll
-                    for (int c4 = 0; c4 < 4; ++c4) {
-                        const int ch = 4 * half + c4;
-                        *reinterpret_cast<uint4 *>(wrow + ((ch ^ (l & 7)) << 4)) =
-                            make_uint4(pack_bf16(-w[8 * c4], -w[8 * c4 + 1]), pack_bf16(-w[8 * c4 + 2], -w[8 * c4 + 3]),
-                                       pack_bf16(-w[8 * c4 + 4], -w[8 * c4 + 5]),
-                                       pack_bf16(-w[8 * c4 + 6], -w[8 * c4 + 7]));
+                        for (int c4 = 0; c4 < 4; ++c4) {
+                            const int ch = 4 * half + c4;
+                            *reinterpret_cast<uint4 *>(wrow + ((ch ^ (l & 7)) << 4)) = make_uint4(
+                                pack_bf16(-w[8 * c4], -w[8 * c4 + 1]), pack_bf16(-w[8 * c4 + 2], -w[8 * c4 + 3]),
+                                pack_bf16(-w[8 * c4 + 4], -w[8 * c4 + 5]), pack_bf16(-w[8 * c4 + 6], -w[8 * c4 + 7]));
+                        }
                     }
                 }
                 if (!fast) exact_scale_k(l, sm + OFF_KQ + s * kKQBytes, s_g);
