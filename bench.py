@@ -151,6 +151,14 @@ def barrier(ws):
         dist.barrier()
 
 
+def whole_job_rate(units_per_rank: float, local_ms: float, ws: int, device) -> tuple[float, float]:
+    """Aggregate throughput of a weak-scaled run: every rank processed
+    `units_per_rank` in `local_ms`; the job took the slowest rank's time.
+    Returns (units per second over all ranks, max milliseconds)."""
+    ms = max_over_ranks(local_ms, ws, device)
+    return units_per_rank * ws / (ms * 1e-3), ms
+
+
 def max_over_ranks(x: float, ws: int, device) -> float:
     if ws == 1:
         return x
@@ -286,11 +294,9 @@ def run_ours(args, ws, rank, local):
     if status != 0:
         raise SystemExit(f"device status {status} in the timed region")
     per_launch_ms = [a.elapsed_time(b) for a, b in ev]
-    total_ms = t_all0.elapsed_time(t_all1)
-    total_ms = max_over_ranks(total_ms, ws, dev)
-    ms_per_step = total_ms / args.steps
     tokens = w["B"] * w["T"]
-    value = tokens * ws * args.steps / (total_ms * 1e-3)
+    value, total_ms = whole_job_rate(tokens * args.steps, t_all0.elapsed_time(t_all1), ws, dev)
+    ms_per_step = total_ms / args.steps
     clocks = clk.summary()
 
     kern_s = statistics.mean(per_launch_ms) * 1e-3

@@ -95,6 +95,12 @@ typedef struct {
  *   GDN_ALGO_CHUNKED (tensor-core chunked kernel; bf16 only, else
  *   GDN_ERR_UNSUPPORTED) or GDN_ALGO_SEQUENTIAL (token-sequential fp32-math
  *   kernel, one CTA per head; segments/log_eps do not apply).
+ * test_stall_chunk: a fault-injection hook for tests of the device-side
+ *   failure detection (chunked kernel only).  When > 0, the tiles of that
+ *   chunk index are never loaded, so the kernel's bounded waits (about one
+ *   second each) run out: the kernel records GDN_ERR_TIMEOUT in the workspace
+ *   status word, stops, and leaves the context usable.  Outputs of such a
+ *   call are undefined.  Leave 0 in normal use.
  */
 typedef enum { GDN_ALGO_AUTO = 0, GDN_ALGO_CHUNKED = 1, GDN_ALGO_SEQUENTIAL = 2 } gdn_algorithm;
 
@@ -103,6 +109,7 @@ typedef struct {
     float log_eps;
     int32_t max_warmup_chunks;
     int32_t algorithm;          /* gdn_algorithm */
+    int32_t test_stall_chunk;   /* test hook, 0 = off: see below */
 } gdn_prefill_options;
 
 /* Text for a status code (static storage, never NULL). */

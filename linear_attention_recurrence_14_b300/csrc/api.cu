@@ -120,10 +120,11 @@ gdn_status gdn_prefill_ex(const gdn_shape *shape, const gdn_prefill_options *opt
     const size_t esz = s.dtype == GDN_BF16 ? 2 : 4;
     const bool has_tokens = s.B * s.T > 0;
 
-    gdn_prefill_options opt{0, 0.f, 0, GDN_ALGO_AUTO};
+    gdn_prefill_options opt{0, 0.f, 0, GDN_ALGO_AUTO, 0};
     if (options) opt = *options;
     if (opt.segments < 0 || opt.max_warmup_chunks < 0 || !(opt.log_eps <= 0.f)) return GDN_ERR_INVALID_ARG;
     if (opt.algorithm < GDN_ALGO_AUTO || opt.algorithm > GDN_ALGO_SEQUENTIAL) return GDN_ERR_INVALID_ARG;
+    if (opt.test_stall_chunk < 0) return GDN_ERR_INVALID_ARG;
     const int algorithm = opt.algorithm;
     const int segments = opt.segments;
 
@@ -189,6 +190,7 @@ gdn_status gdn_prefill_ex(const gdn_shape *shape, const gdn_prefill_options *opt
     p.segments = segments;
     p.log_eps = opt.log_eps < 0.f ? opt.log_eps : kDefaultLogEps;
     p.max_warmup_chunks = opt.max_warmup_chunks > 0 ? opt.max_warmup_chunks : kDefaultMaxWarmupChunks;
+    p.test_stall_chunk = opt.test_stall_chunk;
     st = from_cuda(gdn::launch_chunked(p, stream, num_sms));
     if (st != GDN_OK) return st;
     if (in_place) return from_cuda(cudaMemcpyAsync(S_T, staging, rst.n, cudaMemcpyDeviceToDevice, stream));

@@ -130,7 +130,7 @@ constexpr uint32_t TM_SB = 384;   // 2 x 64: S^T bf16 packed
 struct Dev {
     int64_t T;
     int B, Hqk, Hv, group, d;
-    int nchunks, seg_chunks, nseg, max_warmup;
+    int nchunks, seg_chunks, nseg, max_warmup, test_stall_chunk;
     float log_eps;
     const float *alpha, *beta, *S0;
     __nv_bfloat16 *y;
@@ -542,6 +542,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t ph = (j / kStages) & 1;
                 if (!bwait(&bars[B_EMPTY + s], ph ^ 1, abort_flag, p.status)) break;
                 const int t0 = (c_w + j) * kC;
+                if (p.test_stall_chunk > 0 && c_w + j == p.test_stall_chunk) continue;  // fault injection
                 mbar_arrive_expect_tx(&bars[B_FULL + s], kKQBytes + kVWBytes);
                 uint8_t *kq = sm + OFF_KQ + s * kKQBytes;
                 uint8_t *vw = sm + OFF_VW + s * kVWBytes;
@@ -1076,6 +1077,7 @@ cudaError_t launch_chunked(const ChunkedParams &p, cudaStream_t stream, int num_
     dv.seg_chunks = static_cast<int>(len);
     dv.nseg = P;
     dv.max_warmup = p.max_warmup_chunks;
+    dv.test_stall_chunk = p.test_stall_chunk;
     dv.log_eps = p.log_eps;
     dv.alpha = p.alpha;
     dv.beta = p.beta;

@@ -40,6 +40,7 @@ struct ChunkedParams {
     int segments;                // runs per head
     float log_eps;
     int max_warmup_chunks;
+    int test_stall_chunk;        // > 0: never load this chunk (fault-injection test hook)
 };
 
 // Number of sequence segments per (batch, value head) the chunked prefill uses

@@ -38,7 +38,7 @@ class GdnShape(ctypes.Structure):
 
 class GdnPrefillOptions(ctypes.Structure):
     _fields_ = [("segments", ctypes.c_int32), ("log_eps", ctypes.c_float), ("max_warmup_chunks", ctypes.c_int32),
-                ("algorithm", ctypes.c_int32)]
+                ("algorithm", ctypes.c_int32), ("test_stall_chunk", ctypes.c_int32)]
 
 
 class GdnError(RuntimeError):
@@ -144,7 +144,7 @@ def new_workspace(shape: GdnShape, device) -> torch.Tensor:
 
 
 def prefill(q, k, v, alpha, beta, S0=None, *, y=None, S_T=None, workspace=None, segments=0, log_eps=0.0,
-            max_warmup_chunks=0, algorithm=ALGO_AUTO, stream=None):
+            max_warmup_chunks=0, algorithm=ALGO_AUTO, test_stall_chunk=0, stream=None):
     """Run gdn_prefill_ex on device tensors; returns (y, S_T).
 
     q, k [B,T,Hqk,d]; v [B,T,Hv,d]; alpha, beta [B,T,Hv] fp32; S0 [B,Hv,d,d] fp32 or None.
@@ -157,7 +157,7 @@ def prefill(q, k, v, alpha, beta, S0=None, *, y=None, S_T=None, workspace=None, 
         S_T = torch.empty((shape.B, shape.Hv, shape.dk, shape.dv), dtype=torch.float32, device=v.device)
     if workspace is None:
         workspace = new_workspace(shape, v.device)
-    opts = GdnPrefillOptions(segments, log_eps, max_warmup_chunks, algorithm)
+    opts = GdnPrefillOptions(segments, log_eps, max_warmup_chunks, algorithm, test_stall_chunk)
     rc = lib().gdn_prefill_ex(ctypes.byref(shape), ctypes.byref(opts), _ptr(q), _ptr(k), _ptr(v), _ptr(alpha),
                               _ptr(beta), _ptr(S0), _ptr(y), _ptr(S_T), _ptr(workspace),
                               workspace.numel() * workspace.element_size(), _stream(stream))

@@ -87,6 +87,8 @@ def test_prefill_rejects_bad_arguments(L):
     assert call_prefill(L, shape(), opts=bad) == E["GDN_ERR_INVALID_ARG"]
     bad = gdn.GdnPrefillOptions(0, 0.0, 0, 3)
     assert call_prefill(L, shape(), opts=bad) == E["GDN_ERR_INVALID_ARG"]
+    bad = gdn.GdnPrefillOptions(0, 0.0, 0, 0, -1)
+    assert call_prefill(L, shape(), opts=bad) == E["GDN_ERR_INVALID_ARG"]
 
 
 def test_decode_rejects_bad_arguments(L):
