@@ -65,6 +65,26 @@ def decode_bytes(w: dict, esz: int = 2) -> int:
     return 2 * B * Hv * d * d * 4 + (2 * B * Hqk * d + 2 * B * Hv * d) * esz + 2 * B * Hv * 4
 
 
+# DRAM bytes per launch measured by ncu (dram__bytes_read.sum + dram__bytes_write.sum,
+# summaries under profiles/), valid only for the kernel sources they were taken on:
+# a changed source reports null instead.
+MEASURED_TRAFFIC = {
+    "prefill": {"sources": ("csrc/chunked_tc.cu", "csrc/tc_ptx.cuh"), "sha256_16": "aebd32b4a6913187", "bytes": 1.674376e9},
+    "decode": {"sources": ("csrc/recurrent.cu",), "sha256_16": "f853d2d1c9ebcc76", "bytes": 1.021497e9},
+}
+
+
+def measured_traffic(kind: str):
+    import hashlib
+
+    rec = MEASURED_TRAFFIC[kind]
+    h = hashlib.sha256()
+    for rel in rec["sources"]:
+        with open(os.path.join(ROOT, "linear_attention_recurrence_14_b300", rel), "rb") as f:
+            h.update(f.read())
+    return rec["bytes"] if h.hexdigest()[:16] == rec["sha256_16"] else None
+
+
 def load_peaks() -> dict:
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -306,7 +326,8 @@ def run_ours(args, ws, rank, local):
     achieved_tflops = flops / kern_s / 1e12
     roofline = {
         "bound": "hbm", "achieved": achieved_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-        "frac": achieved_gbs / peaks["hbm_gbs"], "traffic": args.traffic,
+        "frac": achieved_gbs / peaks["hbm_gbs"],
+        "traffic": args.traffic if args.traffic is not None else measured_traffic("prefill"),
         "peak_source": peaks["source"], "bytes_per_launch": pbytes, "launch_ms": kern_s * 1e3,
         "tensor": {"achieved": achieved_tflops, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                    "frac": achieved_tflops / peaks["bf16_tflops"],
@@ -462,7 +483,9 @@ def time_decode(args, peaks, seed, dev, ws, local):
         "value": nsteps * ws / (total_ms * 1e-3), "unit": "steps/s", "steps": nsteps, "ms_per_step": total_ms / nsteps,
         "gpu_launches": nsteps,
         "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                     "frac": gbs / peaks["hbm_gbs"], "traffic": args.decode_traffic, "bytes_per_launch": nbytes,
+                     "frac": gbs / peaks["hbm_gbs"],
+                     "traffic": args.decode_traffic if args.decode_traffic is not None else measured_traffic("decode"),
+                     "bytes_per_launch": nbytes,
                      "launch_ms": kern_s * 1e3, "peak_source": peaks["source"]},
         "clocks": clk.summary(),
         "l2": "state 512 MiB > L2, no flush",
