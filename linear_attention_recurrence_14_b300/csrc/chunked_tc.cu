@@ -322,18 +322,19 @@ __device__ __forceinline__ uint32_t operand_offset(const MmaOperand &o, uint32_t
     return (kk >> o.shift) * o.big + (kk & ((1u << o.shift) - 1u)) * o.small;
 }
 
-// NK consecutive K=16 MMAs of one product (unrolled; the descriptors are
-// precomputed, each step adds a constant offset).
-template <int NK>
+// NK consecutive K=16 MMAs of one product, issued warp-wide (unrolled; the
+// descriptors are precomputed, each step adds a constant offset).  TMEM_A:
+// A is read from tensor memory (a.tmem) instead of shared memory (a.desc).
+template <int NK, bool TMEM_A>
 __device__ __forceinline__ void mma_run_t(uint32_t d, const MmaOperand &a, const MmaOperand &b, uint32_t idesc, uint32_t acc) {
 #pragma unroll
     for (int kk = 0; kk < NK; ++kk) {
         const uint64_t bd = b.desc + (operand_offset(b, kk) >> 4);
         const uint32_t accumulate = acc | (kk > 0 ? 1u : 0u);
-        if (a.tmem)
-            mma_bf16_ts(d, a.tmem + operand_offset(a, kk), bd, idesc, accumulate);
+        if constexpr (TMEM_A)
+            mma_bf16_ts_w(d, a.tmem + operand_offset(a, kk), bd, idesc, accumulate);
         else
-            mma_bf16(d, a.desc + (operand_offset(a, kk) >> 4), bd, idesc, accumulate);
+            mma_bf16_w(d, a.desc + (operand_offset(a, kk) >> 4), bd, idesc, accumulate);
     }
 }
 
@@ -557,7 +558,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
+        // The whole warp runs this role's control flow, so descriptors and TMEM
+        // addresses stay warp-uniform; one elected lane issues each MMA and commit.
+        {
+            auto wait = [&](uint64_t *bar, uint32_t parity) {
+                return warp_ok(bwait(bar, parity, abort_flag, p.status));
+            };
             constexpr uint32_t ID_KK = idesc_bf16(128, 64, false, false);   // A, B K-major
             constexpr uint32_t ID_MK = idesc_bf16(128, 64, true, false);    // A MN-major
             constexpr uint32_t ID_TS = idesc_bf16(128, 64, false, false);   // A in TMEM, B K-major
@@ -574,71 +580,71 @@ __global__ void __launch_bounds__(kThreads, 1)
             };
             auto gram = [&](int j) {
                 const MmaOperand kq = smem_kmajor(kq_addr(j % kStages), 16384u);
-                mma_run_t<8>(tb + TM_GW + (j & 1) * 64, kq, kq, ID_KK, 0u);
+                mma_run_t<8, false>(tb + TM_GW + (j & 1) * 64, kq, kq, ID_KK, 0u);
             };
             auto wu = [&](int j) {
                 const int s = j % kStages;
-                mma_run_t<4>(tb + TM_GW + (j & 1) * 64, smem_mnmajor(kq_addr(s), 16384u), smem_kmajor(t1, 0u), ID_MK, 0u);
-                mma_run_t<4>(tb + TM_ZU, smem_mnmajor(vw_addr(s), 8192u), smem_kmajor(t2, 0u), ID_MK, 0u);
+                mma_run_t<4, false>(tb + TM_GW + (j & 1) * 64, smem_mnmajor(kq_addr(s), 16384u), smem_kmajor(t1, 0u), ID_MK, 0u);
+                mma_run_t<4, false>(tb + TM_ZU, smem_mnmajor(vw_addr(s), 8192u), smem_kmajor(t2, 0u), ID_MK, 0u);
             };
             bool ok = true;
             do {
-                if (!(ok = bwait(&bars[B_FULL + 0], 0, abort_flag, p.status))) break;
+                if (!(ok = wait(&bars[B_FULL + 0], 0))) break;
                 tc_fence_after();
                 gram(0);
-                mma_commit(&bars[B_GRAM + 0]);
+                mma_commit_w(&bars[B_GRAM + 0]);
                 if (n > 1) {
-                    if (!(ok = bwait(&bars[B_FULL + 1 % kStages], (1 / kStages) & 1, abort_flag, p.status))) break;
+                    if (!(ok = wait(&bars[B_FULL + 1 % kStages], (1 / kStages) & 1))) break;
                     tc_fence_after();
                     gram(1);
-                    mma_commit(&bars[B_GRAM + 1]);
+                    mma_commit_w(&bars[B_GRAM + 1]);
                 }
-                if (!(ok = bwait(&bars[B_TREADY], 0, abort_flag, p.status))) break;
+                if (!(ok = wait(&bars[B_TREADY], 0))) break;
                 tc_fence_after();
                 wu(0);
-                mma_commit(&bars[B_WU]);
+                mma_commit_w(&bars[B_WU]);
                 for (int j = 0; j < n && ok; ++j) {
                     const int s = j % kStages;
                     const uint32_t zu = tb + TM_ZU;
                     const uint32_t sb = tb + TM_SB + (j & 1) * 64;
-                    if (!(ok = bwait(&bars[B_OPS], j & 1, abort_flag, p.status))) break;
-                    if (!(ok = bwait(&bars[B_SREADY], j & 1, abort_flag, p.status))) break;
+                    if (!(ok = wait(&bars[B_OPS], j & 1))) break;
+                    if (!(ok = wait(&bars[B_SREADY], j & 1))) break;
                     tc_fence_after();
                     // U^T = U~^T + S^T (-W)^T   (-W^T stored [dk][tokens], MN-major)
                     const MmaOperand sa{0ull, sb, 0u, 8u, 3u};          // S^T bf16: 8 columns per K step
                     const MmaOperand ua{0ull, zu, 32u, 8u, 1u};         // U^T bf16: tokens 0-31 at 0-15, 32-63 at 32-47
-                    mma_run_t<8>(zu, sa, smem_mnmajor(vw_addr(s), 16u), ID_TSM, 1u);
-                    mma_commit(&bars[B_UFULL]);
+                    mma_run_t<8, true>(zu, sa, smem_mnmajor(vw_addr(s), 16u), ID_TSM, 1u);
+                    mma_commit_w(&bars[B_UFULL]);
                     // Gram of chunk j+2 into the GW buffer W^T(j) occupied (read before
                     // OPS(j)); it runs while the chain converts U^T, before MMA2 is issued.
                     if (j + 2 < n) {
                         const int s2 = (j + 2) % kStages;
-                        if (!(ok = bwait(&bars[B_FULL + s2], ((j + 2) / kStages) & 1, abort_flag, p.status))) break;
+                        if (!(ok = wait(&bars[B_FULL + s2], ((j + 2) / kStages) & 1))) break;
                         tc_fence_after();
                         gram(j + 2);
-                        mma_commit(&bars[B_GRAM + (j & 1)]);
+                        mma_commit_w(&bars[B_GRAM + (j & 1)]);
                     }
-                    if (!(ok = bwait(&bars[B_USMEM], j & 1, abort_flag, p.status))) break;
+                    if (!(ok = wait(&bars[B_USMEM], j & 1))) break;
                     tc_fence_after();
                     // dS^T = U^T K~
-                    mma_run_t<4>(tb + TM_D, ua, smem_mnmajor(kq_addr(s), 16384u), ID_TD, 0u);
-                    mma_commit(&bars[B_DFULL]);
-                    if (j > 0 && !(ok = bwait(&bars[B_YFREE], (j - 1) & 1, abort_flag, p.status))) break;
+                    mma_run_t<4, true>(tb + TM_D, ua, smem_mnmajor(kq_addr(s), 16384u), ID_TD, 0u);
+                    mma_commit_w(&bars[B_DFULL]);
+                    if (j > 0 && !(ok = wait(&bars[B_YFREE], (j - 1) & 1))) break;
                     tc_fence_after();
                     // Y^T = S^T Q~^T + U^T P^T
-                    mma_run_t<8>(tb + TM_Y, sa, smem_kmajor(kq_addr(s) + 8192, 16384u), ID_TS, 0u);
-                    mma_run_t<4>(tb + TM_Y, ua, smem_kmajor(p_addr(s), 0u), ID_TS, 1u);
-                    mma_commit(&bars[B_YFULL]);
-                    mma_commit(&bars[B_EMPTY + s]);
+                    mma_run_t<8, true>(tb + TM_Y, sa, smem_kmajor(kq_addr(s) + 8192, 16384u), ID_TS, 0u);
+                    mma_run_t<4, true>(tb + TM_Y, ua, smem_kmajor(p_addr(s), 0u), ID_TS, 1u);
+                    mma_commit_w(&bars[B_YFULL]);
+                    mma_commit_w(&bars[B_EMPTY + s]);
                     if (j + 1 < n) {
-                        if (!(ok = bwait(&bars[B_TREADY], (j + 1) & 1, abort_flag, p.status))) break;
+                        if (!(ok = wait(&bars[B_TREADY], (j + 1) & 1))) break;
                         tc_fence_after();
                         wu(j + 1);
-                        mma_commit(&bars[B_WU]);
+                        mma_commit_w(&bars[B_WU]);
                     }
                 }
             } while (false);
-            mma_commit(&bars[B_FINAL]);
+            mma_commit_w(&bars[B_FINAL]);
         }
     } else if (warp < 4) {
         // ------------------------------------------------------------ gate warps (2, 3)
