@@ -75,8 +75,7 @@ constexpr int kBS = 24;
 constexpr int kBlk = 16 * kBS;
 constexpr uint32_t OFF_AT = OFF_T2 + 64 * 128;
 constexpr uint32_t OFF_TM = OFF_AT + 10 * kBlk * 4;
-constexpr uint32_t OFF_R = OFF_TM + 10 * kBlk * 4;      // 4 warps x [16][kBS]
-constexpr uint32_t OFF_GATES = OFF_R + 4 * kBlk * 4;
+constexpr uint32_t OFF_GATES = OFF_TM + 10 * kBlk * 4;
 // gates, double-buffered by chunk parity: g, u = gamma, w = 1/gamma, beta,
 // beta gamma (64 floats each), misc (64)
 constexpr int kGateFloats = 6 * 64;
@@ -204,19 +203,66 @@ __device__ __forceinline__ float warp_sum(float v) {
     return v;
 }
 
-// Off-diagonal blocks of block column J of T = (I + A)^{-1} (one warp):
-// T_IJ = -T_II R, R = sum_{K=J}^{I-1} A_IK T_KJ, for I = J+1..3, with tf32 warp
-// MMAs (m16n8k8, fp32 accumulation; fp32 operands are passed as is, the
-// tensor core reads their tf32 part).  Writes T_IJ as fp32 (row-major block)
-// and as bf16 T1 = T diag(beta gamma), T2 = T diag(beta).  Loops are kept
-// rolled: the kernel's hot code has to fit the instruction cache.
+// Off-diagonal blocks of T = (I + A)^{-1} from its diagonal blocks T_II, in
+// left-factor form: with F_IK = T_II A_IK (K < I),
+//   T_IJ = -sum_{K=J}^{I-1} F_IK T_KJ      (I > J),
+// so each block column is a chain of plain products once every F is known.
+// Warp MMAs m16n8k8 tf32 with fp32 accumulation (fp32 operands are passed as
+// is; the tensor core reads their tf32 part).
 //
-// NNT = 2 does the whole 16-column block column; NNT = 1 only its 8-column
-// tile nt0 (the two tiles are independent through every level, so block
-// column 0, the longest chain, is split over two warps).
+// Step 1 (solve_factors): the six F_IK, as twelve 8-column tiles, three per
+// warp, written in place of A_IK (column-major within the block: a warp only
+// reads and writes the columns of its own tiles).
+struct FactorJob {
+    uint8_t I, K, nt;
+};
+__constant__ FactorJob kFactorJobs[4][3] = {
+    {{1, 0, 0}, {1, 0, 1}, {2, 0, 0}},
+    {{2, 1, 0}, {2, 1, 1}, {2, 0, 1}},
+    {{3, 2, 0}, {3, 2, 1}, {3, 1, 0}},
+    {{3, 0, 0}, {3, 0, 1}, {3, 1, 1}},
+};
+
+__device__ __forceinline__ void solve_factors(int lw, float *At, const float *Tm, int lane) {
+    const int gq = lane >> 2, t4 = lane & 3;
+    float acc[3][2][4];
+    float *fb[3];
+    int col[3];
+#pragma unroll
+    for (int u = 0; u < 3; ++u) {
+        const FactorJob jb = kFactorJobs[lw][u];
+        const int I = jb.I, K = jb.K;
+        const float *Td = Tm + (I * (I + 1) / 2 + I) * kBlk;   // T_II[r][k] at r*kBS + k
+        fb[u] = At + (I * (I + 1) / 2 + K) * kBlk;             // A_IK[k][n] at n*kBS + k
+        col[u] = 8 * jb.nt + gq;
+#pragma unroll
+        for (int ks = 0; ks < 2; ++ks) {
+            const int k0 = 8 * ks;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[u][ks][e] = 0.f;
+            mma_tf32(acc[u][ks], __float_as_uint(Td[gq * kBS + k0 + t4]), __float_as_uint(Td[(gq + 8) * kBS + k0 + t4]),
+                     __float_as_uint(Td[gq * kBS + k0 + t4 + 4]), __float_as_uint(Td[(gq + 8) * kBS + k0 + t4 + 4]),
+                     __float_as_uint(fb[u][col[u] * kBS + k0 + t4]), __float_as_uint(fb[u][col[u] * kBS + k0 + t4 + 4]));
+        }
+    }
+    __syncwarp();
+#pragma unroll
+    for (int u = 0; u < 3; ++u) {
+        // accumulator (row gq (+8), column 2 t4 (+1) of the tile) -> F[r][n] at n*kBS + r
+        float *f = fb[u] + (col[u] - gq + 2 * t4) * kBS + gq;
+        f[0] = acc[u][0][0] + acc[u][1][0];
+        f[kBS] = acc[u][0][1] + acc[u][1][1];
+        f[8] = acc[u][0][2] + acc[u][1][2];
+        f[kBS + 8] = acc[u][0][3] + acc[u][1][3];
+    }
+}
+
+// Step 2: block column J (NNT = 2: both 8-column tiles; NNT = 1: tile nt0 only),
+// T_IJ for I = J+1..3 in order.  Writes T_IJ as fp32 (row-major, for the next
+// block of the column) and as bf16 T1 = T diag(beta gamma), T2 = T diag(beta).
 template <int NNT>
-__device__ __forceinline__ void merge_column(int J, int nt0, const float *At, float *Tm, float *Rw, uint8_t *t1b,
-                                             uint8_t *t2b, const float *s_b, const float *s_bu, int lane) {
+__device__ __forceinline__ void solve_column(int J, int nt0, const float *At, float *Tm, uint8_t *t1b, uint8_t *t2b,
+                                             const float *s_b, const float *s_bu, int lane) {
     const int gq = lane >> 2, t4 = lane & 3;
 #pragma unroll 1
     for (int I = J + 1; I < 4; ++I) {
@@ -224,17 +270,17 @@ __device__ __forceinline__ void merge_column(int J, int nt0, const float *At, fl
         float e0[4] = {0.f, 0.f, 0.f, 0.f}, e1[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll 1
         for (int K = J; K < I; ++K) {
-            const float *Ab = At + (I * (I + 1) / 2 + K) * kBlk;   // A[r][k] at k*kBS + r
+            const float *Fb = At + (I * (I + 1) / 2 + K) * kBlk;   // F[r][k] at k*kBS + r
             const float *Bb = Tm + (K * (K + 1) / 2 + J) * kBlk;   // T[k][n] at k*kBS + n
             // k-steps 0 and 1 into separate accumulators: two independent MMA chains
             uint32_t a[2][4], b[2][2][2];
 #pragma unroll
             for (int ks = 0; ks < 2; ++ks) {
                 const int k0 = 8 * ks;
-                a[ks][0] = __float_as_uint(Ab[(k0 + t4) * kBS + gq]);
-                a[ks][1] = __float_as_uint(Ab[(k0 + t4) * kBS + gq + 8]);
-                a[ks][2] = __float_as_uint(Ab[(k0 + t4 + 4) * kBS + gq]);
-                a[ks][3] = __float_as_uint(Ab[(k0 + t4 + 4) * kBS + gq + 8]);
+                a[ks][0] = __float_as_uint(Fb[(k0 + t4) * kBS + gq]);
+                a[ks][1] = __float_as_uint(Fb[(k0 + t4) * kBS + gq + 8]);
+                a[ks][2] = __float_as_uint(Fb[(k0 + t4 + 4) * kBS + gq]);
+                a[ks][3] = __float_as_uint(Fb[(k0 + t4 + 4) * kBS + gq + 8]);
 #pragma unroll
                 for (int nt = 0; nt < NNT; ++nt) {
                     b[ks][nt][0] = __float_as_uint(Bb[(k0 + t4) * kBS + 8 * (nt0 + nt) + gq]);
@@ -248,43 +294,19 @@ __device__ __forceinline__ void merge_column(int J, int nt0, const float *At, fl
                 mma_tf32(e1, a[1][0], a[1][1], a[1][2], a[1][3], b[1][NNT - 1][0], b[1][NNT - 1][1]);
             }
         }
-        {
-            const int cb = 8 * nt0 + 2 * t4;
-            *reinterpret_cast<float2 *>(Rw + gq * kBS + cb) = make_float2(c0[0] + e0[0], c0[1] + e0[1]);
-            *reinterpret_cast<float2 *>(Rw + (gq + 8) * kBS + cb) = make_float2(c0[2] + e0[2], c0[3] + e0[3]);
-            if (NNT == 2) {
-                *reinterpret_cast<float2 *>(Rw + gq * kBS + 8 + cb) = make_float2(c1[0] + e1[0], c1[1] + e1[1]);
-                *reinterpret_cast<float2 *>(Rw + (gq + 8) * kBS + 8 + cb) = make_float2(c1[2] + e1[2], c1[3] + e1[3]);
-            }
-        }
-        __syncwarp();
-        float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
-        const float *Td = Tm + (I * (I + 1) / 2 + I) * kBlk;       // T[r][k] at r*kBS + k
-#pragma unroll
-        for (int ks = 0; ks < 2; ++ks) {
-            const int k0 = 8 * ks;
-            const uint32_t a0 = __float_as_uint(Td[gq * kBS + k0 + t4]);
-            const uint32_t a1 = __float_as_uint(Td[(gq + 8) * kBS + k0 + t4]);
-            const uint32_t a2 = __float_as_uint(Td[gq * kBS + k0 + t4 + 4]);
-            const uint32_t a3 = __float_as_uint(Td[(gq + 8) * kBS + k0 + t4 + 4]);
-            mma_tf32(d0, a0, a1, a2, a3, __float_as_uint(Rw[(k0 + t4) * kBS + 8 * nt0 + gq]),
-                     __float_as_uint(Rw[(k0 + t4 + 4) * kBS + 8 * nt0 + gq]));
-            if (NNT == 2)
-                mma_tf32(d1, a0, a1, a2, a3, __float_as_uint(Rw[(k0 + t4) * kBS + 8 + gq]),
-                         __float_as_uint(Rw[(k0 + t4 + 4) * kBS + 8 + gq]));
-        }
         float *Tb = Tm + (I * (I + 1) / 2 + J) * kBlk;
 #pragma unroll
         for (int nt = 0; nt < NNT; ++nt) {
-            const float *dd = nt ? d1 : d0;
+            const float *cc = nt ? c1 : c0;
+            const float *ee = nt ? e1 : e0;
             const int cn = 8 * (nt0 + nt) + 2 * t4;
             const int C = 16 * J + cn;
             const float sa0 = s_bu[C], sa1 = s_bu[C + 1], sb0 = s_b[C], sb1 = s_b[C + 1];
 #pragma unroll
             for (int hr = 0; hr < 2; ++hr) {
                 const int r = gq + 8 * hr;
-                const float v0 = -dd[2 * hr], v1 = -dd[2 * hr + 1];
-                *reinterpret_cast<float2 *>(Tb + r * kBS + cn) = make_float2(v0, v1);
+                const float v0 = -(cc[2 * hr] + ee[2 * hr]), v1 = -(cc[2 * hr + 1] + ee[2 * hr + 1]);
+                if (I < 3) *reinterpret_cast<float2 *>(Tb + r * kBS + cn) = make_float2(v0, v1);
                 const uint32_t off = sw128_elem(16 * I + r, C);
                 *reinterpret_cast<uint32_t *>(t1b + off) = pack_bf16(v0 * sa0, v1 * sa1);
                 *reinterpret_cast<uint32_t *>(t2b + off) = pack_bf16(v0 * sb0, v1 * sb1);
@@ -708,7 +730,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t q = lw;
         float *At = reinterpret_cast<float *>(sm + OFF_AT);
         float *Tm = reinterpret_cast<float *>(sm + OFF_TM);
-        float *Rw = reinterpret_cast<float *>(sm + OFF_R) + lw * 16 * kBS;
         uint8_t *t1b = sm + OFF_T1, *t2b = sm + OFF_T2;
         // Blocks of T1, T2 above the block diagonal are never written: zero them once.
         for (int e = l; e < 2 * 64 * 128 / 16; e += 128)
@@ -822,14 +843,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float *s_g = sg, *s_b = sg + 192, *s_bu = sg + 256, *s_misc = sg + 320;
                 const bool fast = s_misc[2] != 0.f;
                 named_bar(1, 128);   // A, diagonal T blocks and P of chunk j are written
-                // bf16 T1, T2 of diagonal block lw, then the off-diagonal blocks T_IJ:
-                // block column 0 split over warps 0 and 3 (one 8-column tile each),
-                // column 1 on warp 1, column 2 on warp 2.
+                // The factors F_IK (three tiles per warp) and bf16 T1, T2 of diagonal
+                // block lw; then the off-diagonal blocks T_IJ by block column: column 0
+                // split over warps 0 and 3 (one 8-column tile each), column 1 on warp 1,
+                // column 2 on warp 2.
+                solve_factors(lw, At, Tm, lane);
                 diag_block_to_bf16(lw, Tm, t1b, t2b, s_b, s_bu, lane);
+                named_bar(2, 128);   // every F_IK is written
                 if (lw == 0 || lw == 3)
-                    merge_column<1>(0, lw == 3 ? 1 : 0, At, Tm, Rw, t1b, t2b, s_b, s_bu, lane);
+                    solve_column<1>(0, lw == 3 ? 1 : 0, At, Tm, t1b, t2b, s_b, s_bu, lane);
                 else
-                    merge_column<2>(lw, 0, At, Tm, Rw, t1b, t2b, s_b, s_bu, lane);
+                    solve_column<2>(lw, 0, At, Tm, t1b, t2b, s_b, s_bu, lane);
                 fence_proxy_async();
                 mbar_arrive(&bars[B_TREADY]);
                 named_bar(1, 128);   // A and T of chunk j are no longer read
