@@ -344,12 +344,13 @@ __device__ __forceinline__ uint32_t operand_offset(const MmaOperand &o, uint32_t
     return (kk >> o.shift) * o.big + (kk & ((1u << o.shift) - 1u)) * o.small;
 }
 
-// NK consecutive K=16 MMAs of one product, issued warp-wide (unrolled; the
-// descriptors are precomputed, each step adds a constant offset).  TMEM_A:
+// NK consecutive K=16 MMAs of one product, issued warp-wide (a rolled loop:
+// the issuing warp's code stays small; each step adds a constant offset to
+// the descriptors).  TMEM_A:
 // A is read from tensor memory (a.tmem) instead of shared memory (a.desc).
 template <int NK, bool TMEM_A>
 __device__ __forceinline__ void mma_run_t(uint32_t d, const MmaOperand &a, const MmaOperand &b, uint32_t idesc, uint32_t acc) {
-#pragma unroll
+#pragma unroll 1
     for (int kk = 0; kk < NK; ++kk) {
         const uint64_t bd = b.desc + (operand_offset(b, kk) >> 4);
         const uint32_t accumulate = acc | (kk > 0 ? 1u : 0u);
@@ -546,8 +547,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tb = misc->tmem_base;
+    const uint32_t tb_s = tb;
     const int c_w = misc->c_w;
     const int n = c_end - c_w;
+    const int n_s = n;
     const bool use_s0 = c_w == 0 && p.S0 != nullptr;
 
     const uint32_t smb = smem_u32(sm);
@@ -586,6 +589,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             auto wait = [&](uint64_t *bar, uint32_t parity) {
                 return warp_ok(bwait(bar, parity, abort_flag, p.status));
             };
+            // Values read from shared memory, broadcast so that the compiler treats
+            // them (and every descriptor derived from them) as warp-uniform.
+            const uint32_t tb = __shfl_sync(0xffffffffu, tb_s, 0);
+            const int n = __shfl_sync(0xffffffffu, n_s, 0);
             constexpr uint32_t ID_KK = idesc_bf16(128, 64, false, false);   // A, B K-major
             constexpr uint32_t ID_MK = idesc_bf16(128, 64, true, false);    // A MN-major
             constexpr uint32_t ID_TS = idesc_bf16(128, 64, false, false);   // A in TMEM, B K-major

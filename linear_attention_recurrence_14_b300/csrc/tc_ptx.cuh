@@ -174,16 +174,16 @@ __device__ __forceinline__ void mma_commit(uint64_t *bar) {
                  : "memory");
 }
 
-// Warp-wide forms of the three instructions above: every lane of a converged
-// warp executes the call with the same (warp-uniform) operands and one lane,
-// chosen by elect.sync (the same lane every time while the warp is
-// converged), issues the instruction, so one lane issues and commits all of
+// Warp-wide forms of the three instructions above: every lane of the warp
+// executes the call with the same (warp-uniform) operands and lane 0 alone
+// issues the instruction (a predicate on %laneid, not elect.sync, which costs
+// a reconvergence sequence per call), so one thread issues and commits all of
 // the warp's MMAs.
 __device__ __forceinline__ void mma_bf16_w(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                            uint32_t accumulate) {
     asm volatile(
         "{\n\t.reg .pred e, p;\n\t.reg .b32 r;\n\t"
-        "elect.sync r|e, 0xffffffff;\n\t"
+        "mov.u32 r, %%laneid;\n\tsetp.eq.u32 e, r, 0;\n\t"
         "setp.ne.b32 p, %4, 0;\n\t"
         "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
         "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
@@ -194,7 +194,7 @@ __device__ __forceinline__ void mma_bf16_ts_w(uint32_t d_tmem, uint32_t a_tmem, 
                                               uint32_t accumulate) {
     asm volatile(
         "{\n\t.reg .pred e, p;\n\t.reg .b32 r;\n\t"
-        "elect.sync r|e, 0xffffffff;\n\t"
+        "mov.u32 r, %%laneid;\n\tsetp.eq.u32 e, r, 0;\n\t"
         "setp.ne.b32 p, %4, 0;\n\t"
         "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
         "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
@@ -204,7 +204,7 @@ __device__ __forceinline__ void mma_bf16_ts_w(uint32_t d_tmem, uint32_t a_tmem, 
 __device__ __forceinline__ void mma_commit_w(uint64_t *bar) {
     asm volatile(
         "{\n\t.reg .pred e;\n\t.reg .b32 r;\n\t"
-        "elect.sync r|e, 0xffffffff;\n\t"
+        "mov.u32 r, %%laneid;\n\tsetp.eq.u32 e, r, 0;\n\t"
         "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(smem_u32(bar))
         : "memory");
 }
