@@ -59,7 +59,7 @@ constexpr uint64_t kWaitLimitNs = 1000000000ull;  // bounded waits: 1 s
 // Shared-memory layout (offsets from a 1024-byte aligned base).  Operand
 // tiles use the 128-byte swizzle: rows of 128 bytes (64 bf16), 16-byte chunk
 // c of row r stored at chunk position c ^ (r & 7).
-constexpr uint32_t kKQBytes = 2 * 128 * 128;  // [kb][128 rows][64]: K rows 0-63, Q rows 64-127
+constexpr uint32_t kKQBytes = 2 * 128 * 128;  // [kb][128 rows][64]: Q rows 0-63, K rows 64-127
 constexpr uint32_t kVWBytes = 2 * 64 * 128;   // [kb][64 rows][64]: V; later -W^T as [128 dk][64 tokens]
 constexpr uint32_t kPBytes = 64 * 128;        // [64 rows][64]
 constexpr uint32_t OFF_KQ = 0;
@@ -84,7 +84,7 @@ constexpr uint32_t OFF_CHAIN = OFF_GATES + 2 * kGateFloats * 4;
 constexpr int kChainFloats = 132;
 constexpr int kChainSlots = 4;
 constexpr uint32_t OFF_BAR = OFF_CHAIN + kChainSlots * kChainFloats * 4;
-constexpr int kNumBars = 22;
+constexpr int kNumBars = 23;
 constexpr uint32_t OFF_MISC = OFF_BAR + kNumBars * 8;
 constexpr uint32_t kSmemUsed = OFF_MISC + 64;
 constexpr uint32_t kSmemBytes = kSmemUsed + 1024;  // + alignment slack
@@ -107,8 +107,9 @@ enum Bar {
     B_FINAL,              // every MMA issued is complete
     B_GFULL,              // + buffer: gates of a chunk written (gate warps, 64 arrivals)
     B_GEMPTY = B_GFULL + 2,  // + buffer: gates of a chunk consumed (local, 128 arrivals)
+    B_SOLVED = B_GEMPTY + 2,  // A and the diagonal T blocks of a chunk written (gate warps, 64 arrivals)
 };
-static_assert(B_GEMPTY + 2 == kNumBars, "barrier count");
+static_assert(B_SOLVED + 1 == kNumBars, "barrier count");
 
 struct Misc {
     uint32_t tmem_base;
@@ -361,63 +362,122 @@ __device__ __forceinline__ void mma_run_t(uint32_t d, const MmaOperand &a, const
     }
 }
 
-// Exact gate path (a chunk whose decay is below e^kFastLogDecay): per-element
-// e^{g_i - g_j} for A and P, and Q~ = diag(gamma) Q in place.  Cold code.
-__device__ __noinline__ void exact_gram_rows(int j, int l, uint32_t q, uint32_t gw, float *At, uint8_t *pbuf,
-                                             uint8_t *kq, const float *s_g, const float *s_u, const float *s_b) {
-    (void)j;
+// A rows of a chunk (gate warps): row i of K K^T is TMEM lane 64 + i.  Written
+// into the block-packed layout, A[i][j] at blk(i/16, j/16) + (j%16)*kBS + i%16,
+// for j < i.  Fast gates: A_ij = (beta_i gamma_i) (1/gamma_j) (k_i.k_j).
+__device__ __forceinline__ void fast_a_rows(int i, uint32_t q, uint32_t gw, float *At, const float *s_w, const float *s_bu) {
+    const float ci = s_bu[i];
 #pragma unroll 1
     for (int half = 0; half < 2; ++half) {
         float gr[32];
         tmem_ld32(lane_addr(gw, q, 32 * half), gr);
         tmem_wait_ld();
-        if (l < 64) {
-            const int i = l;
-            const float bi = s_b[i], gi = s_g[i];
-            float *abase = At + (kBlkIdx[i >> 4][0] + 2 * half) * kBlk + (i & 15);
+        float *abase = At + (kBlkIdx[i >> 4][0] + 2 * half) * kBlk + (i & 15);
+        float wv[32];
 #pragma unroll
-            for (int cc = 0; cc < 32; ++cc) {
-                const int c = 32 * half + cc;
-                if (c < i) abase[(cc >> 4) * kBlk + (cc & 15) * kBS] = bi * expf(gi - s_g[c]) * gr[cc];
-            }
-        } else {
-            const int i = l - 64;
-            const float gi = s_g[i];
-            uint8_t *prow = pbuf + i * 128;
-#pragma unroll
-            for (int ch4 = 0; ch4 < 4; ++ch4) {
-                uint32_t w4[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int cc = 8 * ch4 + 2 * e, c = 32 * half + cc;
-                    w4[e] = pack_bf16(c <= i ? expf(gi - s_g[c]) * gr[cc] : 0.f,
-                                      c + 1 <= i ? expf(gi - s_g[c + 1]) * gr[cc + 1] : 0.f);
-                }
-                *reinterpret_cast<uint4 *>(prow + (((4 * half + ch4) ^ (i & 7)) << 4)) =
-                    make_uint4(w4[0], w4[1], w4[2], w4[3]);
-            }
+        for (int c4 = 0; c4 < 8; ++c4) {
+            const float4 f = *reinterpret_cast<const float4 *>(s_w + 32 * half + 4 * c4);
+            wv[4 * c4] = f.x * ci;
+            wv[4 * c4 + 1] = f.y * ci;
+            wv[4 * c4 + 2] = f.z * ci;
+            wv[4 * c4 + 3] = f.w * ci;
         }
+        const int lim = i - 32 * half;
+#pragma unroll
+        for (int cc = 0; cc < 32; ++cc)
+            if (cc < lim) abase[(cc >> 4) * kBlk + (cc & 15) * kBS] = gr[cc] * wv[cc];
     }
-    if (l >= 64) {
-        const int i = l - 64;
-        const float gam = s_u[i];
-        uint8_t *qrow = kq + (64 + i) * 128;
+}
+
+// Exact gate path (a chunk whose decay is below e^kFastLogDecay), A rows:
+// A_ij = beta_i e^{g_i - g_j} (k_i.k_j) per element.  Cold code.
+__device__ __noinline__ void exact_a_rows(int i, uint32_t q, uint32_t gw, float *At, const float *s_g, const float *s_b) {
+    const float bi = s_b[i], gi = s_g[i];
 #pragma unroll 1
-        for (int kb = 0; kb < 2; ++kb) {
+    for (int half = 0; half < 2; ++half) {
+        float gr[32];
+        tmem_ld32(lane_addr(gw, q, 32 * half), gr);
+        tmem_wait_ld();
+        float *abase = At + (kBlkIdx[i >> 4][0] + 2 * half) * kBlk + (i & 15);
 #pragma unroll
-            for (int ch = 0; ch < 8; ++ch) {
-                uint4 *ptr = reinterpret_cast<uint4 *>(qrow + kb * 16384 + ch * 16);
-                uint4 raw = *ptr;
-                __nv_bfloat162 *h2 = reinterpret_cast<__nv_bfloat162 *>(&raw);
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float2 f = __bfloat1622float2(h2[e]);
-                    h2[e] = __floats2bfloat162_rn(f.x * gam, f.y * gam);
-                }
-                *ptr = raw;
-            }
+        for (int cc = 0; cc < 32; ++cc) {
+            const int c = 32 * half + cc;
+            if (c < i) abase[(cc >> 4) * kBlk + (cc & 15) * kBS] = bi * expf(gi - s_g[c]) * gr[cc];
         }
     }
+}
+
+// Exact gate path, P rows (row i of Q K^T is TMEM lane i): P_ij = e^{g_i - g_j}
+// (q_i.k_j) for j <= i, and Q~ = diag(gamma) Q in place.  Cold code.
+__device__ __noinline__ void exact_p_rows(int i, uint32_t q, uint32_t gw, uint8_t *pbuf, uint8_t *kq, const float *s_g,
+                                          const float *s_u) {
+    const float gi = s_g[i];
+#pragma unroll 1
+    for (int half = 0; half < 2; ++half) {
+        float gr[32];
+        tmem_ld32(lane_addr(gw, q, 32 * half), gr);
+        tmem_wait_ld();
+        uint8_t *prow = pbuf + i * 128;
+#pragma unroll
+        for (int ch4 = 0; ch4 < 4; ++ch4) {
+            uint32_t w4[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int cc = 8 * ch4 + 2 * e, c = 32 * half + cc;
+                w4[e] = pack_bf16(c <= i ? expf(gi - s_g[c]) * gr[cc] : 0.f,
+                                  c + 1 <= i ? expf(gi - s_g[c + 1]) * gr[cc + 1] : 0.f);
+            }
+            *reinterpret_cast<uint4 *>(prow + (((4 * half + ch4) ^ (i & 7)) << 4)) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+        }
+    }
+    const float gam = s_u[i];
+    uint8_t *qrow = kq + i * 128;
+#pragma unroll 1
+    for (int kb = 0; kb < 2; ++kb) {
+#pragma unroll
+        for (int ch = 0; ch < 8; ++ch) {
+            uint4 *ptr = reinterpret_cast<uint4 *>(qrow + kb * 16384 + ch * 16);
+            uint4 raw = *ptr;
+            __nv_bfloat162 *h2 = reinterpret_cast<__nv_bfloat162 *>(&raw);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float2 f = __bfloat1622float2(h2[e]);
+                h2[e] = __floats2bfloat162_rn(f.x * gam, f.y * gam);
+            }
+            *ptr = raw;
+        }
+    }
+}
+
+// Diagonal blocks of T = (I + A)^{-1} by forward substitution, one column per
+// thread (thread i: block i/16, column i%16; the calling warp wrote both of its
+// blocks' rows).  The block's strictly lower part (column m: rows m+1..15) is
+// loaded in two batches ahead of the arithmetic.
+__device__ __forceinline__ void diag_solve(int i, const float *At, float *Tm) {
+    const int blk = i >> 4, col = i & 15;
+    const float *Ab = At + kBlkIdx[blk][blk] * kBlk;
+    float t[16];
+#pragma unroll
+    for (int r = 0; r < 16; ++r) t[r] = (r == col) ? 1.f : 0.f;
+#pragma unroll
+    for (int mb = 0; mb < 2; ++mb) {
+        constexpr int kSplit = 5;
+        float av[65];
+        const int m0 = mb ? kSplit : 0, m1 = mb ? 15 : kSplit;
+#pragma unroll
+        for (int m = m0; m < m1; ++m)
+#pragma unroll
+            for (int r = m + 1; r < 16; ++r)
+                av[(m * 16 - (m * (m + 1)) / 2 + (r - m - 1)) - (m0 * 16 - (m0 * (m0 + 1)) / 2)] = Ab[m * kBS + r];
+#pragma unroll
+        for (int m = m0; m < m1; ++m)
+#pragma unroll
+            for (int r = m + 1; r < 16; ++r)
+                t[r] = fmaf(-av[(m * 16 - (m * (m + 1)) / 2 + (r - m - 1)) - (m0 * 16 - (m0 * (m0 + 1)) / 2)], t[m], t[r]);
+    }
+    float *Tb = Tm + kBlkIdx[blk][blk] * kBlk + col;
+#pragma unroll
+    for (int r = 0; r < 16; ++r) Tb[r * kBS] = t[r];
 }
 
 // Exact gate path: K~ = diag(lambda) K in place, lambda_r = e^{g_C - g_r}.  Cold code.
@@ -427,7 +487,7 @@ __device__ __noinline__ void exact_scale_k(int l, uint8_t *kq, const float *s_g)
     for (int u = 0; u < 8; ++u) {
         const int idx = l + 128 * u;
         const int kb = idx >> 9, r = (idx >> 3) & 63, ch = idx & 7;
-        uint4 *ptr = reinterpret_cast<uint4 *>(kq + kb * 16384 + r * 128 + ch * 16);
+        uint4 *ptr = reinterpret_cast<uint4 *>(kq + kb * 16384 + 8192 + r * 128 + ch * 16);
         const float lam = expf(g63 - s_g[r]);
         uint4 raw = *ptr;
         __nv_bfloat162 *h2 = reinterpret_cast<__nv_bfloat162 *>(&raw);
@@ -484,6 +544,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&bars[B_GFULL + e], 64);
             mbar_init(&bars[B_GEMPTY + e], 128);
         }
+        mbar_init(&bars[B_SOLVED], 64);
 
         misc->abort = 0;
         fence_mbarrier_init();
@@ -574,8 +635,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint8_t *vw = sm + OFF_VW + s * kVWBytes;
 #pragma unroll
                 for (int kb = 0; kb < 2; ++kb) {
-                    tma_load_4d(kq + kb * 16384, &tm_k, &bars[B_FULL + s], kb * 64, hk, t0, b);
-                    tma_load_4d(kq + kb * 16384 + 8192, &tm_q, &bars[B_FULL + s], kb * 64, hk, t0, b);
+                    tma_load_4d(kq + kb * 16384, &tm_q, &bars[B_FULL + s], kb * 64, hk, t0, b);
+                    tma_load_4d(kq + kb * 16384 + 8192, &tm_k, &bars[B_FULL + s], kb * 64, hk, t0, b);
                     tma_load_4d(vw + kb * 8192, &tm_v, &bars[B_FULL + s], kb * 64, hv, t0, b);
                 }
                 loads_issued[s] = j + 1;
@@ -608,12 +669,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 return MmaOperand{sw128_desc(addr, lbo, 1024), 0u, 8192u, 2048u, 2u};
             };
             auto gram = [&](int j) {
-                const MmaOperand kq = smem_kmajor(kq_addr(j % kStages), 16384u);
-                mma_run_t<8, false>(tb + TM_GW + (j & 1) * 64, kq, kq, ID_KK, 0u);
+                // [Q;K] K^T: Q K^T in lanes 0-63, K K^T in lanes 64-127
+                const uint32_t a = kq_addr(j % kStages);
+                mma_run_t<8, false>(tb + TM_GW + (j & 1) * 64, smem_kmajor(a, 16384u), smem_kmajor(a + 8192, 16384u), ID_KK, 0u);
             };
             auto wu = [&](int j) {
                 const int s = j % kStages;
-                mma_run_t<4, false>(tb + TM_GW + (j & 1) * 64, smem_mnmajor(kq_addr(s), 16384u), smem_kmajor(t1, 0u), ID_MK, 0u);
+                mma_run_t<4, false>(tb + TM_GW + (j & 1) * 64, smem_mnmajor(kq_addr(s) + 8192, 16384u), smem_kmajor(t1, 0u), ID_MK, 0u);
                 mma_run_t<4, false>(tb + TM_ZU, smem_mnmajor(vw_addr(s), 8192u), smem_kmajor(t2, 0u), ID_MK, 0u);
             };
             bool ok = true;
@@ -656,12 +718,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (!(ok = wait(&bars[B_USMEM], j & 1))) break;
                     tc_fence_after();
                     // dS^T = U^T K~
-                    mma_run_t<4, true>(tb + TM_D, ua, smem_mnmajor(kq_addr(s), 16384u), ID_TD, 0u);
+                    mma_run_t<4, true>(tb + TM_D, ua, smem_mnmajor(kq_addr(s) + 8192, 16384u), ID_TD, 0u);
                     mma_commit_w(&bars[B_DFULL]);
                     if (j > 0 && !(ok = wait(&bars[B_YFREE], (j - 1) & 1))) break;
                     tc_fence_after();
                     // Y^T = S^T Q~^T + U^T P^T
-                    mma_run_t<8, true>(tb + TM_Y, sa, smem_kmajor(kq_addr(s) + 8192, 16384u), ID_TS, 0u);
+                    mma_run_t<8, true>(tb + TM_Y, sa, smem_kmajor(kq_addr(s), 16384u), ID_TS, 0u);
                     mma_run_t<4, true>(tb + TM_Y, ua, smem_kmajor(p_addr(s), 0u), ID_TS, 1u);
                     mma_commit_w(&bars[B_YFULL]);
                     mma_commit_w(&bars[B_EMPTY + s]);
@@ -678,6 +740,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp < 4) {
         // ------------------------------------------------------------ gate warps (2, 3)
         const int gt = tid - 64;
+        float *At = reinterpret_cast<float *>(sm + OFF_AT);
+        float *Tm = reinterpret_cast<float *>(sm + OFF_TM);
         const float *alpha_h = p.alpha + static_cast<int64_t>(b) * p.T * p.Hv + hv;
         const float *beta_h = p.beta + static_cast<int64_t>(b) * p.T * p.Hv + hv;
         float a_nxt = 1.f, b_nxt = 0.f;
@@ -729,6 +793,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                 s_misc[2] = fastc ? 1.f : 0.f;
             }
             mbar_arrive(&bars[B_GFULL + buf]);
+            named_bar(4, 64);   // this chunk's gates are visible to both gate warps
+            // A rows of chunk j (K K^T, TMEM lanes 64-127: row gt) and the diagonal
+            // blocks of T, once the local warpgroup is done with chunk j-1's A and
+            // T (TREADY(j-1)).
+            bool ok2 = j == 0 || bwait(&bars[B_TREADY], (j - 1) & 1, abort_flag, p.status);
+            ok2 = ok2 && bwait(&bars[B_GRAM + (j & 1)], (j >> 1) & 1, abort_flag, p.status);
+            if (!warp_ok(ok2)) break;
+            tc_fence_after();
+            const uint32_t gw = tb + TM_GW + (j & 1) * 64;
+            if (fastc)
+                fast_a_rows(gt, warp, gw, At, s_w, s_bu);
+            else
+                exact_a_rows(gt, warp, gw, At, s_g, s_b);
+            tc_fence_before();
+            __syncwarp();
+            diag_solve(gt, At, Tm);
+            mbar_arrive(&bars[B_SOLVED]);
         }
     } else if (warp >= 4 && warp < 8) {
         // ------------------------------------------------------------ local warpgroup
@@ -741,106 +822,53 @@ __global__ void __launch_bounds__(kThreads, 1)
         // Blocks of T1, T2 above the block diagonal are never written: zero them once.
         for (int e = l; e < 2 * 64 * 128 / 16; e += 128)
             reinterpret_cast<uint4 *>(t1b)[e] = make_uint4(0u, 0u, 0u, 0u);
-        // AP(j): gated Gram readout of chunk j -> A (warps 4-5, which then invert
-        // their two diagonal blocks) and P (warps 6-7).  Runs one chunk ahead of
-        // the W readout so the W^T MMA of chunk j overlaps it.
-        auto ap = [&](int j) -> bool {
+        // P rows of chunk j (Q K^T, TMEM lanes 0-63: warps 4-5, row l) as the bf16
+        // operand P^ = mask(Q K^T) / gamma_C (fast gates; y is scaled by the chain)
+        // or P = mask(e^{g_i - g_j} q_i.k_j) with Q~ = diag(gamma) Q (exact gates).
+        auto p_readout = [&](int j) -> bool {
             const int s = j % kStages;
             const int gbuf = j & 1;
             const float *sg = reinterpret_cast<const float *>(sm + OFF_GATES) + gbuf * kGateFloats;
-            const float *s_g = sg, *s_u = sg + 64, *s_w = sg + 128, *s_b = sg + 192, *s_bu = sg + 256,
-                        *s_misc = sg + 320;
+            const float *s_g = sg, *s_u = sg + 64, *s_misc = sg + 320;
             bool ok = bwait(&bars[B_GFULL + gbuf], (j >> 1) & 1, abort_flag, p.status);
             ok = ok && bwait(&bars[B_FULL + s], (j / kStages) & 1, abort_flag, p.status);
             ok = ok && bwait(&bars[B_GRAM + (j & 1)], (j >> 1) & 1, abort_flag, p.status);
             if (!warp_ok(ok)) return false;
-            const bool fast = s_misc[2] != 0.f;
+            if (l >= 64) return true;
+            const uint32_t gw = tb + TM_GW + (j & 1) * 64;
+            uint8_t *pbuf = sm + OFF_P + s * kPBytes;
             tc_fence_after();
-            if (fast) {
+            if (s_misc[2] != 0.f) {
+                const int i = l;
+                const float pinv = s_misc[1];
+                uint8_t *prow = pbuf + i * 128;
 #pragma unroll 1
                 for (int half = 0; half < 2; ++half) {
                     float gr[32];
-                    tmem_ld32(lane_addr(tb + TM_GW + (j & 1) * 64, q, 32 * half), gr);
+                    tmem_ld32(lane_addr(gw, q, 32 * half), gr);
                     tmem_wait_ld();
-                    if (l < 64) {
-                        // A row i = l: beta_i gamma_i w_j (k_i.k_j), j < i, into the block-packed
-                        // layout (A[i][j] at blk(i/16, j/16) + (j%16)*kBS + i%16); loads before stores.
-                        const int i = l;
-                        float *abase = At + (kBlkIdx[i >> 4][0] + 2 * half) * kBlk + (i & 15);
-                        const float ci = s_bu[i];
-                        float wv[32];
+                    const int lim = i - 32 * half;
 #pragma unroll
-                        for (int c4 = 0; c4 < 8; ++c4) {
-                            const float4 f = *reinterpret_cast<const float4 *>(s_w + 32 * half + 4 * c4);
-                            wv[4 * c4] = f.x * ci;
-                            wv[4 * c4 + 1] = f.y * ci;
-                            wv[4 * c4 + 2] = f.z * ci;
-                            wv[4 * c4 + 3] = f.w * ci;
+                    for (int ch4 = 0; ch4 < 4; ++ch4) {
+                        uint32_t w4[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int cc = 8 * ch4 + 2 * e;
+                            w4[e] = pack_bf16(cc <= lim ? gr[cc] * pinv : 0.f, cc + 1 <= lim ? gr[cc + 1] * pinv : 0.f);
                         }
-                        const int lim = i - 32 * half;
-#pragma unroll
-                        for (int cc = 0; cc < 32; ++cc)
-                            if (cc < lim) abase[(cc >> 4) * kBlk + (cc & 15) * kBS] = gr[cc] * wv[cc];
-                    } else {
-                        // P row i = l - 64, bf16: (q_i.k_j) / gamma_C for j <= i (the gates
-                        // are applied to U and y by the chain).
-                        const int i = l - 64;
-                        const float pinv = s_misc[1];
-                        const int lim = i - 32 * half;
-                        uint8_t *prow = sm + OFF_P + s * kPBytes + i * 128;
-#pragma unroll
-                        for (int ch4 = 0; ch4 < 4; ++ch4) {
-                            uint32_t w4[4];
-#pragma unroll
-                            for (int e = 0; e < 4; ++e) {
-                                const int cc = 8 * ch4 + 2 * e;
-                                w4[e] = pack_bf16(cc <= lim ? gr[cc] * pinv : 0.f, cc + 1 <= lim ? gr[cc + 1] * pinv : 0.f);
-                            }
-                            *reinterpret_cast<uint4 *>(prow + (((4 * half + ch4) ^ (i & 7)) << 4)) =
-                                make_uint4(w4[0], w4[1], w4[2], w4[3]);
-                        }
+                        *reinterpret_cast<uint4 *>(prow + (((4 * half + ch4) ^ (i & 7)) << 4)) =
+                            make_uint4(w4[0], w4[1], w4[2], w4[3]);
                     }
                 }
             } else {
-                exact_gram_rows(j, l, q, tb + TM_GW + (j & 1) * 64, At, sm + OFF_P + s * kPBytes,
-                                sm + OFF_KQ + s * kKQBytes, s_g, s_u, s_b);
+                exact_p_rows(l, q, gw, pbuf, sm + OFF_KQ + s * kKQBytes, s_g, s_u);
             }
             tc_fence_before();
-            if (l < 64) {
-                // Diagonal blocks of T = (I + A)^{-1} by forward substitution, one
-                // column per thread; this warp wrote both blocks' rows.  The block's
-                // strictly lower part (column m: rows m+1..15) is loaded in two
-                // batches ahead of the arithmetic.
-                __syncwarp();
-                const int blk = l >> 4, col = l & 15;
-                const float *Ab = At + kBlkIdx[blk][blk] * kBlk;
-                float t[16];
-#pragma unroll
-                for (int r = 0; r < 16; ++r) t[r] = (r == col) ? 1.f : 0.f;
-#pragma unroll
-                for (int mb = 0; mb < 2; ++mb) {
-                    constexpr int kSplit = 5;
-                    float av[65];
-                    const int m0 = mb ? kSplit : 0, m1 = mb ? 15 : kSplit;
-#pragma unroll
-                    for (int m = m0; m < m1; ++m)
-#pragma unroll
-                        for (int r = m + 1; r < 16; ++r)
-                            av[(m * 16 - (m * (m + 1)) / 2 + (r - m - 1)) - (m0 * 16 - (m0 * (m0 + 1)) / 2)] = Ab[m * kBS + r];
-#pragma unroll
-                    for (int m = m0; m < m1; ++m)
-#pragma unroll
-                        for (int r = m + 1; r < 16; ++r)
-                            t[r] = fmaf(-av[(m * 16 - (m * (m + 1)) / 2 + (r - m - 1)) - (m0 * 16 - (m0 * (m0 + 1)) / 2)], t[m], t[r]);
-                }
-                float *Tb = Tm + kBlkIdx[blk][blk] * kBlk + col;
-#pragma unroll
-                for (int r = 0; r < 16; ++r) Tb[r * kBS] = t[r];
-            }
             return true;
         };
 
-        // AP(j) of the next chunk runs between chunk j's merges and its W readout.
+        // Chunk j: merges (once the gate warps have written A and the diagonal T
+        // blocks), the next chunk's P rows, then chunk j's -W operand.
 #pragma unroll 1
         for (int j = -1; j < n; ++j) {
             if (j >= 0) {
@@ -849,7 +877,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float *sg = reinterpret_cast<const float *>(sm + OFF_GATES) + gbuf * kGateFloats;
                 const float *s_g = sg, *s_b = sg + 192, *s_bu = sg + 256, *s_misc = sg + 320;
                 const bool fast = s_misc[2] != 0.f;
-                named_bar(1, 128);   // A, diagonal T blocks and P of chunk j are written
+                {
+                    const bool ok = bwait(&bars[B_SOLVED], j & 1, abort_flag, p.status);
+                    if (!warp_ok(ok)) break;
+                }
                 // The factors F_IK (three tiles per warp) and bf16 T1, T2 of diagonal
                 // block lw; then the off-diagonal blocks T_IJ by block column: column 0
                 // split over warps 0 and 3 (one 8-column tile each), column 1 on warp 1,
@@ -863,8 +894,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     solve_column<2>(lw, 0, At, Tm, t1b, t2b, s_b, s_bu, lane);
                 fence_proxy_async();
                 mbar_arrive(&bars[B_TREADY]);
-                named_bar(1, 128);   // A and T of chunk j are no longer read
-                if (j + 1 < n && !ap(j + 1)) break;
+                if (j + 1 < n && !p_readout(j + 1)) break;
 
                 // The W^T, U~^T MMAs of chunk j have read T1, T2 (rewritten by the next
                 // merges) and K (exact path: K~ = diag(lambda) K in place).  Waiting here
@@ -897,7 +927,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_before();
                 mbar_arrive(&bars[B_OPS]);
                 mbar_arrive(&bars[B_GEMPTY + gbuf]);
-            } else if (!ap(0)) {
+            } else if (!p_readout(0)) {
                 break;
             }
         }
