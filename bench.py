@@ -7,7 +7,9 @@ fp32 gates and state, S0 ~ N(0, 0.02^2)).  Inputs are resident in HBM and
 larger than L2 (1.6 GB per step), so no flush is needed between steps.
 The same run also times the decode workload (B=256 sequences, 32 value heads
 over 16 key heads, d=128, 128 single-token steps, fp32 state updated in place)
-and reports it under "decode".
+and reports it under "decode", and the layer steps around the recurrence
+(fused prologue: short convolution, SiLU, L2Norm, gates; fused epilogue:
+sigmoid gate times zero-centred RMSNorm) on the prefill shape under "layer".
 
 Printed: one JSON line (rank 0).  `value` is prefill tokens/s summed over all
 ranks; `e2e` is the same metric through the C ABI with host buffers (pinned
@@ -355,6 +357,12 @@ def run_ours(args, ws, rank, local):
     if not args.no_decode:
         dec = time_decode(args, peaks, seed, dev, ws, local)
 
+    # ------------------------------------------------------------- layer prologue / epilogue
+    layer = None
+    if not args.no_layer:
+        layer = time_layer(args, peaks, seed, dev, ws, local)
+        torch.cuda.empty_cache()
+
     # ------------------------------------------------------------- cpu baseline
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -372,7 +380,7 @@ def run_ours(args, ws, rank, local):
                    "algorithm": gdn.ALGO_NAMES[args.algorithm], "segments": args.segments,
                    "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"},
         "roofline": roofline, "clocks": clocks, "e2e": e2e, "cpu_baseline": cpu, "gpu_launches": gpu_launches,
-        "decode": dec, "check": check,
+        "decode": dec, "layer": layer, "check": check,
     }
     if rank == 0:
         print(json.dumps(line), flush=True)
@@ -435,6 +443,64 @@ def time_e2e(args, x, shape, w, dev, ws):
     value = w["B"] * w["T"] * ws * steps / (ms * 1e-3)
     return {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "steps": steps, "ms_per_step": ms / steps}
+
+
+def layer_bytes(B, T, Hqk, Hv, d, kconv=4) -> tuple[int, int]:
+    """Algorithmic HBM bytes of the layer prologue and epilogue: every input read once and
+    every output written once (bf16 features, fp32 gates; taps and states negligible)."""
+    rows_qk, rows_v = B * T * Hqk, B * T * Hv
+    pro = 2 * (2 * rows_qk + rows_v) * d * 2 + 4 * rows_v * 4
+    epi = 3 * rows_v * d * 2
+    return pro, epi
+
+
+def time_layer(args, peaks, seed, dev, ws, local):
+    """The layer prologue and epilogue on the prefill shape (B=1, T=65536, Hqk=16, Hv=32, d=128,
+    four convolution taps); each against measured HBM bandwidth."""
+    import torch
+
+    from linear_attention_recurrence_14_b300 import gdn
+    from linear_attention_recurrence_14_b300.inputs import make_layer_inputs
+
+    B, T, Hqk, Hv, d, K = 1, 65536, 16, 32, 128, 4
+    x = make_layer_inputs(B, T, Hqk, Hv, d, K, seed=seed, device=dev, with_state=True)
+    out = gdn.layer_prologue(x.xq, x.xk, x.xv, x.wq, x.wk, x.wv, x.a_raw, x.b_raw, x.A, x.b_alpha,
+                             state_q=x.state_q, state_k=x.state_k, state_v=x.state_v, state_out=True)
+    o = torch.empty_like(x.y)
+    stream = torch.cuda.current_stream()
+
+    def pro():
+        gdn.layer_prologue(x.xq, x.xk, x.xv, x.wq, x.wk, x.wv, x.a_raw, x.b_raw, x.A, x.b_alpha,
+                           state_q=x.state_q, state_k=x.state_k, state_v=x.state_v, state_out=True, out=out)
+
+    def epi():
+        gdn.layer_epilogue(x.y, x.z, x.norm_w, 1e-6, o=o)
+
+    res = {}
+    pb, eb = layer_bytes(B, T, Hqk, Hv, d, K)
+    with ClockSampler(local) as clk:
+        for name, fn, nbytes in (("prologue", pro, pb), ("epilogue", epi, eb)):
+            for _ in range(max(3, args.warmup)):
+                fn()
+            torch.cuda.synchronize()
+            evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(20)]
+            barrier(ws)
+            for a, b in evs:
+                a.record(stream)
+                fn()
+                b.record(stream)
+            torch.cuda.synchronize()
+            ms = max_over_ranks(statistics.median(a.elapsed_time(b) for a, b in evs), ws, dev)
+            gbs = nbytes / (ms * 1e-3) / 1e9
+            res[name] = {"ms": ms, "tokens_per_s": B * T * ws / (ms * 1e-3),
+                         "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                                      "frac": gbs / peaks["hbm_gbs"], "traffic": None, "bytes_per_launch": nbytes,
+                                      "peak_source": peaks["source"]},
+                         "gpu_launches": 1}
+    res["config"] = "B=1, T=65536, Hqk=16, Hv=32, d=128, 4 taps, bf16 features, fp32 gates; median of 20 launches"
+    res["l2"] = "inputs larger than L2 (2.2 GB prologue, 1.6 GB epilogue), no flush"
+    res["clocks"] = clk.summary()
+    return res
 
 
 def time_decode(args, peaks, seed, dev, ws, local):
@@ -507,6 +573,7 @@ def main(argv=None):
     ap.add_argument("--decode-traffic", type=float, default=None, help="ncu dram bytes per decode launch")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-layer", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-check", dest="check", action="store_false")
     args = ap.parse_args(argv)

@@ -28,7 +28,7 @@ def sources() -> list[str]:
 
 def _inputs() -> list[str]:
     return sources() + sorted(glob.glob(os.path.join(CSRC, "*.h")) + glob.glob(os.path.join(CSRC, "*.cuh"))) + [
-        os.path.join(INCLUDE, "gdn.h"), os.path.abspath(__file__)]
+        *sorted(glob.glob(os.path.join(INCLUDE, "*.h"))), os.path.abspath(__file__)]
 
 
 def is_stale() -> bool:

@@ -1,0 +1,354 @@
+// GDN layer steps on either side of the recurrence (gdn_layer.h): the fused
+// prologue (short causal depthwise convolution, SiLU, L2Norm of q and k, the
+// decay and write gates) and the fused epilogue (sigmoid output gate times a
+// zero-centred RMSNorm), following the Qwen3.8-Next reading notes, section 2.1
+// "Gated DeltaNet" ("Feature parameterization", "Gating dynamics").
+//
+// Both are single HBM passes, one warp per row of d channels (a (token, head)
+// row is 128 or 256 contiguous bytes of bf16, so a warp's loads and stores are
+// fully coalesced), fp32 arithmetic, bf16 outputs rounded to nearest even.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "gdn_internal.h"
+#include "gdn_layer.h"
+
+namespace gdn {
+namespace {
+
+constexpr int kTile = 64;          // tokens per prologue warp
+constexpr int kMaxConv = 4;
+constexpr float kL2Eps = 1e-6f;
+
+__device__ __forceinline__ float warp_allsum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+__device__ __forceinline__ float sigmoidf_(float u) { return 1.f / (1.f + __expf(-u)); }
+
+// log(1 + e^u), stable for either sign of u.
+__device__ __forceinline__ float softplusf_(float u) { return fmaxf(u, 0.f) + log1pf(__expf(-fabsf(u))); }
+
+// CPL consecutive bf16 channels <-> floats (CPL = 2: one 32-bit word; 4: two).
+template <int CPL>
+__device__ __forceinline__ void load_bf16(const __nv_bfloat16 *p, float (&f)[CPL]) {
+    if constexpr (CPL == 4) {
+        const uint2 r = *reinterpret_cast<const uint2 *>(p);
+        const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&r.x));
+        const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&r.y));
+        f[0] = a.x; f[1] = a.y; f[2] = b.x; f[3] = b.y;
+    } else {
+        const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(p));
+        f[0] = a.x; f[1] = a.y;
+    }
+}
+
+template <int CPL>
+__device__ __forceinline__ void store_bf16(__nv_bfloat16 *p, const float (&f)[CPL]) {
+    if constexpr (CPL == 4) {
+        const __nv_bfloat162 a = __floats2bfloat162_rn(f[0], f[1]), b = __floats2bfloat162_rn(f[2], f[3]);
+        uint2 r;
+        r.x = *reinterpret_cast<const uint32_t *>(&a);
+        r.y = *reinterpret_cast<const uint32_t *>(&b);
+        *reinterpret_cast<uint2 *>(p) = r;
+    } else {
+        *reinterpret_cast<__nv_bfloat162 *>(p) = __floats2bfloat162_rn(f[0], f[1]);
+    }
+}
+
+struct ProloguePlan {
+    int64_t B, T;
+    int Hqk, Hv, d, kconv, ntiles;
+    gdn_prologue_io io;
+};
+
+// One warp: one (batch, head) row of one of q, k, v over a tile of kTile
+// tokens.  The lane's CPL channels keep the last kconv-1 inputs in registers,
+// so each input is read once (plus kconv-1 tokens of overlap per tile).
+template <int CPL>
+__global__ void __launch_bounds__(128) prologue_kernel(ProloguePlan p) {
+    const int lane = threadIdx.x & 31;
+    const int64_t job = static_cast<int64_t>(blockIdx.x) * 4 + (threadIdx.x >> 5);
+    const int nrows = 2 * p.Hqk + p.Hv;
+    if (job >= p.B * nrows * p.ntiles) return;
+    const int tile = static_cast<int>(job % p.ntiles);
+    const int row = static_cast<int>((job / p.ntiles) % nrows);
+    const int64_t b = job / (static_cast<int64_t>(p.ntiles) * nrows);
+    const int which = row < p.Hqk ? 0 : (row < 2 * p.Hqk ? 1 : 2);   // q, k, v
+    const int h = which == 0 ? row : (which == 1 ? row - p.Hqk : row - 2 * p.Hqk);
+    const int H = which == 2 ? p.Hv : p.Hqk;
+    const int d = p.d, K = p.kconv;
+    const int64_t C = static_cast<int64_t>(H) * d;
+    const __nv_bfloat16 *x = static_cast<const __nv_bfloat16 *>(which == 0 ? p.io.xq : which == 1 ? p.io.xk : p.io.xv);
+    const float *w = which == 0 ? p.io.wq : which == 1 ? p.io.wk : p.io.wv;
+    const __nv_bfloat16 *sin = static_cast<const __nv_bfloat16 *>(
+        which == 0 ? p.io.state_q_in : which == 1 ? p.io.state_k_in : p.io.state_v_in);
+    __nv_bfloat16 *sout = static_cast<__nv_bfloat16 *>(
+        which == 0 ? p.io.state_q_out : which == 1 ? p.io.state_k_out : p.io.state_v_out);
+    __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(which == 0 ? p.io.q : which == 1 ? p.io.k : p.io.v);
+
+    const int64_t ch = static_cast<int64_t>(h) * d + lane * CPL;   // first channel of this lane
+    // back[e][j]: the tap applied to the input j tokens back (0 = current; 0 beyond K)
+    float back[CPL][kMaxConv];
+#pragma unroll
+    for (int e = 0; e < CPL; ++e)
+#pragma unroll
+        for (int j = 0; j < kMaxConv; ++j) back[e][j] = (j < K && p.T > 0) ? w[(ch + e) * K + (K - 1 - j)] : 0.f;
+
+    // win[e][i]: input i+1 tokens before the current one (i < K-1)
+    float win[CPL][kMaxConv - 1];
+    const int64_t t0 = static_cast<int64_t>(tile) * kTile;
+#pragma unroll
+    for (int i = 0; i < kMaxConv - 1; ++i) {
+        float f[CPL];
+#pragma unroll
+        for (int e = 0; e < CPL; ++e) f[e] = 0.f;
+        const int64_t t = t0 - 1 - i;
+        if (i < K - 1) {
+            if (t >= 0)
+                load_bf16<CPL>(x + ((b * p.T + t) * C + ch), f);
+            else if (sin)
+                load_bf16<CPL>(sin + ((b * (K - 1) + (K - 1 + t)) * C + ch), f);
+        }
+#pragma unroll
+        for (int e = 0; e < CPL; ++e) win[e][i] = f[e];
+    }
+
+    const int64_t t1 = t0 + kTile < p.T ? t0 + kTile : p.T;
+    const bool normalise = which < 2;
+#pragma unroll 1
+    for (int64_t t = t0; t < t1; ++t) {
+        float xc[CPL];
+        load_bf16<CPL>(x + ((b * p.T + t) * C + ch), xc);
+        float u[CPL];
+        float ss = 0.f;
+#pragma unroll
+        for (int e = 0; e < CPL; ++e) {
+            float acc = back[e][0] * xc[e];
+#pragma unroll
+            for (int i = 0; i < kMaxConv - 1; ++i) acc = fmaf(back[e][i + 1], win[e][i], acc);
+            u[e] = acc * sigmoidf_(acc);
+            ss = fmaf(u[e], u[e], ss);
+#pragma unroll
+            for (int i = kMaxConv - 2; i > 0; --i) win[e][i] = win[e][i - 1];
+            win[e][0] = xc[e];
+        }
+        if (normalise) {
+            const float inv = rsqrtf(warp_allsum(ss) + kL2Eps);
+#pragma unroll
+            for (int e = 0; e < CPL; ++e) u[e] *= inv;
+        }
+        store_bf16<CPL>(out + ((b * p.T + t) * C + ch), u);
+    }
+    if (sout && t1 >= p.T) {
+        // the last K-1 inputs of the sequence (state entries 0 .. K-2, oldest first)
+#pragma unroll
+        for (int i = 0; i < kMaxConv - 1; ++i) {
+            if (i < K - 1) {
+                float f[CPL];
+#pragma unroll
+                for (int e = 0; e < CPL; ++e) f[e] = win[e][i];
+                store_bf16<CPL>(sout + ((b * (K - 1) + (K - 2 - i)) * C + ch), f);
+            }
+        }
+    }
+    if (which == 2 && t1 > t0) {
+        // decay and write gates of this value head over the tile
+        const float eA = __expf(p.io.A[h]), ba = p.io.b_alpha[h];
+        for (int64_t t = t0 + lane; t < t1; t += 32) {
+            const int64_t gi = (b * p.T + t) * p.Hv + h;
+            p.io.alpha[gi] = __expf(-eA * softplusf_(p.io.a_raw[gi] + ba));
+            p.io.beta[gi] = sigmoidf_(p.io.b_raw[gi]);
+        }
+    }
+}
+
+struct EpiloguePlan {
+    int64_t rows;          // B * T * Hv
+    int d;
+    float eps;
+    const __nv_bfloat16 *y, *z;
+    const float *w;
+    __nv_bfloat16 *o;
+};
+
+// One warp per (token, value head) row, grid-stride, two rows in flight.
+template <int CPL>
+__global__ void __launch_bounds__(256) epilogue_kernel(EpiloguePlan p) {
+    const int lane = threadIdx.x & 31;
+    const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+    const int64_t w0 = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    float g[CPL];
+#pragma unroll
+    for (int e = 0; e < CPL; ++e) g[e] = 1.f + p.w[lane * CPL + e];
+    const float inv_d = 1.f / static_cast<float>(p.d);
+#pragma unroll 1
+    for (int64_t r = w0; r < p.rows; r += 2 * warps) {
+        const int64_t r2 = r + warps;
+        const bool two = r2 < p.rows;
+        float y0[CPL], z0[CPL], y1[CPL], z1[CPL];
+        load_bf16<CPL>(p.y + r * p.d + lane * CPL, y0);
+        load_bf16<CPL>(p.z + r * p.d + lane * CPL, z0);
+        if (two) {
+            load_bf16<CPL>(p.y + r2 * p.d + lane * CPL, y1);
+            load_bf16<CPL>(p.z + r2 * p.d + lane * CPL, z1);
+        }
+        float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+        for (int e = 0; e < CPL; ++e) {
+            s0 = fmaf(y0[e], y0[e], s0);
+            s1 = two ? fmaf(y1[e], y1[e], s1) : 0.f;
+        }
+        s0 = warp_allsum(s0);
+        s1 = warp_allsum(s1);
+        const float i0 = rsqrtf(s0 * inv_d + p.eps), i1 = rsqrtf(s1 * inv_d + p.eps);
+        float o0[CPL], o1[CPL];
+#pragma unroll
+        for (int e = 0; e < CPL; ++e) {
+            o0[e] = sigmoidf_(z0[e]) * y0[e] * i0 * g[e];
+            o1[e] = two ? sigmoidf_(z1[e]) * y1[e] * i1 * g[e] : 0.f;
+        }
+        store_bf16<CPL>(p.o + r * p.d + lane * CPL, o0);
+        if (two) store_bf16<CPL>(p.o + r2 * p.d + lane * CPL, o1);
+    }
+}
+
+bool aligned(const void *q, uintptr_t a) { return (reinterpret_cast<uintptr_t>(q) & (a - 1)) == 0; }
+
+struct Span {
+    const void *p;
+    int64_t n;
+};
+
+bool overlap(Span a, Span b) {
+    if (!a.p || !b.p || a.n <= 0 || b.n <= 0) return false;
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(a.p), b0 = reinterpret_cast<uintptr_t>(b.p);
+    return a0 < b0 + static_cast<uintptr_t>(b.n) && b0 < a0 + static_cast<uintptr_t>(a.n);
+}
+
+gdn_status check_layer_shape(const gdn_layer_shape *s) {
+    if (!s || s->B < 0 || s->T < 0 || s->Hqk <= 0 || s->Hv <= 0 || s->Hv % s->Hqk != 0) return GDN_ERR_INVALID_ARG;
+    if (s->kconv < 1 || s->kconv > kMaxConv) return GDN_ERR_INVALID_ARG;
+    if (s->d != 64 && s->d != 128) return GDN_ERR_UNSUPPORTED;
+    // element counts must stay far from int64 overflow
+    if (s->B > (int64_t{1} << 24) || s->T > (int64_t{1} << 34) || s->Hv > 4096) return GDN_ERR_INVALID_ARG;
+    if (s->B * s->T > (int64_t{1} << 36)) return GDN_ERR_INVALID_ARG;
+    return GDN_OK;
+}
+
+gdn_status device_ok() {
+    int dev = 0, major = 0, minor = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) {
+        cudaGetLastError();
+        return GDN_ERR_CUDA;
+    }
+    return (major == 10 && minor == 3) ? GDN_OK : GDN_ERR_UNSUPPORTED;
+}
+
+}  // namespace
+}  // namespace gdn
+
+using namespace gdn;
+
+extern "C" gdn_status gdn_layer_prologue(const gdn_layer_shape *shape, const gdn_prologue_io *io, void *stream) {
+    const gdn_status st = check_layer_shape(shape);
+    if (st != GDN_OK) return st;
+    if (!io) return GDN_ERR_INVALID_ARG;
+    const gdn_layer_shape s = *shape;
+    const gdn_prologue_io &a = *io;
+    // With no tokens only the convolution states are touched; the token
+    // tensors may then be empty (NULL).
+    if (s.B > 0 && s.T > 0 &&
+        (!a.xq || !a.xk || !a.xv || !a.wq || !a.wk || !a.wv || !a.a_raw || !a.b_raw || !a.A || !a.b_alpha || !a.q ||
+         !a.k || !a.v || !a.alpha || !a.beta))
+        return GDN_ERR_INVALID_ARG;
+    const void *bf[] = {a.xq, a.xk, a.xv, a.q, a.k, a.v, a.state_q_in, a.state_k_in, a.state_v_in,
+                        a.state_q_out, a.state_k_out, a.state_v_out};
+    for (const void *ptr : bf)
+        if (!aligned(ptr, 16)) return GDN_ERR_ALIGNMENT;
+    const void *fp[] = {a.wq, a.wk, a.wv, a.a_raw, a.b_raw, a.A, a.b_alpha, a.alpha, a.beta};
+    for (const void *ptr : fp)
+        if (!aligned(ptr, 4)) return GDN_ERR_ALIGNMENT;
+
+    const int64_t nq = s.B * s.T * s.Hqk * s.d * 2, nv = s.B * s.T * s.Hv * s.d * 2, ng = s.B * s.T * s.Hv * 4;
+    const int64_t sq = s.B * (s.kconv - 1) * s.Hqk * s.d * 2, sv = s.B * (s.kconv - 1) * s.Hv * s.d * 2;
+    const Span ins[] = {{a.xq, nq}, {a.xk, nq}, {a.xv, nv}, {a.wq, int64_t{s.Hqk} * s.d * s.kconv * 4},
+                        {a.wk, int64_t{s.Hqk} * s.d * s.kconv * 4}, {a.wv, int64_t{s.Hv} * s.d * s.kconv * 4},
+                        {a.state_q_in, sq}, {a.state_k_in, sq}, {a.state_v_in, sv}, {a.a_raw, ng}, {a.b_raw, ng},
+                        {a.A, s.Hv * 4}, {a.b_alpha, s.Hv * 4}};
+    const Span outs[] = {{a.q, nq}, {a.k, nq}, {a.v, nv}, {a.alpha, ng}, {a.beta, ng},
+                         {a.state_q_out, sq}, {a.state_k_out, sq}, {a.state_v_out, sv}};
+    for (const Span &o : outs) {
+        for (const Span &i : ins)
+            if (overlap(o, i)) return GDN_ERR_ALIASING;
+        for (const Span &o2 : outs)
+            if (&o2 != &o && overlap(o, o2)) return GDN_ERR_ALIASING;
+    }
+    const gdn_status dev = device_ok();
+    if (dev != GDN_OK) return dev;
+    if (s.B == 0) return GDN_OK;
+
+    ProloguePlan p;
+    p.B = s.B;
+    p.T = s.T;
+    p.Hqk = s.Hqk;
+    p.Hv = s.Hv;
+    p.d = s.d;
+    p.kconv = s.kconv;
+    p.ntiles = static_cast<int>(s.T == 0 ? 1 : (s.T + kTile - 1) / kTile);
+    p.io = a;
+    const int64_t warps = s.B * (2 * s.Hqk + s.Hv) * p.ntiles;
+    if ((warps + 3) / 4 > 0x7fffffff) return GDN_ERR_INVALID_ARG;
+    const dim3 grid(static_cast<unsigned>((warps + 3) / 4));
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    if (s.d == 128)
+        prologue_kernel<4><<<grid, 128, 0, cs>>>(p);
+    else
+        prologue_kernel<2><<<grid, 128, 0, cs>>>(p);
+    const cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
+extern "C" gdn_status gdn_layer_epilogue(const gdn_layer_shape *shape, const void *y, const void *z,
+                                         const float *norm_w, float eps, void *o, void *stream) {
+    const gdn_status st = check_layer_shape(shape);
+    if (st != GDN_OK) return st;
+    if (!(eps > 0.f)) return GDN_ERR_INVALID_ARG;
+    if (shape->B * shape->T == 0) return GDN_OK;
+    if (!y || !z || !norm_w || !o) return GDN_ERR_INVALID_ARG;
+    if (!aligned(y, 16) || !aligned(z, 16) || !aligned(o, 16) || !aligned(norm_w, 4)) return GDN_ERR_ALIGNMENT;
+    const gdn_layer_shape s = *shape;
+    const int64_t n = s.B * s.T * s.Hv * s.d * 2;
+    if (overlap({o, n}, {y, n}) || overlap({o, n}, {z, n}) || overlap({o, n}, {norm_w, s.d * 4}))
+        return GDN_ERR_ALIASING;
+    const gdn_status dev = device_ok();
+    if (dev != GDN_OK) return dev;
+    EpiloguePlan p;
+    p.rows = s.B * s.T * s.Hv;
+    if (p.rows == 0) return GDN_OK;
+    p.d = s.d;
+    p.eps = eps;
+    p.y = static_cast<const __nv_bfloat16 *>(y);
+    p.z = static_cast<const __nv_bfloat16 *>(z);
+    p.w = norm_w;
+    p.o = static_cast<__nv_bfloat16 *>(o);
+    int dev_id = 0, sms = 148;
+    cudaGetDevice(&dev_id);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev_id);
+    // 8 resident CTAs of 8 warps per SM, two rows per warp per iteration
+    const int64_t want = (p.rows + 15) / 16;
+    const unsigned grid = static_cast<unsigned>(want < int64_t{sms} * 8 ? want : int64_t{sms} * 8);
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    if (s.d == 128)
+        epilogue_kernel<4><<<grid, 256, 0, cs>>>(p);
+    else
+        epilogue_kernel<2><<<grid, 256, 0, cs>>>(p);
+    const cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}

@@ -24,10 +24,10 @@ GDN_F32, GDN_BF16 = 0, 1
 ALGO_AUTO, ALGO_CHUNKED, ALGO_SEQUENTIAL = 0, 1, 2
 ALGO_NAMES = {ALGO_AUTO: "auto", ALGO_CHUNKED: "chunked", ALGO_SEQUENTIAL: "sequential"}
 
-# Every symbol include/gdn.h declares.
+# Every symbol include/gdn.h and include/gdn_layer.h declare.
 EXPORTS = ("gdn_status_string", "gdn_prefill_workspace_bytes", "gdn_prefill", "gdn_prefill_ex",
            "gdn_decode_step", "gdn_read_device_status", "gdn_device_supported", "gdn_abi_version",
-           "gdn_prefill_noalloc")
+           "gdn_prefill_noalloc", "gdn_layer_prologue", "gdn_layer_epilogue")
 NOALLOC_SCRATCH_BYTES = 256 + 8 * 1024 * 1024
 
 
@@ -39,6 +39,18 @@ class GdnShape(ctypes.Structure):
 class GdnPrefillOptions(ctypes.Structure):
     _fields_ = [("segments", ctypes.c_int32), ("log_eps", ctypes.c_float), ("max_warmup_chunks", ctypes.c_int32),
                 ("algorithm", ctypes.c_int32), ("test_stall_chunk", ctypes.c_int32)]
+
+
+class GdnLayerShape(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int64), ("T", ctypes.c_int64), ("Hqk", ctypes.c_int32), ("Hv", ctypes.c_int32),
+                ("d", ctypes.c_int32), ("kconv", ctypes.c_int32)]
+
+
+class GdnPrologueIO(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in (
+        "xq", "xk", "xv", "wq", "wk", "wv", "state_q_in", "state_k_in", "state_v_in",
+        "state_q_out", "state_k_out", "state_v_out", "a_raw", "b_raw", "A", "b_alpha",
+        "q", "k", "v", "alpha", "beta")]
 
 
 class GdnError(RuntimeError):
@@ -76,6 +88,10 @@ def lib() -> ctypes.CDLL:
             L.gdn_decode_step.argtypes = [sp, vp, vp, vp, fp, fp, fp, vp, vp]
             L.gdn_read_device_status.restype = ctypes.c_int
             L.gdn_read_device_status.argtypes = [vp, vp]
+            L.gdn_layer_prologue.restype = ctypes.c_int
+            L.gdn_layer_prologue.argtypes = [ctypes.POINTER(GdnLayerShape), ctypes.POINTER(GdnPrologueIO), vp]
+            L.gdn_layer_epilogue.restype = ctypes.c_int
+            L.gdn_layer_epilogue.argtypes = [ctypes.POINTER(GdnLayerShape), vp, vp, fp, ctypes.c_float, vp, vp]
             L.gdn_device_supported.restype = ctypes.c_int
             L.gdn_abi_version.restype = ctypes.c_int
             _lib = L
@@ -189,6 +205,53 @@ def decode_step(q, k, v, alpha, beta, S, *, y=None, stream=None):
                                _ptr(y), _stream(stream))
     _check(rc, "gdn_decode_step")
     return y
+
+
+def layer_prologue(xq, xk, xv, wq, wk, wv, a_raw, b_raw, A, b_alpha, *, state_q=None, state_k=None,
+                   state_v=None, state_out=False, out=None, stream=None):
+    """Run gdn_layer_prologue: q, k, v (bf16) and alpha, beta (fp32) from the projected features.
+
+    xq, xk [B,T,Hqk,d] and xv [B,T,Hv,d] bf16; wq, wk [Hqk*d, K], wv [Hv*d, K] fp32 taps;
+    a_raw, b_raw [B,T,Hv] fp32; A, b_alpha [Hv] fp32; optional incoming convolution states
+    [B, K-1, H*d] bf16.  Returns a dict with q, k, v, alpha, beta and, with state_out=True,
+    the outgoing states state_q, state_k, state_v."""
+    _require(dict(xq=xq, xk=xk, xv=xv, wq=wq, wk=wk, wv=wv, a_raw=a_raw, b_raw=b_raw, A=A, b_alpha=b_alpha,
+                  state_q=state_q, state_k=state_k, state_v=state_v))
+    B, T, Hqk, d = xq.shape
+    Hv = xv.shape[2]
+    K = wq.shape[1]
+    shape = GdnLayerShape(B, T, Hqk, Hv, d, K)
+    dev = xq.device
+    o = dict(out or {})
+    o.setdefault("q", torch.empty_like(xq))
+    o.setdefault("k", torch.empty_like(xk))
+    o.setdefault("v", torch.empty_like(xv))
+    o.setdefault("alpha", torch.empty((B, T, Hv), dtype=torch.float32, device=dev))
+    o.setdefault("beta", torch.empty((B, T, Hv), dtype=torch.float32, device=dev))
+    if state_out:
+        o.setdefault("state_q", torch.empty((B, K - 1, Hqk * d), dtype=torch.bfloat16, device=dev))
+        o.setdefault("state_k", torch.empty((B, K - 1, Hqk * d), dtype=torch.bfloat16, device=dev))
+        o.setdefault("state_v", torch.empty((B, K - 1, Hv * d), dtype=torch.bfloat16, device=dev))
+    _require(o)
+    io = GdnPrologueIO(*[None if t is None else t.data_ptr() for t in (
+        xq, xk, xv, wq, wk, wv, state_q, state_k, state_v, o.get("state_q"), o.get("state_k"), o.get("state_v"),
+        a_raw, b_raw, A, b_alpha, o["q"], o["k"], o["v"], o["alpha"], o["beta"])])
+    rc = lib().gdn_layer_prologue(ctypes.byref(shape), ctypes.byref(io), _stream(stream))
+    _check(rc, "gdn_layer_prologue")
+    return o
+
+
+def layer_epilogue(y, z, norm_w, eps=1e-6, *, o=None, Hqk=None, stream=None):
+    """Run gdn_layer_epilogue: o = sigmoid(z) * RMSNorm(y) (zero-centred weight), bf16 [B,T,Hv,d]."""
+    _require(dict(y=y, z=z, norm_w=norm_w, o=o))
+    B, T, Hv, d = y.shape
+    shape = GdnLayerShape(B, T, Hqk or Hv, Hv, d, 1)
+    if o is None:
+        o = torch.empty_like(y)
+    rc = lib().gdn_layer_epilogue(ctypes.byref(shape), _ptr(y), _ptr(z), _ptr(norm_w), float(eps), _ptr(o),
+                                  _stream(stream))
+    _check(rc, "gdn_layer_epilogue")
+    return o
 
 
 def prefill_launches(shape: GdnShape, algorithm=ALGO_AUTO, segments=0) -> int:

@@ -119,3 +119,57 @@ def workload_inputs(name: str, seed: int = 0, device="cpu", **overrides):
                                   w["decay_scale"], w["s0_std"], seed, device)
     return make_prefill_inputs(w["B"], w["T"], w["Hqk"], w["Hv"], w["d"], w["dtype"],
                                w["decay_scale"], w["s0_std"], seed, device)
+
+
+@dataclass
+class LayerInputs:
+    xq: torch.Tensor       # [B, T, Hqk, d] bf16: W_q x
+    xk: torch.Tensor       # [B, T, Hqk, d] bf16: W_k x
+    xv: torch.Tensor       # [B, T, Hv, d]  bf16: W_v x
+    wq: torch.Tensor       # [Hqk*d, K] fp32 convolution taps
+    wk: torch.Tensor
+    wv: torch.Tensor       # [Hv*d, K]
+    a_raw: torch.Tensor    # [B, T, Hv] fp32: W_alpha x
+    b_raw: torch.Tensor    # [B, T, Hv] fp32: W_beta x
+    A: torch.Tensor        # [Hv] fp32
+    b_alpha: torch.Tensor  # [Hv] fp32
+    state_q: torch.Tensor | None   # [B, K-1, Hqk*d] bf16 incoming convolution states
+    state_k: torch.Tensor | None
+    state_v: torch.Tensor | None
+    y: torch.Tensor        # [B, T, Hv, d] bf16: recurrence output (epilogue input)
+    z: torch.Tensor        # [B, T, Hv, d] bf16: W_z x
+    norm_w: torch.Tensor   # [d] fp32 zero-centred RMSNorm weight
+
+
+def make_layer_inputs(B, T, Hqk, Hv, d, kconv=4, decay_scale=0.05, seed=0, device="cpu",
+                      with_state=False, vary_heads=False) -> LayerInputs:
+    """Inputs of the layer steps around the recurrence.
+
+    Projections (W_q x, ..., W_z x) and y ~ N(0, 1) per element, stored bf16;
+    convolution taps ~ N(0, 1/kconv); W_alpha x, W_beta x ~ N(0, 1) fp32;
+    norm weight ~ N(0, 0.1^2).  With A = ln(decay_scale) and b_alpha = 0 the
+    decay gate exp(-exp(A) softplus(a)) has exactly the distribution of the
+    core workloads' alpha (exp(-softplus(a) * decay_scale)); vary_heads adds
+    N(0, 0.5^2) per head to both, so per-head indexing is exercised.  Incoming
+    convolution states (with_state) ~ N(0, 1) bf16."""
+    bf = torch.bfloat16
+    xq = _randn((B, T, Hqk, d), seed, "xq", device).to(bf)
+    xk = _randn((B, T, Hqk, d), seed, "xk", device).to(bf)
+    xv = _randn((B, T, Hv, d), seed, "xv", device).to(bf)
+    sc = 1.0 / kconv ** 0.5
+    wq = _randn((Hqk * d, kconv), seed, "wq", device) * sc
+    wk = _randn((Hqk * d, kconv), seed, "wk", device) * sc
+    wv = _randn((Hv * d, kconv), seed, "wv", device) * sc
+    a_raw = _randn((B, T, Hv), seed, "a_raw", device)
+    b_raw = _randn((B, T, Hv), seed, "b_raw", device)
+    A = torch.full((Hv,), float(torch.log(torch.tensor(decay_scale))), device=device)
+    b_alpha = torch.zeros(Hv, device=device)
+    if vary_heads:
+        A = A + 0.5 * _randn((Hv,), seed, "A", device)
+        b_alpha = 0.5 * _randn((Hv,), seed, "b_alpha", device)
+    st = (lambda H, n: _randn((B, kconv - 1, H * d), seed, n, device).to(bf)) if with_state else (lambda H, n: None)
+    y = _randn((B, T, Hv, d), seed, "y", device).to(bf)
+    z = _randn((B, T, Hv, d), seed, "z", device).to(bf)
+    norm_w = 0.1 * _randn((d,), seed, "norm_w", device)
+    return LayerInputs(xq, xk, xv, wq.contiguous(), wk.contiguous(), wv.contiguous(), a_raw, b_raw, A.contiguous(),
+                       b_alpha.contiguous(), st(Hqk, "state_q"), st(Hqk, "state_k"), st(Hv, "state_v"), y, z, norm_w)

@@ -1,5 +1,5 @@
 """C-ABI checks that need no GPU: the library loads, exports every symbol
-include/gdn.h declares, and rejects bad arguments on the host before any CUDA
+include/*.h declares, and rejects bad arguments on the host before any CUDA
 call (the pointers below are never dereferenced)."""
 import ctypes
 import os
@@ -20,7 +20,8 @@ def L():
 
 
 def declared_functions():
-    text = open(os.path.join(ROOT, "include", "gdn.h")).read()
+    text = "".join(open(os.path.join(ROOT, "include", h)).read()
+                   for h in sorted(os.listdir(os.path.join(ROOT, "include"))) if h.endswith(".h"))
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
     return sorted(set(re.findall(r"\b(gdn_[a-z_]+)\s*\(", text)))
 
@@ -107,3 +108,51 @@ def test_decode_rejects_bad_arguments(L):
     bad = list(args)
     bad[5] = vp(BASE + 5 * MB + 4)
     assert L.gdn_decode_step(ctypes.byref(s), *bad, None) == E["GDN_ERR_ALIGNMENT"]
+
+
+def layer_shape(B=1, T=64, Hqk=2, Hv=4, d=128, K=4):
+    return gdn.GdnLayerShape(B, T, Hqk, Hv, d, K)
+
+
+def call_prologue(L, s, **over):
+    names = [f[0] for f in gdn.GdnPrologueIO._fields_]
+    vals = {n: BASE + i * 64 * MB for i, n in enumerate(names)}
+    for n in ("state_q_in", "state_k_in", "state_v_in", "state_q_out", "state_k_out", "state_v_out"):
+        vals[n] = None
+    vals.update(over)
+    io = gdn.GdnPrologueIO(*[vals[n] for n in names])
+    return L.gdn_layer_prologue(ctypes.byref(s) if s is not None else None, ctypes.byref(io), None)
+
+
+def test_layer_prologue_rejects_bad_arguments(L):
+    E = {v: k for k, v in gdn.STATUS_NAMES.items()}
+    assert call_prologue(L, None) == E["GDN_ERR_INVALID_ARG"]
+    assert L.gdn_layer_prologue(ctypes.byref(layer_shape()), None, None) == E["GDN_ERR_INVALID_ARG"]
+    assert call_prologue(L, layer_shape(Hqk=3, Hv=4)) == E["GDN_ERR_INVALID_ARG"]
+    assert call_prologue(L, layer_shape(K=0)) == E["GDN_ERR_INVALID_ARG"]
+    assert call_prologue(L, layer_shape(K=5)) == E["GDN_ERR_INVALID_ARG"]
+    assert call_prologue(L, layer_shape(T=-1)) == E["GDN_ERR_INVALID_ARG"]
+    assert call_prologue(L, layer_shape(d=96)) == E["GDN_ERR_UNSUPPORTED"]
+    assert call_prologue(L, layer_shape(), xq=None) == E["GDN_ERR_INVALID_ARG"]
+    assert call_prologue(L, layer_shape(), alpha=None) == E["GDN_ERR_INVALID_ARG"]
+    assert call_prologue(L, layer_shape(), xv=BASE + 2 * 64 * MB + 8) == E["GDN_ERR_ALIGNMENT"]
+    assert call_prologue(L, layer_shape(), A=BASE + 14 * 64 * MB + 2) == E["GDN_ERR_ALIGNMENT"]
+    assert call_prologue(L, layer_shape(), state_v_out=BASE + 8) == E["GDN_ERR_ALIGNMENT"]
+    # an output on top of an input, and two outputs on top of each other
+    assert call_prologue(L, layer_shape(), q=BASE) == E["GDN_ERR_ALIASING"]
+    assert call_prologue(L, layer_shape(), beta=BASE + 19 * 64 * MB) == E["GDN_ERR_ALIASING"]
+    assert call_prologue(L, layer_shape(), state_q_in=BASE + 30 * 64 * MB,
+                         state_q_out=BASE + 30 * 64 * MB) == E["GDN_ERR_ALIASING"]
+
+
+def test_layer_epilogue_rejects_bad_arguments(L):
+    E = {v: k for k, v in gdn.STATUS_NAMES.items()}
+    vp = ctypes.c_void_p
+    s = ctypes.byref(layer_shape())
+    y, z, w, o = vp(BASE), vp(BASE + 64 * MB), vp(BASE + 128 * MB), vp(BASE + 192 * MB)
+    assert L.gdn_layer_epilogue(None, y, z, w, 1e-6, o, None) == E["GDN_ERR_INVALID_ARG"]
+    assert L.gdn_layer_epilogue(s, y, z, w, 0.0, o, None) == E["GDN_ERR_INVALID_ARG"]
+    assert L.gdn_layer_epilogue(s, None, z, w, 1e-6, o, None) == E["GDN_ERR_INVALID_ARG"]
+    assert L.gdn_layer_epilogue(s, vp(BASE + 8), z, w, 1e-6, o, None) == E["GDN_ERR_ALIGNMENT"]
+    assert L.gdn_layer_epilogue(s, y, z, w, 1e-6, y, None) == E["GDN_ERR_ALIASING"]
+    assert L.gdn_layer_epilogue(ctypes.byref(layer_shape(d=32)), y, z, w, 1e-6, o, None) == E["GDN_ERR_UNSUPPORTED"]
