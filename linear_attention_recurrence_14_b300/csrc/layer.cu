@@ -20,12 +20,17 @@ namespace {
 
 constexpr int kTile = 64;          // tokens per prologue warp
 constexpr int kMaxConv = 4;
+constexpr int kPrefetch = 16;      // tokens a prologue warp prefetches ahead
 constexpr float kL2Eps = 1e-6f;
 
 __device__ __forceinline__ float warp_allsum(float v) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
     return v;
+}
+
+__device__ __forceinline__ void prefetch_l2(const void *p) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
 }
 
 __device__ __forceinline__ float sigmoidf_(float u) { return 1.f / (1.f + __expf(-u)); }
@@ -36,13 +41,16 @@ __device__ __forceinline__ float softplusf_(float u) { return fmaxf(u, 0.f) + lo
 // CPL consecutive bf16 channels <-> floats (CPL = 2: one 32-bit word; 4: two).
 template <int CPL>
 __device__ __forceinline__ void load_bf16(const __nv_bfloat16 *p, float (&f)[CPL]) {
+    // read-only path (the inputs never alias the outputs), so loads may be
+    // issued ahead of earlier stores
     if constexpr (CPL == 4) {
-        const uint2 r = *reinterpret_cast<const uint2 *>(p);
+        const uint2 r = __ldg(reinterpret_cast<const uint2 *>(p));
         const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&r.x));
         const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&r.y));
         f[0] = a.x; f[1] = a.y; f[2] = b.x; f[3] = b.y;
     } else {
-        const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(p));
+        const unsigned int r = __ldg(reinterpret_cast<const unsigned int *>(p));
+        const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&r));
         f[0] = a.x; f[1] = a.y;
     }
 }
@@ -75,8 +83,10 @@ __global__ void __launch_bounds__(128) prologue_kernel(ProloguePlan p) {
     const int64_t job = static_cast<int64_t>(blockIdx.x) * 4 + (threadIdx.x >> 5);
     const int nrows = 2 * p.Hqk + p.Hv;
     if (job >= p.B * nrows * p.ntiles) return;
-    const int tile = static_cast<int>(job % p.ntiles);
-    const int row = static_cast<int>((job / p.ntiles) % nrows);
+    // job = (b * ntiles + tile) * nrows + row: consecutive warps take consecutive
+    // heads of one token tile, so the rows in flight are contiguous in memory
+    const int row = static_cast<int>(job % nrows);
+    const int tile = static_cast<int>((job / nrows) % p.ntiles);
     const int64_t b = job / (static_cast<int64_t>(p.ntiles) * nrows);
     const int which = row < p.Hqk ? 0 : (row < 2 * p.Hqk ? 1 : 2);   // q, k, v
     const int h = which == 0 ? row : (which == 1 ? row - p.Hqk : row - 2 * p.Hqk);
@@ -120,8 +130,14 @@ __global__ void __launch_bounds__(128) prologue_kernel(ProloguePlan p) {
 
     const int64_t t1 = t0 + kTile < p.T ? t0 + kTile : p.T;
     const bool normalise = which < 2;
+    // The loop below is latency-bound (one row in flight per warp), so rows are
+    // prefetched into L2 kPrefetch tokens ahead of their load.
+    const __nv_bfloat16 *xrow = x + (b * p.T) * C + ch;
+#pragma unroll 1
+    for (int64_t t = t0; t < t0 + kPrefetch && t < t1; ++t) prefetch_l2(xrow + t * C);
 #pragma unroll 1
     for (int64_t t = t0; t < t1; ++t) {
+        if (t + kPrefetch < t1) prefetch_l2(xrow + (t + kPrefetch) * C);
         float xc[CPL];
         load_bf16<CPL>(x + ((b * p.T + t) * C + ch), xc);
         float u[CPL];
@@ -176,44 +192,61 @@ struct EpiloguePlan {
     __nv_bfloat16 *o;
 };
 
-// One warp per (token, value head) row, grid-stride, two rows in flight.
-template <int CPL>
+// 16-byte accesses: a lane handles 8 channels, a row of d channels takes
+// d/8 lanes (16 for d = 128, 8 for d = 64), so a warp covers 32*8/d rows per
+// access; two such row sets are in flight per iteration; grid-stride.
+template <int LPR>   // lanes per row
 __global__ void __launch_bounds__(256) epilogue_kernel(EpiloguePlan p) {
+    constexpr int RPW = 32 / LPR;   // rows per warp access
     const int lane = threadIdx.x & 31;
+    const int sub = lane / LPR, cl = lane % LPR;
     const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
     const int64_t w0 = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
-    float g[CPL];
+    float g[8];
 #pragma unroll
-    for (int e = 0; e < CPL; ++e) g[e] = 1.f + p.w[lane * CPL + e];
+    for (int e = 0; e < 8; ++e) g[e] = 1.f + p.w[cl * 8 + e];
     const float inv_d = 1.f / static_cast<float>(p.d);
+    const int64_t nsets = (p.rows + RPW - 1) / RPW;
 #pragma unroll 1
-    for (int64_t r = w0; r < p.rows; r += 2 * warps) {
-        const int64_t r2 = r + warps;
-        const bool two = r2 < p.rows;
-        float y0[CPL], z0[CPL], y1[CPL], z1[CPL];
-        load_bf16<CPL>(p.y + r * p.d + lane * CPL, y0);
-        load_bf16<CPL>(p.z + r * p.d + lane * CPL, z0);
-        if (two) {
-            load_bf16<CPL>(p.y + r2 * p.d + lane * CPL, y1);
-            load_bf16<CPL>(p.z + r2 * p.d + lane * CPL, z1);
-        }
-        float s0 = 0.f, s1 = 0.f;
+    for (int64_t s0 = w0; s0 < nsets; s0 += 2 * warps) {
+        uint4 yr[2], zr[2];
+        int64_t r[2];
 #pragma unroll
-        for (int e = 0; e < CPL; ++e) {
-            s0 = fmaf(y0[e], y0[e], s0);
-            s1 = two ? fmaf(y1[e], y1[e], s1) : 0.f;
+        for (int j = 0; j < 2; ++j) {
+            r[j] = (s0 + j * warps) * RPW + sub;
+            if (r[j] < p.rows) {
+                yr[j] = *reinterpret_cast<const uint4 *>(p.y + r[j] * p.d + cl * 8);
+                zr[j] = *reinterpret_cast<const uint4 *>(p.z + r[j] * p.d + cl * 8);
+            } else {
+                yr[j] = zr[j] = make_uint4(0u, 0u, 0u, 0u);
+            }
         }
-        s0 = warp_allsum(s0);
-        s1 = warp_allsum(s1);
-        const float i0 = rsqrtf(s0 * inv_d + p.eps), i1 = rsqrtf(s1 * inv_d + p.eps);
-        float o0[CPL], o1[CPL];
 #pragma unroll
-        for (int e = 0; e < CPL; ++e) {
-            o0[e] = sigmoidf_(z0[e]) * y0[e] * i0 * g[e];
-            o1[e] = two ? sigmoidf_(z1[e]) * y1[e] * i1 * g[e] : 0.f;
+        for (int j = 0; j < 2; ++j) {
+            const __nv_bfloat162 *yh = reinterpret_cast<const __nv_bfloat162 *>(&yr[j]);
+            const __nv_bfloat162 *zh = reinterpret_cast<const __nv_bfloat162 *>(&zr[j]);
+            float y[8], z[8];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float2 a = __bfloat1622float2(yh[e]), c = __bfloat1622float2(zh[e]);
+                y[2 * e] = a.x; y[2 * e + 1] = a.y; z[2 * e] = c.x; z[2 * e + 1] = c.y;
+            }
+            float ss = 0.f;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) ss = fmaf(y[e], y[e], ss);
+#pragma unroll
+            for (int o = LPR / 2; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+            const float inv = rsqrtf(ss * inv_d + p.eps);
+            uint4 orow;
+            uint32_t *ow = reinterpret_cast<uint32_t *>(&orow);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const __nv_bfloat162 v = __floats2bfloat162_rn(sigmoidf_(z[2 * e]) * y[2 * e] * inv * g[2 * e],
+                                                               sigmoidf_(z[2 * e + 1]) * y[2 * e + 1] * inv * g[2 * e + 1]);
+                ow[e] = *reinterpret_cast<const uint32_t *>(&v);
+            }
+            if (r[j] < p.rows) *reinterpret_cast<uint4 *>(p.o + r[j] * p.d + cl * 8) = orow;
         }
-        store_bf16<CPL>(p.o + r * p.d + lane * CPL, o0);
-        if (two) store_bf16<CPL>(p.o + r2 * p.d + lane * CPL, o1);
     }
 }
 
@@ -341,14 +374,15 @@ extern "C" gdn_status gdn_layer_epilogue(const gdn_layer_shape *shape, const voi
     int dev_id = 0, sms = 148;
     cudaGetDevice(&dev_id);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev_id);
-    // 8 resident CTAs of 8 warps per SM, two rows per warp per iteration
-    const int64_t want = (p.rows + 15) / 16;
+    // 8 resident CTAs of 8 warps per SM; each warp covers 2 * 256 / d rows per iteration
+    const int64_t rows_per_cta = 8 * 2 * (256 / s.d);
+    const int64_t want = (p.rows + rows_per_cta - 1) / rows_per_cta;
     const unsigned grid = static_cast<unsigned>(want < int64_t{sms} * 8 ? want : int64_t{sms} * 8);
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
     if (s.d == 128)
-        epilogue_kernel<4><<<grid, 256, 0, cs>>>(p);
+        epilogue_kernel<16><<<grid, 256, 0, cs>>>(p);
     else
-        epilogue_kernel<2><<<grid, 256, 0, cs>>>(p);
+        epilogue_kernel<8><<<grid, 256, 0, cs>>>(p);
     const cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
