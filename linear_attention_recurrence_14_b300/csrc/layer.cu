@@ -20,17 +20,12 @@ namespace {
 
 constexpr int kTile = 64;          // tokens per prologue warp
 constexpr int kMaxConv = 4;
-constexpr int kPrefetch = 16;      // tokens a prologue warp prefetches ahead
 constexpr float kL2Eps = 1e-6f;
 
 __device__ __forceinline__ float warp_allsum(float v) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
     return v;
-}
-
-__device__ __forceinline__ void prefetch_l2(const void *p) {
-    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
 }
 
 __device__ __forceinline__ float sigmoidf_(float u) { return 1.f / (1.f + __expf(-u)); }
@@ -56,6 +51,28 @@ __device__ __forceinline__ void load_bf16(const __nv_bfloat16 *p, float (&f)[CPL
 }
 
 template <int CPL>
+struct RawOf {
+    using type = uint32_t;
+};
+template <>
+struct RawOf<4> {
+    using type = uint2;
+};
+
+// CPL bf16 channels from shared memory.
+template <int CPL>
+__device__ __forceinline__ void load_smem(const __nv_bfloat16 *p, float (&f)[CPL]) {
+    const typename RawOf<CPL>::type r = *reinterpret_cast<const typename RawOf<CPL>::type *>(p);
+    const __nv_bfloat162 *h2 = reinterpret_cast<const __nv_bfloat162 *>(&r);
+#pragma unroll
+    for (int e = 0; e < CPL / 2; ++e) {
+        const float2 a = __bfloat1622float2(h2[e]);
+        f[2 * e] = a.x;
+        f[2 * e + 1] = a.y;
+    }
+}
+
+template <int CPL>
 __device__ __forceinline__ void store_bf16(__nv_bfloat16 *p, const float (&f)[CPL]) {
     if constexpr (CPL == 4) {
         const __nv_bfloat162 a = __floats2bfloat162_rn(f[0], f[1]), b = __floats2bfloat162_rn(f[2], f[3]);
@@ -74,17 +91,31 @@ struct ProloguePlan {
     gdn_prologue_io io;
 };
 
-// One warp: one (batch, head) row of one of q, k, v over a tile of kTile
-// tokens.  The lane's CPL channels keep the last kconv-1 inputs in registers,
-// so each input is read once (plus kconv-1 tokens of overlap per tile).
+// One CTA (4 warps): one (batch, head) row of one of q, k, v over a tile of
+// kTile tokens.  The tile's input rows, with kMaxConv-1 rows of history in
+// front, are first copied into shared memory with asynchronous 16-byte copies
+// (all in flight at once: the kernel is HBM-bound, not latency-bound); then
+// each warp computes kTile/4 tokens from shared memory, one row per step, and
+// stores its rows straight to global memory.  CTAs are ordered by memory
+// (consecutive CTAs take consecutive heads of one tile).
+constexpr int kHalo = kMaxConv - 1;
+
+__device__ __forceinline__ void cp_async16(void *smem, const void *gmem) {
+    const uint32_t sa = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(sa), "l"(gmem) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_wait_all() {
+    asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+}
+
 template <int CPL>
 __global__ void __launch_bounds__(128) prologue_kernel(ProloguePlan p) {
-    const int lane = threadIdx.x & 31;
-    const int64_t job = static_cast<int64_t>(blockIdx.x) * 4 + (threadIdx.x >> 5);
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    __nv_bfloat16 *rows = reinterpret_cast<__nv_bfloat16 *>(smem_raw);   // [kHalo + kTile][d]
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int64_t job = blockIdx.x;
     const int nrows = 2 * p.Hqk + p.Hv;
-    if (job >= p.B * nrows * p.ntiles) return;
-    // job = (b * ntiles + tile) * nrows + row: consecutive warps take consecutive
-    // heads of one token tile, so the rows in flight are contiguous in memory
     const int row = static_cast<int>(job % nrows);
     const int tile = static_cast<int>((job / nrows) % p.ntiles);
     const int64_t b = job / (static_cast<int64_t>(p.ntiles) * nrows);
@@ -100,58 +131,59 @@ __global__ void __launch_bounds__(128) prologue_kernel(ProloguePlan p) {
     __nv_bfloat16 *sout = static_cast<__nv_bfloat16 *>(
         which == 0 ? p.io.state_q_out : which == 1 ? p.io.state_k_out : p.io.state_v_out);
     __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(which == 0 ? p.io.q : which == 1 ? p.io.k : p.io.v);
+    const int64_t t0 = static_cast<int64_t>(tile) * kTile;
+    const int64_t t1 = t0 + kTile < p.T ? t0 + kTile : p.T;
+    const int nr = static_cast<int>(t1 - t0) + kHalo;   // rows in shared memory: tokens t0-kHalo .. t1-1
+
+    // Stage the rows: 16-byte pieces, d/8 per row.
+    const int per_row = d / 8;
+    for (int idx = tid; idx < nr * per_row; idx += 128) {
+        const int i = idx / per_row, c = idx % per_row;
+        const int64_t t = t0 - kHalo + i;
+        __nv_bfloat16 *dst = rows + i * d + c * 8;
+        const int64_t off = static_cast<int64_t>(h) * d + c * 8;
+        if (t >= 0) {
+            cp_async16(dst, x + (b * p.T + t) * C + off);
+        } else if (sin && t >= -(K - 1)) {
+            *reinterpret_cast<uint4 *>(dst) = *reinterpret_cast<const uint4 *>(sin + (b * (K - 1) + (K - 1 + t)) * C + off);
+        } else {
+            *reinterpret_cast<uint4 *>(dst) = make_uint4(0u, 0u, 0u, 0u);
+        }
+    }
+    cp_async_wait_all();
+    __syncthreads();
 
     const int64_t ch = static_cast<int64_t>(h) * d + lane * CPL;   // first channel of this lane
+    const int cl = lane * CPL;                                      // ... within the head
     // back[e][j]: the tap applied to the input j tokens back (0 = current; 0 beyond K)
     float back[CPL][kMaxConv];
 #pragma unroll
     for (int e = 0; e < CPL; ++e)
 #pragma unroll
-        for (int j = 0; j < kMaxConv; ++j) back[e][j] = (j < K && p.T > 0) ? w[(ch + e) * K + (K - 1 - j)] : 0.f;
-
-    // win[e][i]: input i+1 tokens before the current one (i < K-1)
-    float win[CPL][kMaxConv - 1];
-    const int64_t t0 = static_cast<int64_t>(tile) * kTile;
-#pragma unroll
-    for (int i = 0; i < kMaxConv - 1; ++i) {
-        float f[CPL];
-#pragma unroll
-        for (int e = 0; e < CPL; ++e) f[e] = 0.f;
-        const int64_t t = t0 - 1 - i;
-        if (i < K - 1) {
-            if (t >= 0)
-                load_bf16<CPL>(x + ((b * p.T + t) * C + ch), f);
-            else if (sin)
-                load_bf16<CPL>(sin + ((b * (K - 1) + (K - 1 + t)) * C + ch), f);
-        }
-#pragma unroll
-        for (int e = 0; e < CPL; ++e) win[e][i] = f[e];
-    }
-
-    const int64_t t1 = t0 + kTile < p.T ? t0 + kTile : p.T;
+        for (int j = 0; j < kMaxConv; ++j) back[e][j] = (j < K && t1 > t0) ? w[(ch + e) * K + (K - 1 - j)] : 0.f;
     const bool normalise = which < 2;
-    // The loop below is latency-bound (one row in flight per warp), so rows are
-    // prefetched into L2 kPrefetch tokens ahead of their load.
-    const __nv_bfloat16 *xrow = x + (b * p.T) * C + ch;
+    constexpr int kPerWarp = kTile / 4;
+    const int64_t ta = t0 + warp * kPerWarp;
+    const int64_t tb = ta + kPerWarp < t1 ? ta + kPerWarp : t1;
 #pragma unroll 1
-    for (int64_t t = t0; t < t0 + kPrefetch && t < t1; ++t) prefetch_l2(xrow + t * C);
-#pragma unroll 1
-    for (int64_t t = t0; t < t1; ++t) {
-        if (t + kPrefetch < t1) prefetch_l2(xrow + (t + kPrefetch) * C);
-        float xc[CPL];
-        load_bf16<CPL>(x + ((b * p.T + t) * C + ch), xc);
+    for (int64_t t = ta; t < tb; ++t) {
+        const int i = static_cast<int>(t - t0) + kHalo;
         float u[CPL];
+        float acc[CPL];
+#pragma unroll
+        for (int e = 0; e < CPL; ++e) acc[e] = 0.f;
+#pragma unroll
+        for (int j = 0; j < kMaxConv; ++j) {
+            float f[CPL];
+            load_smem<CPL>(rows + (i - j) * d + cl, f);
+#pragma unroll
+            for (int e = 0; e < CPL; ++e) acc[e] = fmaf(back[e][j], f[e], acc[e]);
+        }
         float ss = 0.f;
 #pragma unroll
         for (int e = 0; e < CPL; ++e) {
-            float acc = back[e][0] * xc[e];
-#pragma unroll
-            for (int i = 0; i < kMaxConv - 1; ++i) acc = fmaf(back[e][i + 1], win[e][i], acc);
-            u[e] = acc * sigmoidf_(acc);
+            u[e] = acc[e] * sigmoidf_(acc[e]);
             ss = fmaf(u[e], u[e], ss);
-#pragma unroll
-            for (int i = kMaxConv - 2; i > 0; --i) win[e][i] = win[e][i - 1];
-            win[e][0] = xc[e];
         }
         if (normalise) {
             const float inv = rsqrtf(warp_allsum(ss) + kL2Eps);
@@ -160,25 +192,22 @@ __global__ void __launch_bounds__(128) prologue_kernel(ProloguePlan p) {
         }
         store_bf16<CPL>(out + ((b * p.T + t) * C + ch), u);
     }
-    if (sout && t1 >= p.T) {
-        // the last K-1 inputs of the sequence (state entries 0 .. K-2, oldest first)
-#pragma unroll
-        for (int i = 0; i < kMaxConv - 1; ++i) {
-            if (i < K - 1) {
-                float f[CPL];
-#pragma unroll
-                for (int e = 0; e < CPL; ++e) f[e] = win[e][i];
-                store_bf16<CPL>(sout + ((b * (K - 1) + (K - 2 - i)) * C + ch), f);
-            }
+    if (sout && t1 >= p.T && warp == 0) {
+        // the last K-1 inputs of the sequence, oldest first
+        for (int j = 0; j < K - 1; ++j) {
+            const int i = nr - (K - 1) + j;
+            *reinterpret_cast<typename RawOf<CPL>::type *>(sout + (b * (K - 1) + j) * C + ch) =
+                *reinterpret_cast<const typename RawOf<CPL>::type *>(rows + i * d + cl);
         }
     }
-    if (which == 2 && t1 > t0) {
+    if (which == 2 && t1 > t0 && tid < kTile) {
         // decay and write gates of this value head over the tile
-        const float eA = __expf(p.io.A[h]), ba = p.io.b_alpha[h];
-        for (int64_t t = t0 + lane; t < t1; t += 32) {
+        const int64_t t = t0 + tid;
+        if (t < t1) {
+            const float eA = __expf(p.io.A[h]), ba = p.io.b_alpha[h];
             const int64_t gi = (b * p.T + t) * p.Hv + h;
-            p.io.alpha[gi] = __expf(-eA * softplusf_(p.io.a_raw[gi] + ba));
-            p.io.beta[gi] = sigmoidf_(p.io.b_raw[gi]);
+            p.io.alpha[gi] = __expf(-eA * softplusf_(__ldg(p.io.a_raw + gi) + ba));
+            p.io.beta[gi] = sigmoidf_(__ldg(p.io.b_raw + gi));
         }
     }
 }
@@ -336,14 +365,15 @@ extern "C" gdn_status gdn_layer_prologue(const gdn_layer_shape *shape, const gdn
     p.kconv = s.kconv;
     p.ntiles = static_cast<int>(s.T == 0 ? 1 : (s.T + kTile - 1) / kTile);
     p.io = a;
-    const int64_t warps = s.B * (2 * s.Hqk + s.Hv) * p.ntiles;
-    if ((warps + 3) / 4 > 0x7fffffff) return GDN_ERR_INVALID_ARG;
-    const dim3 grid(static_cast<unsigned>((warps + 3) / 4));
+    const int64_t ctas = s.B * (2 * s.Hqk + s.Hv) * p.ntiles;
+    if (ctas > 0x7fffffff) return GDN_ERR_INVALID_ARG;
+    const dim3 grid(static_cast<unsigned>(ctas));
+    const size_t smem = static_cast<size_t>(kHalo + kTile) * s.d * 2;
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
     if (s.d == 128)
-        prologue_kernel<4><<<grid, 128, 0, cs>>>(p);
+        prologue_kernel<4><<<grid, 128, smem, cs>>>(p);
     else
-        prologue_kernel<2><<<grid, 128, 0, cs>>>(p);
+        prologue_kernel<2><<<grid, 128, smem, cs>>>(p);
     const cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
