@@ -168,20 +168,30 @@ __global__ void __launch_bounds__(128) prologue_kernel(ProloguePlan p) {
     constexpr int kPerWarp = kTile / 4;
     const int64_t ta = t0 + warp * kPerWarp;
     const int64_t tb = ta + kPerWarp < t1 ? ta + kPerWarp : t1;
+    // win[j][e]: the input j+1 tokens back; one shared-memory row read per token
+    float win[kMaxConv - 1][CPL];
+    if (ta < tb) {
+#pragma unroll
+        for (int j = 0; j < kMaxConv - 1; ++j) load_smem<CPL>(rows + (static_cast<int>(ta - t0) + kHalo - 1 - j) * d + cl, win[j]);
+    }
 #pragma unroll 1
     for (int64_t t = ta; t < tb; ++t) {
         const int i = static_cast<int>(t - t0) + kHalo;
         float u[CPL];
-        float acc[CPL];
+        float acc[CPL], cur[CPL];
+        load_smem<CPL>(rows + i * d + cl, cur);
 #pragma unroll
-        for (int e = 0; e < CPL; ++e) acc[e] = 0.f;
+        for (int e = 0; e < CPL; ++e) {
+            acc[e] = back[e][0] * cur[e];
 #pragma unroll
-        for (int j = 0; j < kMaxConv; ++j) {
-            float f[CPL];
-            load_smem<CPL>(rows + (i - j) * d + cl, f);
-#pragma unroll
-            for (int e = 0; e < CPL; ++e) acc[e] = fmaf(back[e][j], f[e], acc[e]);
+            for (int j = 0; j < kMaxConv - 1; ++j) acc[e] = fmaf(back[e][j + 1], win[j][e], acc[e]);
         }
+#pragma unroll
+        for (int j = kMaxConv - 2; j > 0; --j)
+#pragma unroll
+            for (int e = 0; e < CPL; ++e) win[j][e] = win[j - 1][e];
+#pragma unroll
+        for (int e = 0; e < CPL; ++e) win[0][e] = cur[e];
         float ss = 0.f;
 #pragma unroll
         for (int e = 0; e < CPL; ++e) {
