@@ -12,9 +12,10 @@ and reports it under "decode", and the layer steps around the recurrence
 sigmoid gate times zero-centred RMSNorm) on the prefill shape under "layer".
 
 Printed: one JSON line (rank 0).  `value` is prefill tokens/s summed over all
-ranks; `e2e` is the same metric through the C ABI with host buffers (pinned
-host -> device copies of the inputs and device -> host copies of y and S_T
-inside the timed region); `roofline` is the prefill kernel against measured
+ranks; `e2e` is the same metric through the C ABI with host buffers
+(gdn_prefill_host: pinned host -> device copies of the inputs and device ->
+host copies of y and S_T inside the timed region, overlapped with the
+prefill piece by piece); `roofline` is the prefill kernel against measured
 HBM bandwidth (its binding roof) with its tensor-core fraction beside it;
 `cpu_baseline` is the fp64 oracle timed on a bounded sample on the host cores.
 
@@ -402,30 +403,24 @@ def spot_check(x, y, S_T, w):
 
 
 def time_e2e(args, x, shape, w, dev, ws):
-    """Prefill through the C ABI with host buffers: H2D of inputs, prefill, D2H of y and S_T per step."""
+    """Prefill from host buffers through gdn_prefill_host (the public entry point for host memory):
+    the host-to-device copy of the inputs and the device-to-host copy of y and S_T are inside the
+    timed region, overlapped with the prefill piece by piece (pieces of T/8 tokens)."""
     import torch
 
     from linear_attention_recurrence_14_b300 import gdn
 
     host = {n: getattr(x, n).cpu().pin_memory() for n in ("q", "k", "v", "alpha", "beta")}
-    if x.S0 is not None:
-        host["S0"] = x.S0.cpu().pin_memory()
-    dev_in = {n: torch.empty_like(t, device=dev) for n, t in host.items()}
-    y_dev = torch.empty_like(dev_in["v"])
-    S_dev = torch.empty((w["B"], w["Hv"], w["d"], w["d"]), dtype=torch.float32, device=dev)
+    host["S0"] = x.S0.cpu().pin_memory() if x.S0 is not None else None
     y_host = torch.empty_like(host["v"]).pin_memory()
-    S_host = torch.empty(S_dev.shape, dtype=torch.float32).pin_memory()
-    wsb = gdn.new_workspace(shape, dev)
-    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    S_host = torch.empty((w["B"], w["Hv"], w["d"], w["d"]), dtype=torch.float32).pin_memory()
+    wsb = gdn.new_host_workspace(shape, dev)
+    h2d = sum(t.numel() * t.element_size() for t in host.values() if t is not None)
     d2h = y_host.numel() * y_host.element_size() + S_host.numel() * 4
 
     def step():
-        for n, t in host.items():
-            dev_in[n].copy_(t, non_blocking=True)
-        gdn.prefill(dev_in["q"], dev_in["k"], dev_in["v"], dev_in["alpha"], dev_in["beta"], dev_in.get("S0"),
-                    y=y_dev, S_T=S_dev, workspace=wsb, algorithm=args.algorithm, segments=args.segments)
-        y_host.copy_(y_dev, non_blocking=True)
-        S_host.copy_(S_dev, non_blocking=True)
+        gdn.prefill_host(host["q"], host["k"], host["v"], host["alpha"], host["beta"], host["S0"], y=y_host,
+                         S_T=S_host, workspace=wsb, device=dev)
 
     for _ in range(max(1, args.warmup)):
         step()
@@ -442,7 +437,7 @@ def time_e2e(args, x, shape, w, dev, ws):
     ms = max_over_ranks(e0.elapsed_time(e1), ws, dev)
     value = w["B"] * w["T"] * ws * steps / (ms * 1e-3)
     return {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "steps": steps, "ms_per_step": ms / steps}
+            "steps": steps, "ms_per_step": ms / steps, "api": "gdn_prefill_host (pinned host buffers)"}
 
 
 def layer_bytes(B, T, Hqk, Hv, d, kconv=4) -> tuple[int, int]:

@@ -195,6 +195,32 @@ gdn_status gdn_prefill_noalloc(const gdn_shape *shape,
                                const float *alpha, const float *beta,
                                const float *S0, void *y, float *S_T, void *stream);
 
+/*
+ * Prefill from host memory.  q, k, v, alpha, beta, S0 (NULL = zero state),
+ * y and S_T (NULL = not returned) are host buffers in the layouts above; they
+ * should be page-locked (cudaHostAlloc / cudaHostRegister) for the copies to
+ * overlap, and are otherwise copied synchronously.  The sequence is cut into
+ * pieces of tokens_per_piece tokens (0 = about an eighth of T, a multiple of
+ * 64); piece p's host-to-device copy, piece p-1's prefill and piece p-2's
+ * device-to-host copy of y run concurrently on two internal streams and
+ * `stream`.  Each piece starts from the state the previous one left, so the
+ * result is that of gdn_prefill over the whole sequence up to rounding.
+ *
+ * ws: device memory of gdn_prefill_host_workspace_bytes(shape,
+ * tokens_per_piece) bytes, 256-byte aligned, whose first 256 bytes are zero
+ * (as for gdn_prefill): two piece-sized copies of the inputs and y, two state
+ * buffers and a prefill workspace.  The device status of the prefills is read
+ * with gdn_read_device_status(ws, stream).  The call returns once the work is
+ * queued; `stream` waits for every copy, so a synchronisation of `stream`
+ * means that y and S_T are in host memory.
+ */
+size_t gdn_prefill_host_workspace_bytes(const gdn_shape *shape, int64_t tokens_per_piece);
+
+gdn_status gdn_prefill_host(const gdn_shape *shape, int64_t tokens_per_piece,
+                            const void *q, const void *k, const void *v,
+                            const float *alpha, const float *beta, const float *S0,
+                            void *y, float *S_T, void *ws, size_t ws_bytes, void *stream);
+
 /* 1 if the current CUDA device can run these kernels (compute capability 10.3). */
 int gdn_device_supported(void);
 

@@ -27,7 +27,8 @@ ALGO_NAMES = {ALGO_AUTO: "auto", ALGO_CHUNKED: "chunked", ALGO_SEQUENTIAL: "sequ
 # Every symbol include/gdn.h and include/gdn_layer.h declare.
 EXPORTS = ("gdn_status_string", "gdn_prefill_workspace_bytes", "gdn_prefill", "gdn_prefill_ex",
            "gdn_decode_step", "gdn_read_device_status", "gdn_device_supported", "gdn_abi_version",
-           "gdn_prefill_noalloc", "gdn_layer_prologue", "gdn_layer_epilogue")
+           "gdn_prefill_noalloc", "gdn_layer_prologue", "gdn_layer_epilogue", "gdn_prefill_host_workspace_bytes",
+           "gdn_prefill_host")
 NOALLOC_SCRATCH_BYTES = 256 + 8 * 1024 * 1024
 
 
@@ -92,6 +93,10 @@ def lib() -> ctypes.CDLL:
             L.gdn_layer_prologue.argtypes = [ctypes.POINTER(GdnLayerShape), ctypes.POINTER(GdnPrologueIO), vp]
             L.gdn_layer_epilogue.restype = ctypes.c_int
             L.gdn_layer_epilogue.argtypes = [ctypes.POINTER(GdnLayerShape), vp, vp, fp, ctypes.c_float, vp, vp]
+            L.gdn_prefill_host_workspace_bytes.restype = c_size
+            L.gdn_prefill_host_workspace_bytes.argtypes = [sp, ctypes.c_int64]
+            L.gdn_prefill_host.restype = ctypes.c_int
+            L.gdn_prefill_host.argtypes = [sp, ctypes.c_int64, vp, vp, vp, fp, fp, fp, vp, fp, vp, c_size, vp]
             L.gdn_device_supported.restype = ctypes.c_int
             L.gdn_abi_version.restype = ctypes.c_int
             _lib = L
@@ -252,6 +257,47 @@ def layer_epilogue(y, z, norm_w, eps=1e-6, *, o=None, Hqk=None, stream=None):
                                   _stream(stream))
     _check(rc, "gdn_layer_epilogue")
     return o
+
+
+def host_workspace_bytes(shape: GdnShape, tokens_per_piece: int = 0) -> int:
+    return int(lib().gdn_prefill_host_workspace_bytes(ctypes.byref(shape), int(tokens_per_piece)))
+
+
+def new_host_workspace(shape: GdnShape, device, tokens_per_piece: int = 0) -> torch.Tensor:
+    """A zeroed device workspace for gdn_prefill_host."""
+    n = host_workspace_bytes(shape, tokens_per_piece)
+    if n == 0:
+        raise ValueError("invalid shape for gdn_prefill_host")
+    return torch.zeros(n, dtype=torch.uint8, device=device)
+
+
+def prefill_host(q, k, v, alpha, beta, S0=None, *, y=None, S_T=None, workspace=None, tokens_per_piece=0,
+                 device=None, stream=None):
+    """Run gdn_prefill_host on host (CPU, preferably pinned) tensors; returns (y, S_T) as host tensors.
+
+    The copies overlap the prefill; the call returns once the work is queued on `stream`
+    (default: the current stream of `device`), so synchronise before reading y and S_T."""
+    for name, t in dict(q=q, k=k, v=v, alpha=alpha, beta=beta, S0=S0, y=y, S_T=S_T).items():
+        if t is not None and (t.is_cuda or not t.is_contiguous()):
+            raise ValueError(f"{name} must be a contiguous host tensor")
+    shape = shape_of(q, v)
+    if y is None:
+        y = torch.empty_like(v).pin_memory()
+    if S_T is None:
+        S_T = torch.empty((shape.B, shape.Hv, shape.dk, shape.dv), dtype=torch.float32).pin_memory()
+    if device is None:
+        device = torch.device("cuda", torch.cuda.current_device())
+    if workspace is None:
+        workspace = new_host_workspace(shape, device, tokens_per_piece)
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    rc = lib().gdn_prefill_host(ctypes.byref(shape), int(tokens_per_piece), _ptr(q), _ptr(k), _ptr(v),
+                                _ptr(alpha), _ptr(beta), _ptr(S0), _ptr(y), _ptr(S_T), _ptr(workspace),
+                                workspace.numel() * workspace.element_size(), ctypes.c_void_p(stream.cuda_stream))
+    _check(rc, "gdn_prefill_host")
+    # the work is still in flight: keep the device workspace from being reused before it ends
+    workspace.record_stream(stream)
+    return y, S_T
 
 
 def prefill_launches(shape: GdnShape, algorithm=ALGO_AUTO, segments=0) -> int:

@@ -156,3 +156,32 @@ def test_layer_epilogue_rejects_bad_arguments(L):
     assert L.gdn_layer_epilogue(s, vp(BASE + 8), z, w, 1e-6, o, None) == E["GDN_ERR_ALIGNMENT"]
     assert L.gdn_layer_epilogue(s, y, z, w, 1e-6, y, None) == E["GDN_ERR_ALIASING"]
     assert L.gdn_layer_epilogue(ctypes.byref(layer_shape(d=32)), y, z, w, 1e-6, o, None) == E["GDN_ERR_UNSUPPORTED"]
+
+
+def test_host_prefill_workspace_and_arguments(L):
+    E = {v: k for k, v in gdn.STATUS_NAMES.items()}
+    s = shape(B=2, T=1000, Hqk=2, Hv=4, d=128)
+    # pieces of 256 tokens: prefill workspace, two states, two slots of (q, k, v, y, alpha, beta)
+    r = lambda n: (n + 255) // 256 * 256  # noqa: E731
+    inner = r(256 + 2 * 4 * 128 * 128 * 4)
+    state = r(2 * 4 * 128 * 128 * 4)
+    slot = 2 * r(2 * 256 * 2 * 128 * 2) + 2 * r(2 * 256 * 4 * 128 * 2) + 2 * r(2 * 256 * 4 * 4)
+    assert gdn.host_workspace_bytes(s, 256) == inner + 2 * state + 2 * slot
+    # default pieces: about T/8 tokens, a multiple of 64
+    assert gdn.host_workspace_bytes(s, 0) == gdn.host_workspace_bytes(s, 128)
+    assert gdn.host_workspace_bytes(s, -1) == 0
+    assert gdn.host_workspace_bytes(shape(Hqk=3, Hv=4), 0) == 0
+    vp = lambda x: None if x is None else ctypes.c_void_p(x)  # noqa: E731
+    n = gdn.host_workspace_bytes(s, 256)
+
+    def call(shp=s, tpp=256, q=BASE, ws=BASE + 512 * MB, ws_bytes=n):
+        return L.gdn_prefill_host(ctypes.byref(shp), tpp, vp(q), vp(BASE + MB), vp(BASE + 2 * MB),
+                                  vp(BASE + 3 * MB), vp(BASE + 4 * MB), None, vp(BASE + 5 * MB), None, vp(ws),
+                                  ws_bytes, None)
+    assert call(shp=shape(Hqk=3, Hv=4)) == E["GDN_ERR_INVALID_ARG"]
+    assert call(shp=gdn.GdnShape(1, 64, 1, 1, 96, 96, 1)) == E["GDN_ERR_UNSUPPORTED"]
+    assert call(tpp=-5) == E["GDN_ERR_INVALID_ARG"]
+    assert call(ws=None) == E["GDN_ERR_WORKSPACE"]
+    assert call(ws_bytes=n - 1) == E["GDN_ERR_WORKSPACE"]
+    assert call(ws=BASE + 512 * MB + 16) == E["GDN_ERR_ALIGNMENT"]
+    assert call(q=None) == E["GDN_ERR_INVALID_ARG"]
