@@ -69,10 +69,10 @@ def decode_bytes(w: dict, esz: int = 2) -> int:
 
 
 # DRAM bytes per launch measured by ncu (dram__bytes_read.sum + dram__bytes_write.sum,
-# summaries under profiles/), valid only for the kernel sources they were taken on:
-# a changed source reports null instead.
+# summaries under profiles/), valid only for the kernel sources they were taken on
+# (or sources that differ from them in comments only): a changed source reports null.
 MEASURED_TRAFFIC = {
-    "prefill": {"sources": ("csrc/chunked_tc.cu", "csrc/tc_ptx.cuh"), "sha256_16": "dbd744968591eef3", "bytes": 1.653944e9},
+    "prefill": {"sources": ("csrc/chunked_tc.cu", "csrc/tc_ptx.cuh"), "sha256_16": "7e2f27312b22fa65", "bytes": 1.653944e9},
     "decode": {"sources": ("csrc/recurrent.cu",), "sha256_16": "f853d2d1c9ebcc76", "bytes": 1.021497e9},
 }
 

@@ -15,7 +15,7 @@
 //   S_C  = gamma_C S0 + K~^T U,   K~_i = e^{g_C - g_i} k_i
 // Every contraction runs as an M = 128 tcgen05 MMA in the value-major
 // (transposed) orientation, so the state's value dimension is the TMEM lane:
-//   Gram   [K;Q] K^T            -> KK^T (lanes 0-63), QK^T (lanes 64-127)
+//   Gram   [Q;K] K^T            -> QK^T (lanes 0-63), KK^T (lanes 64-127)
 //   W^T  = K^T (T diag(beta gamma))^T,   U~^T = V^T (T diag(beta))^T
 //   U^T  = U~^T + S^T (-W)^T              (accumulated onto U~^T)
 //   Y^T  = S^T Q~^T + U^T P^T             (Q~ = diag(gamma) Q)
@@ -30,11 +30,14 @@
 // difference to the exact state by that factor times the state norm.
 //
 // Warp roles (512 threads):
-//   warp 0        TMA producer (one thread): K, Q, V tiles of each chunk
-//   warp 1        MMA issuer (one thread); owns the TMEM allocation
-//   warps 2-3     gates of each chunk (one chunk ahead of the local warpgroup)
-//   warps 4-7     "local" warpgroup: gated Gram products, the triangular
-//                 solve, the T, P and -W operands (Q~, K~ on the exact path)
+//   warp 0        TMA producer (one thread): Q, K, V tiles of each chunk
+//   warp 1        MMA issuer (the whole warp runs the control flow, lane 0
+//                 issues); owns the TMEM allocation
+//   warps 2-3     gates of each chunk, then its A rows (KK^T, TMEM lanes
+//                 64-127) and the diagonal blocks of T = (I + A)^{-1}
+//   warps 4-7     "local" warpgroup: the off-diagonal blocks of T and the
+//                 bf16 T operands, the P rows (QK^T), the -W operand (Q~, K~
+//                 on the exact path)
 //   warps 8-15    "chain" warpgroups: the fp32 state (dv lane x dk half),
 //                 U conversion, state update, y output
 #include <cuda.h>
