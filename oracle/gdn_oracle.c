@@ -31,6 +31,14 @@
  *
  * Each (b, h) pair is an independent sequential loop; pairs are spread over
  * POSIX threads.  No blocking, fusion or reordering beyond the definition.
+ *
+ * Channel-wise decay (gdn_oracle_recurrence_cw): the decay gate is a vector
+ * alpha_t in (0,1]^dk per value head, layout [B, T, Hv, dk], and the decay
+ * step scales row i of the state (key dimension i) by alpha_t[i]:
+ *     S~ = diag(alpha_t) S_{t-1}
+ * -- the per-channel ("diagonal") gate of Kimi Delta Attention, which the
+ * pages name as the same family of fast delta-rule kernels (section 2.1, "Why
+ * the delta rule matters").  The other three lines are unchanged.
  */
 #include <pthread.h>
 #include <stdint.h>
@@ -40,6 +48,7 @@
 typedef struct {
     int64_t B, T;
     int Hqk, Hv, dk, dv;
+    int alpha_cw;            /* 1: alpha is [B, T, Hv, dk] (per key channel) */
     const double *q, *k, *v, *alpha, *beta, *S0;
     double *y, *S_T;
     int64_t next;            /* next (b, h) pair to take */
@@ -60,16 +69,20 @@ static void run_head(const oracle_job *J, int64_t b, int hv, double *S, double *
 
     for (int64_t t = 0; t < J->T; ++t) {
         const size_t tok = (size_t)b * (size_t)J->T + (size_t)t;
-        const double a = J->alpha[tok * J->Hv + hv];
+        const double *at = J->alpha + (J->alpha_cw ? (tok * J->Hv + hv) * (size_t)dk : tok * J->Hv + hv);
         const double bt = J->beta[tok * J->Hv + hv];
         const double *kt = J->k + (tok * J->Hqk + hk) * dk;
         const double *qt = J->q + (tok * J->Hqk + hk) * dk;
         const double *vt = J->v + (tok * J->Hv + hv) * dv;
         double *yt = J->y + (tok * J->Hv + hv) * dv;
 
-        /* S~ = alpha_t S_{t-1} */
-        for (size_t i = 0; i < state_elems; ++i)
-            S[i] *= a;
+        /* S~ = alpha_t S_{t-1}, or diag(alpha_t) S_{t-1} per key channel */
+        for (int i = 0; i < dk; ++i) {
+            const double a = J->alpha_cw ? at[i] : at[0];
+            double *row = S + (size_t)i * dv;
+            for (int j = 0; j < dv; ++j)
+                row[j] *= a;
+        }
 
         /* e_t = v_t - S~^T k_t :  e[j] = v[j] - sum_i S~[i][j] k[i] */
         for (int j = 0; j < dv; ++j)
@@ -131,17 +144,17 @@ static void *worker(void *arg)
  * Returns 0 on success, 1 on invalid arguments, 2 on allocation or thread
  * failure.  y must hold B*T*Hv*dv doubles; S_T (may be NULL) B*Hv*dk*dv.
  */
-int gdn_oracle_recurrence(int64_t B, int64_t T, int Hqk, int Hv, int dk, int dv,
-                          const double *q, const double *k, const double *v,
-                          const double *alpha, const double *beta, const double *S0,
-                          double *y, double *S_T, int n_threads)
+static int run_all(int64_t B, int64_t T, int Hqk, int Hv, int dk, int dv, int alpha_cw,
+                   const double *q, const double *k, const double *v,
+                   const double *alpha, const double *beta, const double *S0,
+                   double *y, double *S_T, int n_threads)
 {
     if (B < 0 || T < 0 || Hqk <= 0 || Hv <= 0 || dk <= 0 || dv <= 0 || Hv % Hqk != 0)
         return 1;
     if ((B * T > 0) && (!q || !k || !v || !alpha || !beta || !y))
         return 1;
     oracle_job J;
-    J.B = B; J.T = T; J.Hqk = Hqk; J.Hv = Hv; J.dk = dk; J.dv = dv;
+    J.B = B; J.T = T; J.Hqk = Hqk; J.Hv = Hv; J.dk = dk; J.dv = dv; J.alpha_cw = alpha_cw;
     J.q = q; J.k = k; J.v = v; J.alpha = alpha; J.beta = beta; J.S0 = S0;
     J.y = y; J.S_T = S_T;
     J.next = 0;
@@ -171,4 +184,21 @@ int gdn_oracle_recurrence(int64_t B, int64_t T, int Hqk, int Hv, int dk, int dv,
     free(th);
     pthread_mutex_destroy(&J.lock);
     return rc;
+}
+
+int gdn_oracle_recurrence(int64_t B, int64_t T, int Hqk, int Hv, int dk, int dv,
+                          const double *q, const double *k, const double *v,
+                          const double *alpha, const double *beta, const double *S0,
+                          double *y, double *S_T, int n_threads)
+{
+    return run_all(B, T, Hqk, Hv, dk, dv, 0, q, k, v, alpha, beta, S0, y, S_T, n_threads);
+}
+
+/* As gdn_oracle_recurrence with alpha of layout [B, T, Hv, dk] (channel-wise decay). */
+int gdn_oracle_recurrence_cw(int64_t B, int64_t T, int Hqk, int Hv, int dk, int dv,
+                             const double *q, const double *k, const double *v,
+                             const double *alpha, const double *beta, const double *S0,
+                             double *y, double *S_T, int n_threads)
+{
+    return run_all(B, T, Hqk, Hv, dk, dv, 1, q, k, v, alpha, beta, S0, y, S_T, n_threads);
 }

@@ -45,11 +45,12 @@ def _load():
         build()
         lib = ctypes.CDLL(_LIB)
         dp = ctypes.POINTER(ctypes.c_double)
-        lib.gdn_oracle_recurrence.restype = ctypes.c_int
-        lib.gdn_oracle_recurrence.argtypes = [
-            ctypes.c_int64, ctypes.c_int64, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
-            dp, dp, dp, dp, dp, dp, dp, dp, ctypes.c_int,
-        ]
+        for fn in (lib.gdn_oracle_recurrence, lib.gdn_oracle_recurrence_cw):
+            fn.restype = ctypes.c_int
+            fn.argtypes = [
+                ctypes.c_int64, ctypes.c_int64, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                dp, dp, dp, dp, dp, dp, dp, dp, ctypes.c_int,
+            ]
         _lib = lib
     return _lib
 
@@ -74,21 +75,26 @@ def _ptr(a):
 def recurrence(q, k, v, alpha, beta, S0=None, threads: int | None = None):
     """Run the recurrence on full tensors.
 
-    q, k: [B, T, Hqk, dk]; v: [B, T, Hv, dv]; alpha, beta: [B, T, Hv];
+    q, k: [B, T, Hqk, dk]; v: [B, T, Hv, dv]; beta: [B, T, Hv]; alpha: [B, T, Hv]
+    (scalar decay) or [B, T, Hv, dk] (channel-wise decay, S~ = diag(alpha_t) S);
     S0: [B, Hv, dk, dv] or None (zeros).  Returns (y [B,T,Hv,dv], S_T [B,Hv,dk,dv])
     as float64 numpy arrays.
     """
     q, k, v, alpha, beta, S0 = (_f64(t) for t in (q, k, v, alpha, beta, S0))
     B, T, Hqk, dk = q.shape
     Hv, dv = v.shape[2], v.shape[3]
-    if k.shape != q.shape or v.shape[:2] != (B, T) or alpha.shape != (B, T, Hv) or beta.shape != (B, T, Hv):
+    cw = alpha.ndim == 4
+    if k.shape != q.shape or v.shape[:2] != (B, T) or beta.shape != (B, T, Hv):
         raise ValueError("inconsistent shapes")
+    if alpha.shape != ((B, T, Hv, dk) if cw else (B, T, Hv)):
+        raise ValueError("alpha shape")
     if S0 is not None and S0.shape != (B, Hv, dk, dv):
         raise ValueError("S0 shape")
     y = np.zeros((B, T, Hv, dv), dtype=np.float64)
     S_T = np.zeros((B, Hv, dk, dv), dtype=np.float64)
     nthreads = threads if threads is not None else (os.cpu_count() or 1)
-    rc = _load().gdn_oracle_recurrence(
+    fn = _load().gdn_oracle_recurrence_cw if cw else _load().gdn_oracle_recurrence
+    rc = fn(
         B, T, Hqk, Hv, dk, dv, _ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(beta), _ptr(S0),
         _ptr(y), _ptr(S_T), nthreads,
     )

@@ -15,7 +15,7 @@ SRC = os.path.join(os.path.dirname(ormod.__file__), "gdn_oracle.c")
 
 MUTATIONS = {
     # e formed from the undecayed state (the walkthrough snippet's reading)
-    "undecayed_residual": ("for (size_t i = 0; i < state_elems; ++i)\n            S[i] *= a;", "/* no decay */"),
+    "undecayed_residual": ("                row[j] *= a;", "                row[j] *= 1.0 + 0.0 * a;"),
     # output read before the write
     "read_before_write": ("/* S_t = S~ + beta_t k_t e_t^T */", "/* write skipped */ if (0)"),
     # wrong sign of the residual
