@@ -73,7 +73,7 @@ def decode_bytes(w: dict, esz: int = 2) -> int:
 # (or sources that differ from them in comments only): a changed source reports null.
 MEASURED_TRAFFIC = {
     "prefill": {"sources": ("csrc/chunked_tc.cu", "csrc/tc_ptx.cuh"), "sha256_16": "7e2f27312b22fa65", "bytes": 1.653944e9},
-    "decode": {"sources": ("csrc/recurrent.cu",), "sha256_16": "f853d2d1c9ebcc76", "bytes": 1.021497e9},
+    "decode": {"sources": ("csrc/recurrent.cu",), "sha256_16": "a3dc266465d55bf7", "bytes": 1.021420e9},
 }
 
 
@@ -354,9 +354,10 @@ def run_ours(args, ws, rank, local):
     torch.cuda.empty_cache()
 
     # ------------------------------------------------------------- decode
-    dec = None
+    dec = dec_cw = None
     if not args.no_decode:
         dec = time_decode(args, peaks, seed, dev, ws, local)
+        dec_cw = time_decode(args, peaks, seed, dev, ws, local, channelwise=True)
 
     # ------------------------------------------------------------- layer prologue / epilogue
     layer = None
@@ -381,7 +382,7 @@ def run_ours(args, ws, rank, local):
                    "algorithm": gdn.ALGO_NAMES[args.algorithm], "segments": args.segments,
                    "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"},
         "roofline": roofline, "clocks": clocks, "e2e": e2e, "cpu_baseline": cpu, "gpu_launches": gpu_launches,
-        "decode": dec, "layer": layer, "check": check,
+        "decode": dec, "decode_channelwise": dec_cw, "layer": layer, "check": check,
     }
     if rank == 0:
         print(json.dumps(line), flush=True)
@@ -498,12 +499,13 @@ def time_layer(args, peaks, seed, dev, ws, local):
     return res
 
 
-def time_decode(args, peaks, seed, dev, ws, local):
-    """128 decode steps of the decode workload, state in place; returns steps/s and its HBM roofline."""
+def time_decode(args, peaks, seed, dev, ws, local, channelwise=False):
+    """128 decode steps of the decode workload, state in place; returns steps/s and its HBM roofline.
+    channelwise: the per-key-channel decay gate (gdn_decode_step_cw, alpha [B, 1, Hv, dk])."""
     import torch
 
     from linear_attention_recurrence_14_b300 import gdn
-    from linear_attention_recurrence_14_b300.inputs import WORKLOADS, make_decode_inputs
+    from linear_attention_recurrence_14_b300.inputs import WORKLOADS, make_channelwise_alpha, make_decode_inputs
 
     w = dict(WORKLOADS[DECODE_WORKLOAD])
     nsteps = args.decode_steps
@@ -511,10 +513,19 @@ def time_decode(args, peaks, seed, dev, ws, local):
                            seed=seed, device=dev)
     S = d.S0.clone()
     ys = torch.empty((nsteps,) + tuple(d.v.shape[1:]), dtype=d.v.dtype, device=dev)
+    if channelwise:
+        acw = make_channelwise_alpha(nsteps * w["B"], 1, w["Hv"], w["d"], w["decay_scale"], seed=seed, device=dev)
+        acw = acw.reshape(nsteps, w["B"], 1, w["Hv"], w["d"])
+
+    def one(s):
+        if channelwise:
+            gdn.decode_step_cw(d.q[s], d.k[s], d.v[s], acw[s], d.beta[s], S, y=ys[s])
+        else:
+            gdn.decode_step(d.q[s], d.k[s], d.v[s], d.alpha[s], d.beta[s], S, y=ys[s])
 
     def run_all():
         for s in range(nsteps):
-            gdn.decode_step(d.q[s], d.k[s], d.v[s], d.alpha[s], d.beta[s], S, y=ys[s])
+            one(s)
 
     for _ in range(max(1, args.warmup)):
         S.copy_(d.S0)
@@ -530,22 +541,24 @@ def time_decode(args, peaks, seed, dev, ws, local):
         a0.record(stream)
         for s in range(nsteps):
             evs[s][0].record(stream)
-            gdn.decode_step(d.q[s], d.k[s], d.v[s], d.alpha[s], d.beta[s], S, y=ys[s])
+            one(s)
             evs[s][1].record(stream)
         a1.record(stream)
         torch.cuda.synchronize()
     total_ms = max_over_ranks(a0.elapsed_time(a1), ws, dev)
     per = [a.elapsed_time(b) for a, b in evs]
     kern_s = statistics.mean(per) * 1e-3
-    nbytes = decode_bytes(w)
+    nbytes = decode_bytes(w) + (w["B"] * w["Hv"] * (w["d"] - 1) * 4 if channelwise else 0)
     gbs = nbytes / kern_s / 1e9
     return {
-        "metric": "decode steps/s (B=256, Hv=32, Hqk=16, d=128, fp32 state in place, bf16 q/k/v)",
+        "metric": "decode steps/s (B=256, Hv=32, Hqk=16, d=128, fp32 state in place, bf16 q/k/v"
+                  + (", channel-wise decay gate)" if channelwise else ")"),
         "value": nsteps * ws / (total_ms * 1e-3), "unit": "steps/s", "steps": nsteps, "ms_per_step": total_ms / nsteps,
         "gpu_launches": nsteps,
         "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": gbs / peaks["hbm_gbs"],
-                     "traffic": args.decode_traffic if args.decode_traffic is not None else measured_traffic("decode"),
+                     "traffic": None if channelwise else (
+                         args.decode_traffic if args.decode_traffic is not None else measured_traffic("decode")),
                      "bytes_per_launch": nbytes,
                      "launch_ms": kern_s * 1e3, "peak_source": peaks["source"]},
         "clocks": clk.summary(),

@@ -196,6 +196,25 @@ gdn_status gdn_prefill_noalloc(const gdn_shape *shape,
                                const float *S0, void *y, float *S_T, void *stream);
 
 /*
+ * Channel-wise decay: the decay gate is a vector over the key dimension,
+ * alpha [B, T, Hv, dk] fp32 (16-byte aligned), and the decay step scales row
+ * i of the state by alpha_t[i]: S~ = diag(alpha_t) S_{t-1}; the other three
+ * lines of the recurrence are unchanged.  This is the per-channel ("diagonal")
+ * gate of Kimi Delta Attention, which the reading notes name beside the delta
+ * rule (section 2.1, "Why the delta rule matters").  With all channels equal
+ * it is the scalar recurrence.  Both calls run the token-sequential kernel
+ * (dtype bf16 or fp32, state in fp32 registers); they need no workspace, and
+ * S_T may equal S0.  Layouts, ownership and errors otherwise as gdn_prefill
+ * and gdn_decode_step.
+ */
+gdn_status gdn_prefill_cw(const gdn_shape *shape, const void *q, const void *k, const void *v,
+                          const float *alpha, const float *beta, const float *S0, void *y, float *S_T,
+                          void *stream);
+
+gdn_status gdn_decode_step_cw(const gdn_shape *shape, const void *q, const void *k, const void *v,
+                              const float *alpha, const float *beta, float *S_inout, void *y, void *stream);
+
+/*
  * Prefill from host memory.  q, k, v, alpha, beta, S0 (NULL = zero state),
  * y and S_T (NULL = not returned) are host buffers in the layouts above; they
  * should be page-locked (cudaHostAlloc / cudaHostRegister) for the copies to

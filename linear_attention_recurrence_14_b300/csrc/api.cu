@@ -235,6 +235,61 @@ gdn_status gdn_decode_step(const gdn_shape *shape, const void *q, const void *k,
                                            static_cast<cudaStream_t>(stream_)));
 }
 
+// Channel-wise decay (alpha [B, T, Hv, dk]): the token-sequential kernel for
+// prefill (any T, dtype bf16 or fp32) and decode (T == 1); S_T may equal S0.
+static gdn_status recurrence_cw(const gdn_shape *shape, bool decode, const void *q, const void *k, const void *v,
+                                const float *alpha, const float *beta, const float *S0, float *S_T, void *y,
+                                void *stream_) {
+    int64_t n_qk, n_v, n_gate, n_state;
+    gdn_status st = check_shape(shape, &n_qk, &n_v, &n_gate, &n_state);
+    if (st != GDN_OK) return st;
+    const gdn_shape &s = *shape;
+    if (decode && s.T != 1) return GDN_ERR_INVALID_ARG;
+    if (decode && !S_T) return GDN_ERR_INVALID_ARG;
+    const bool has_tokens = s.B * s.T > 0;
+    if (has_tokens && (!q || !k || !v || !alpha || !beta || !y)) return GDN_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(y, 16) || !aligned(S0, 16) ||
+        !aligned(S_T, 16) || !aligned(alpha, 16) || !aligned(beta, 4))
+        return GDN_ERR_ALIGNMENT;
+    const size_t esz = s.dtype == GDN_BF16 ? 2 : 4;
+    const Range rq{q, static_cast<size_t>(n_qk) * esz}, rk{k, static_cast<size_t>(n_qk) * esz};
+    const Range rv{v, static_cast<size_t>(n_v) * esz}, ry{y, static_cast<size_t>(n_v) * esz};
+    const Range ra{alpha, static_cast<size_t>(n_gate) * s.dk * 4}, rb{beta, static_cast<size_t>(n_gate) * 4};
+    const Range rs0{S0, static_cast<size_t>(n_state) * 4}, rst{S_T, static_cast<size_t>(n_state) * 4};
+    for (const Range &in : {rq, rk, rv, ra, rb, rs0, rst})
+        if (overlap(ry, in)) return GDN_ERR_ALIASING;
+    for (const Range &in : {rq, rk, rv, ra, rb})
+        if (overlap(rst, in)) return GDN_ERR_ALIASING;
+    if (S0 != S_T && overlap(rst, rs0)) return GDN_ERR_ALIASING;
+    int num_sms = 0;
+    st = check_device(&num_sms);
+    if (st != GDN_OK) return st;
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+    if (s.B * s.Hv == 0) return GDN_OK;
+    if (!has_tokens) {
+        if (S_T && S_T != S0) {
+            if (S0) return from_cuda(cudaMemcpyAsync(S_T, S0, rst.n, cudaMemcpyDeviceToDevice, stream));
+            return from_cuda(cudaMemsetAsync(S_T, 0, rst.n, stream));
+        }
+        return GDN_OK;
+    }
+    gdn::RecurrentParams p{};
+    p.B = s.B; p.T = s.T; p.Hqk = s.Hqk; p.Hv = s.Hv; p.group = s.Hv / s.Hqk;
+    p.q = q; p.k = k; p.v = v; p.alpha = alpha; p.beta = beta; p.alpha_cw = true;
+    p.S_in = S0; p.S_out = S_T; p.y = y;
+    return from_cuda(gdn::launch_recurrent(p, s.dk, s.dv, static_cast<gdn_dtype>(s.dtype), stream));
+}
+
+gdn_status gdn_prefill_cw(const gdn_shape *shape, const void *q, const void *k, const void *v, const float *alpha,
+                          const float *beta, const float *S0, void *y, float *S_T, void *stream) {
+    return recurrence_cw(shape, false, q, k, v, alpha, beta, S0, S_T, y, stream);
+}
+
+gdn_status gdn_decode_step_cw(const gdn_shape *shape, const void *q, const void *k, const void *v,
+                              const float *alpha, const float *beta, float *S_inout, void *y, void *stream) {
+    return recurrence_cw(shape, true, q, k, v, alpha, beta, S_inout, S_inout, y, stream);
+}
+
 gdn_status gdn_read_device_status(void *ws, void *stream_) {
     if (!ws) return GDN_ERR_INVALID_ARG;
     cudaStream_t stream = static_cast<cudaStream_t>(stream_);

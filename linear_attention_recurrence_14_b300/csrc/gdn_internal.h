@@ -19,7 +19,8 @@ struct RecurrentParams {
     int64_t B, T;
     int Hqk, Hv, group;          // group = Hv / Hqk
     const void *q, *k, *v;       // [B, T, Hqk, dk] / [B, T, Hv, dv]
-    const float *alpha, *beta;   // [B, T, Hv]
+    const float *alpha, *beta;   // [B, T, Hv] ([B, T, Hv, dk] for alpha when alpha_cw)
+    bool alpha_cw;               // channel-wise decay: S~ = diag(alpha_t) S
     const float *S_in;           // [B, Hv, dk, dv] or nullptr (zero state)
     float *S_out;                // [B, Hv, dk, dv] or nullptr
     void *y;                     // [B, T, Hv, dv]

@@ -17,6 +17,11 @@
 // Used for decode (T = 1: the state is streamed HBM -> registers -> HBM
 // once, the kernel is bound by HBM bandwidth) and for fp32 prefill, where the
 // state stays in registers across all T tokens.
+//
+// Channel-wise decay (CW): alpha_t is a vector over the key dimension and
+// S~ = diag(alpha_t) S, so row i of the state decays by alpha_t[i]:
+//   r_k = S^T (alpha o k),  r_q = S^T (alpha o q),  e = v - r_k,
+//   y = r_q + beta (k.q) e,  S = diag(alpha) S + beta k e^T.
 #include <cuda_bf16.h>
 
 #include "gdn_internal.h"
@@ -107,7 +112,7 @@ __device__ __forceinline__ void store_state_row(float *__restrict__ dst, const f
     }
 }
 
-template <int DK, int DV, typename TIn>
+template <int DK, int DV, typename TIn, bool CW>
 __global__ void __launch_bounds__(kThreads, 2) recurrent_kernel(RecurrentParams p) {
     constexpr int R = DK / kWarps;   // state rows per warp
     constexpr int C = DV / 32;       // state columns per lane
@@ -154,8 +159,14 @@ __global__ void __launch_bounds__(kThreads, 2) recurrent_kernel(RecurrentParams 
         load_row<TIn, R>(k + (tok * p.Hqk + hk) * DK + row0, kr);
         load_row<TIn, R>(q + (tok * p.Hqk + hk) * DK + row0, qr);
         load_row<TIn, C>(v + (tok * p.Hv + hv) * DV + col0, vr);
-        const float a = __ldg(p.alpha + tok * p.Hv + hv);
         const float bt = __ldg(p.beta + tok * p.Hv + hv);
+        // a: the scalar gate; ar: the gate of each of this warp's rows (CW)
+        float a = 1.f, ar[R];
+        if constexpr (CW) {
+            load_row<float, R>(p.alpha + (tok * p.Hv + hv) * DK + row0, ar);
+        } else {
+            a = __ldg(p.alpha + tok * p.Hv + hv);
+        }
 
         float pk[C], pq[C];
 #pragma unroll
@@ -164,10 +175,11 @@ __global__ void __launch_bounds__(kThreads, 2) recurrent_kernel(RecurrentParams 
 #pragma unroll
         for (int r = 0; r < R; ++r) {
             kq = fmaf(kr[r], qr[r], kq);
+            const float ka = CW ? ar[r] * kr[r] : kr[r], qa = CW ? ar[r] * qr[r] : qr[r];
 #pragma unroll
             for (int c = 0; c < C; ++c) {
-                pk[c] = fmaf(S[r][c], kr[r], pk[c]);
-                pq[c] = fmaf(S[r][c], qr[r], pq[c]);
+                pk[c] = fmaf(S[r][c], ka, pk[c]);
+                pq[c] = fmaf(S[r][c], qa, pq[c]);
             }
         }
 #pragma unroll
@@ -203,8 +215,9 @@ __global__ void __launch_bounds__(kThreads, 2) recurrent_kernel(RecurrentParams 
 #pragma unroll
         for (int r = 0; r < R; ++r) {
             const float w = bt * kr[r];
+            const float ad = CW ? ar[r] : a;
 #pragma unroll
-            for (int c = 0; c < C; ++c) S[r][c] = fmaf(a, S[r][c], w * e[c]);
+            for (int c = 0; c < C; ++c) S[r][c] = fmaf(ad, S[r][c], w * e[c]);
         }
     }
 
@@ -222,10 +235,17 @@ cudaError_t launch_dims(const RecurrentParams &p, gdn_dtype dtype, cudaStream_t 
     if (pairs == 0) return cudaSuccess;
     if (pairs > 0x7fffffffLL) return cudaErrorInvalidValue;
     const dim3 grid(static_cast<unsigned>(pairs));
-    if (dtype == GDN_BF16)
-        recurrent_kernel<DK, DV, __nv_bfloat16><<<grid, kThreads, 0, stream>>>(p);
-    else
-        recurrent_kernel<DK, DV, float><<<grid, kThreads, 0, stream>>>(p);
+    if (p.alpha_cw) {
+        if (dtype == GDN_BF16)
+            recurrent_kernel<DK, DV, __nv_bfloat16, true><<<grid, kThreads, 0, stream>>>(p);
+        else
+            recurrent_kernel<DK, DV, float, true><<<grid, kThreads, 0, stream>>>(p);
+    } else {
+        if (dtype == GDN_BF16)
+            recurrent_kernel<DK, DV, __nv_bfloat16, false><<<grid, kThreads, 0, stream>>>(p);
+        else
+            recurrent_kernel<DK, DV, float, false><<<grid, kThreads, 0, stream>>>(p);
+    }
     return cudaGetLastError();
 }
 

@@ -28,7 +28,7 @@ ALGO_NAMES = {ALGO_AUTO: "auto", ALGO_CHUNKED: "chunked", ALGO_SEQUENTIAL: "sequ
 EXPORTS = ("gdn_status_string", "gdn_prefill_workspace_bytes", "gdn_prefill", "gdn_prefill_ex",
            "gdn_decode_step", "gdn_read_device_status", "gdn_device_supported", "gdn_abi_version",
            "gdn_prefill_noalloc", "gdn_layer_prologue", "gdn_layer_epilogue", "gdn_prefill_host_workspace_bytes",
-           "gdn_prefill_host")
+           "gdn_prefill_host", "gdn_prefill_cw", "gdn_decode_step_cw")
 NOALLOC_SCRATCH_BYTES = 256 + 8 * 1024 * 1024
 
 
@@ -97,6 +97,10 @@ def lib() -> ctypes.CDLL:
             L.gdn_prefill_host_workspace_bytes.argtypes = [sp, ctypes.c_int64]
             L.gdn_prefill_host.restype = ctypes.c_int
             L.gdn_prefill_host.argtypes = [sp, ctypes.c_int64, vp, vp, vp, fp, fp, fp, vp, fp, vp, c_size, vp]
+            L.gdn_prefill_cw.restype = ctypes.c_int
+            L.gdn_prefill_cw.argtypes = [sp, vp, vp, vp, fp, fp, fp, vp, fp, vp]
+            L.gdn_decode_step_cw.restype = ctypes.c_int
+            L.gdn_decode_step_cw.argtypes = [sp, vp, vp, vp, fp, fp, fp, vp, vp]
             L.gdn_device_supported.restype = ctypes.c_int
             L.gdn_abi_version.restype = ctypes.c_int
             _lib = L
@@ -298,6 +302,32 @@ def prefill_host(q, k, v, alpha, beta, S0=None, *, y=None, S_T=None, workspace=N
     # the work is still in flight: keep the device workspace from being reused before it ends
     workspace.record_stream(stream)
     return y, S_T
+
+
+def prefill_cw(q, k, v, alpha, beta, S0=None, *, y=None, S_T=None, stream=None):
+    """Run gdn_prefill_cw (channel-wise decay, alpha [B,T,Hv,dk] fp32); returns (y, S_T)."""
+    _require(dict(q=q, k=k, v=v, alpha=alpha, beta=beta, S0=S0, y=y, S_T=S_T))
+    shape = shape_of(q, v)
+    if y is None:
+        y = torch.empty_like(v)
+    if S_T is None:
+        S_T = torch.empty((shape.B, shape.Hv, shape.dk, shape.dv), dtype=torch.float32, device=v.device)
+    rc = lib().gdn_prefill_cw(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(beta), _ptr(S0),
+                              _ptr(y), _ptr(S_T), _stream(stream))
+    _check(rc, "gdn_prefill_cw")
+    return y, S_T
+
+
+def decode_step_cw(q, k, v, alpha, beta, S, *, y=None, stream=None):
+    """Run gdn_decode_step_cw (channel-wise decay, alpha [B,1,Hv,dk]): S updated in place; returns y."""
+    _require(dict(q=q, k=k, v=v, alpha=alpha, beta=beta, S=S, y=y))
+    shape = shape_of(q, v)
+    if y is None:
+        y = torch.empty_like(v)
+    rc = lib().gdn_decode_step_cw(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(beta), _ptr(S),
+                                  _ptr(y), _stream(stream))
+    _check(rc, "gdn_decode_step_cw")
+    return y
 
 
 def prefill_launches(shape: GdnShape, algorithm=ALGO_AUTO, segments=0) -> int:

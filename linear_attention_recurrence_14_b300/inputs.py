@@ -173,3 +173,10 @@ def make_layer_inputs(B, T, Hqk, Hv, d, kconv=4, decay_scale=0.05, seed=0, devic
     norm_w = 0.1 * _randn((d,), seed, "norm_w", device)
     return LayerInputs(xq, xk, xv, wq.contiguous(), wk.contiguous(), wv.contiguous(), a_raw, b_raw, A.contiguous(),
                        b_alpha.contiguous(), st(Hqk, "state_q"), st(Hqk, "state_k"), st(Hv, "state_v"), y, z, norm_w)
+
+
+def make_channelwise_alpha(B, T, Hv, dk, decay_scale=0.05, seed=0, device="cpu") -> torch.Tensor:
+    """Channel-wise decay gate [B, T, Hv, dk] fp32: alpha = exp(-softplus(a) * decay_scale),
+    a ~ N(0, 1) drawn independently per key channel (the per-channel form of the scalar recipe)."""
+    a = _randn((B, T, Hv, dk), seed, "a_cw", device)
+    return torch.exp(-torch.nn.functional.softplus(a) * decay_scale).contiguous()

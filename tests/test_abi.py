@@ -185,3 +185,18 @@ def test_host_prefill_workspace_and_arguments(L):
     assert call(ws_bytes=n - 1) == E["GDN_ERR_WORKSPACE"]
     assert call(ws=BASE + 512 * MB + 16) == E["GDN_ERR_ALIGNMENT"]
     assert call(q=None) == E["GDN_ERR_INVALID_ARG"]
+
+
+def test_channelwise_entry_points_reject_bad_arguments(L):
+    E = {v: k for k, v in gdn.STATUS_NAMES.items()}
+    vp = lambda x: None if x is None else ctypes.c_void_p(x)  # noqa: E731
+    s = ctypes.byref(shape(T=8))
+    args = [vp(BASE), vp(BASE + MB), vp(BASE + 2 * MB), vp(BASE + 3 * MB), vp(BASE + 4 * MB)]
+    assert L.gdn_prefill_cw(None, *args, None, vp(BASE + 5 * MB), vp(BASE + 6 * MB), None) == E["GDN_ERR_INVALID_ARG"]
+    assert L.gdn_prefill_cw(s, None, *args[1:], None, vp(BASE + 5 * MB), vp(BASE + 6 * MB), None) == \
+        E["GDN_ERR_INVALID_ARG"]
+    assert L.gdn_prefill_cw(s, *args[:3], vp(BASE + 3 * MB + 4), args[4], None, vp(BASE + 5 * MB),
+                            vp(BASE + 6 * MB), None) == E["GDN_ERR_ALIGNMENT"]
+    assert L.gdn_prefill_cw(s, *args, None, vp(BASE), vp(BASE + 6 * MB), None) == E["GDN_ERR_ALIASING"]
+    # decode: T must be 1
+    assert L.gdn_decode_step_cw(s, *args, vp(BASE + 6 * MB), vp(BASE + 5 * MB), None) == E["GDN_ERR_INVALID_ARG"]
