@@ -9,7 +9,9 @@ The same run also times the decode workload (B=256 sequences, 32 value heads
 over 16 key heads, d=128, 128 single-token steps, fp32 state updated in place)
 and reports it under "decode", and the layer steps around the recurrence
 (fused prologue: short convolution, SiLU, L2Norm, gates; fused epilogue:
-sigmoid gate times zero-centred RMSNorm) on the prefill shape under "layer".
+sigmoid gate times zero-centred RMSNorm) on the prefill shape under "layer",
+and the backward pass (gradients of the recurrence) on the training-shape
+workload (B=2, H=16, T=4096, d=128, bf16) under "backward".
 
 Printed: one JSON line (rank 0).  `value` is prefill tokens/s summed over all
 ranks; `e2e` is the same metric through the C ABI with host buffers
@@ -365,6 +367,12 @@ def run_ours(args, ws, rank, local):
         layer = time_layer(args, peaks, seed, dev, ws, local)
         torch.cuda.empty_cache()
 
+    # ------------------------------------------------------------- backward
+    bwd = None
+    if not args.no_backward:
+        bwd = time_backward(args, peaks, seed, dev, ws, local)
+        torch.cuda.empty_cache()
+
     # ------------------------------------------------------------- cpu baseline
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -382,7 +390,7 @@ def run_ours(args, ws, rank, local):
                    "algorithm": gdn.ALGO_NAMES[args.algorithm], "segments": args.segments,
                    "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"},
         "roofline": roofline, "clocks": clocks, "e2e": e2e, "cpu_baseline": cpu, "gpu_launches": gpu_launches,
-        "decode": dec, "decode_channelwise": dec_cw, "layer": layer, "check": check,
+        "decode": dec, "decode_channelwise": dec_cw, "layer": layer, "backward": bwd, "check": check,
     }
     if rank == 0:
         print(json.dumps(line), flush=True)
@@ -499,6 +507,71 @@ def time_layer(args, peaks, seed, dev, ws, local):
     return res
 
 
+def backward_flops_per_token_head(d: int) -> float:
+    """Useful fp32 FLOPs of one backward token per (token, value head): eight d x d passes of two FLOPs
+    per element -- S dy, G += q dy^T, G^T k, G e, S~ de, G -= k de^T, and the forward rebuild's S^T k
+    and state update."""
+    return 8 * 2.0 * d * d
+
+
+def fp32_alu_peak_tflops(sm_mhz: float, sms: int = 148) -> float:
+    """FP32 FMA peak: 128 FMA lanes per SM, 2 FLOPs per FMA, at the given SM clock."""
+    return sms * 128 * 2 * sm_mhz * 1e6 / 1e12
+
+
+def time_backward(args, peaks, seed, dev, ws, local):
+    """gdn_backward on the training-shape workload (B=2, H=16, T=4096, d=128, bf16 inputs, dy ~ N(0,1),
+    dS_T ~ N(0,1)); median of 10 calls, each the per-slab kernel plus its reduction."""
+    import torch
+
+    from linear_attention_recurrence_14_b300 import gdn
+    from linear_attention_recurrence_14_b300.inputs import make_backward_grads, workload_inputs
+
+    x = workload_inputs("train", seed=seed, device=dev)
+    B, T, Hqk, d = x.q.shape
+    Hv = x.v.shape[2]
+    g = make_backward_grads(B, T, Hv, d, "bf16", ds_std=1.0, seed=seed, device=dev)
+    shape = gdn.shape_of(x.q, x.v)
+    wsb = gdn.new_backward_workspace(shape, dev)
+    out = gdn.backward(x.q, x.k, x.v, x.alpha, x.beta, x.S0, g.dy, g.dS_T, workspace=wsb)
+    stream = torch.cuda.current_stream()
+
+    def fn():
+        gdn.backward(x.q, x.k, x.v, x.alpha, x.beta, x.S0, g.dy, g.dS_T, out=out, workspace=wsb)
+
+    for _ in range(max(3, args.warmup)):
+        fn()
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(10)]
+    barrier(ws)
+    with ClockSampler(local) as clk:
+        for a, b in evs:
+            a.record(stream)
+            fn()
+            b.record(stream)
+        torch.cuda.synchronize()
+    ms = max_over_ranks(statistics.median(a.elapsed_time(b) for a, b in evs), ws, dev)
+    clocks = clk.summary()
+    flops = backward_flops_per_token_head(d) * B * T * Hv
+    tflops = flops / (ms * 1e-3) / 1e12
+    mhz = clocks.get("sm_max_mhz") or 2032
+    peak = fp32_alu_peak_tflops(mhz)
+    # algorithmic HBM bytes: inputs (q, k, v, dy bf16; alpha, beta fp32), outputs (dq, dk, dv fp32,
+    # dlog_alpha, dbeta fp32), dS_T in and dS0 out
+    nbytes = (2 * B * T * Hqk * d * 2 + 2 * B * T * Hv * d * 2 + 2 * B * T * Hv * 4
+              + 2 * B * T * Hqk * d * 4 + B * T * Hv * d * 4 + 2 * B * T * Hv * 4 + 2 * B * Hv * d * d * 4)
+    return {"ms": ms, "tokens_per_s": B * T * ws / (ms * 1e-3),
+            "roofline": {"bound": "alu", "achieved": tflops, "peak": peak, "unit": "TFLOP/s", "frac": tflops / peak,
+                         "traffic": None, "flops_per_call": flops,
+                         "peak_source": "fp32 FMA: 148 SMs x 128 lanes x 2 FLOPs at the sampled max SM clock",
+                         "hbm": {"bytes_per_call": nbytes, "achieved_gbs": nbytes / (ms * 1e-3) / 1e9,
+                                 "frac": nbytes / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"]}},
+            "gpu_launches": gdn.backward_launches(shape),
+            "config": "training-shape backward: B=2, H=16, T=4096, d=128, bf16 q/k/v/dy, fp32 gates, state and "
+                      "gradients; median of 10 calls",
+            "l2": "inputs and workspace larger than L2 (1.3 GB), no flush", "clocks": clocks}
+
+
 def time_decode(args, peaks, seed, dev, ws, local, channelwise=False):
     """128 decode steps of the decode workload, state in place; returns steps/s and its HBM roofline.
     channelwise: the per-key-channel decay gate (gdn_decode_step_cw, alpha [B, 1, Hv, dk])."""
@@ -582,6 +655,7 @@ def main(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-layer", action="store_true")
+    ap.add_argument("--no-backward", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-check", dest="check", action="store_false")
     args = ap.parse_args(argv)

@@ -240,6 +240,47 @@ gdn_status gdn_prefill_host(const gdn_shape *shape, int64_t tokens_per_piece,
                             const float *alpha, const float *beta, const float *S0,
                             void *y, float *S_T, void *ws, size_t ws_bytes, void *stream);
 
+/*
+ * Backward (gradients of the recurrence, for training).  Given the forward
+ * inputs and the upstream gradients dy = dL/dy [B, T, Hv, dv] (dtype of the
+ * shape) and dS_T = dL/dS_T [B, Hv, dk, dv] fp32 (NULL = zero), returns, for
+ * the loss L whose gradients those are:
+ *   dq, dk       [B, T, Hqk, dk] fp32  (summed over the value heads that share
+ *                                       the query/key head)
+ *   dv           [B, T, Hv, dv]  fp32
+ *   dlog_alpha   [B, T, Hv]      fp32  the gradient with respect to log alpha_t,
+ *                                       i.e. alpha_t * dL/dalpha_t (divide by
+ *                                       alpha_t for dL/dalpha_t)
+ *   dbeta        [B, T, Hv]      fp32
+ *   dS0          [B, Hv, dk, dv] fp32  (NULL = not returned; may be the very
+ *                                       buffer of dS_T, read before written)
+ * This is the chain rule applied to the four lines of the recurrence above,
+ * from t = T down to 1 (same section of the reading notes).  The decay
+ * gradient is given in log space because the layer forms alpha as an
+ * exponential of its gate pre-activation; the kernel obtains it from a scalar
+ * recursion that never divides by alpha, so it stays finite as alpha -> 0.
+ *
+ * Scalar decay only.  All arithmetic is fp32 on CUDA cores, token by token:
+ * the kernel recomputes the forward states from checkpoints taken every 8
+ * tokens.  ws: device memory of gdn_backward_workspace_bytes(shape) bytes,
+ * 256-byte aligned (no initial contents needed): the checkpoints
+ * (B*Hv*ceil(T/8)*dk*dv fp32) and per-slab partial sums (2*B*T*Hv*(dv/32)*dk
+ * fp32 and a little more).  Inputs q, k, v, dy, S0, dS_T and the outputs dq,
+ * dk, dv, dS0 16-byte aligned; alpha, beta, dlog_alpha, dbeta 4-byte aligned.
+ * No output may overlap an input, another output or the workspace (except dS0
+ * == dS_T).  T == 0 writes dS0 = dS_T (or zeros).  Results are deterministic
+ * (fixed summation order).  Layouts, ownership and errors otherwise as
+ * gdn_prefill.
+ */
+size_t gdn_backward_workspace_bytes(const gdn_shape *shape);
+
+gdn_status gdn_backward(const gdn_shape *shape,
+                        const void *q, const void *k, const void *v,
+                        const float *alpha, const float *beta, const float *S0,
+                        const void *dy, const float *dS_T,
+                        float *dq, float *dk, float *dv, float *dlog_alpha, float *dbeta, float *dS0,
+                        void *ws, size_t ws_bytes, void *stream);
+
 /* 1 if the current CUDA device can run these kernels (compute capability 10.3). */
 int gdn_device_supported(void);
 

@@ -290,6 +290,95 @@ gdn_status gdn_decode_step_cw(const gdn_shape *shape, const void *q, const void 
     return recurrence_cw(shape, true, q, k, v, alpha, beta, S_inout, S_inout, y, stream);
 }
 
+// Backward: the workspace holds the slab-state checkpoints and per-slab partial sums.
+static gdn_status backward_workspace(const gdn_shape *shape, size_t *bytes) {
+    int64_t n_qk, n_v, n_gate, n_state;
+    gdn_status st = check_shape(shape, &n_qk, &n_v, &n_gate, &n_state);
+    if (st != GDN_OK) return st;
+    const int64_t nc = (shape->T + gdn::kBackwardCheckpointTokens - 1) / gdn::kBackwardCheckpointTokens;
+    int64_t ck = 0;
+    if (!mul_ok(n_state, nc, &ck) || ck > (INT64_MAX >> 4) || n_v > (INT64_MAX >> 6)) return GDN_ERR_INVALID_ARG;
+    *bytes = gdn::backward_workspace_layout(shape->B, shape->T, shape->Hv, shape->dk, nullptr, nullptr, nullptr,
+                                            nullptr);
+    return GDN_OK;
+}
+
+size_t gdn_backward_workspace_bytes(const gdn_shape *shape) {
+    size_t bytes = 0;
+    return backward_workspace(shape, &bytes) == GDN_OK ? bytes : 0;
+}
+
+gdn_status gdn_backward(const gdn_shape *shape, const void *q, const void *k, const void *v, const float *alpha,
+                        const float *beta, const float *S0, const void *dy, const float *dS_T, float *dq, float *dk,
+                        float *dv, float *dlog_alpha, float *dbeta, float *dS0, void *ws, size_t ws_bytes,
+                        void *stream_) {
+    int64_t n_qk, n_v, n_gate, n_state;
+    gdn_status st = check_shape(shape, &n_qk, &n_v, &n_gate, &n_state);
+    if (st != GDN_OK) return st;
+    size_t need = 0;
+    st = backward_workspace(shape, &need);
+    if (st != GDN_OK) return st;
+    const gdn_shape &s = *shape;
+    const bool has_tokens = s.B * s.T > 0;
+    if (has_tokens && (!q || !k || !v || !alpha || !beta || !dy || !dq || !dk || !dv || !dlog_alpha || !dbeta))
+        return GDN_ERR_INVALID_ARG;
+    if (need > 0 && !ws) return GDN_ERR_WORKSPACE;
+    if (ws_bytes < need) return GDN_ERR_WORKSPACE;
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(dy, 16) || !aligned(S0, 16) ||
+        !aligned(dS_T, 16) || !aligned(dq, 16) || !aligned(dk, 16) || !aligned(dv, 16) || !aligned(dS0, 16) ||
+        !aligned(alpha, 4) || !aligned(beta, 4) || !aligned(dlog_alpha, 4) || !aligned(dbeta, 4) ||
+        !aligned(ws, 256))
+        return GDN_ERR_ALIGNMENT;
+
+    const size_t esz = s.dtype == GDN_BF16 ? 2 : 4;
+    const Range rq{q, static_cast<size_t>(n_qk) * esz}, rk{k, static_cast<size_t>(n_qk) * esz};
+    const Range rv{v, static_cast<size_t>(n_v) * esz}, rdy{dy, static_cast<size_t>(n_v) * esz};
+    const Range ra{alpha, static_cast<size_t>(n_gate) * 4}, rb{beta, static_cast<size_t>(n_gate) * 4};
+    const Range rs0{S0, static_cast<size_t>(n_state) * 4}, rdst{dS_T, static_cast<size_t>(n_state) * 4};
+    const Range rdq{dq, static_cast<size_t>(n_qk) * 4}, rdk{dk, static_cast<size_t>(n_qk) * 4};
+    const Range rdv{dv, static_cast<size_t>(n_v) * 4}, rdg{dlog_alpha, static_cast<size_t>(n_gate) * 4};
+    const Range rdb{dbeta, static_cast<size_t>(n_gate) * 4}, rds0{dS0, static_cast<size_t>(n_state) * 4};
+    const Range rws{ws, need};
+    const Range outs[] = {rdq, rdk, rdv, rdg, rdb, rds0, rws};
+    const Range ins[] = {rq, rk, rv, rdy, ra, rb, rs0, rdst};
+    // dS0 may be the very buffer of dS_T (each element is read before it is written).
+    const bool ds_in_place = dS0 && dS0 == dS_T;
+    for (int o = 0; o < 7; ++o) {
+        for (const Range &in : ins)
+            if (!(ds_in_place && o == 5 && in.p == rdst.p) && overlap(outs[o], in)) return GDN_ERR_ALIASING;
+        for (int o2 = o + 1; o2 < 7; ++o2)
+            if (overlap(outs[o], outs[o2])) return GDN_ERR_ALIASING;
+    }
+
+    int num_sms = 0;
+    st = check_device(&num_sms);
+    if (st != GDN_OK) return st;
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+    if (s.B * s.Hv == 0) return GDN_OK;
+    if (!has_tokens) {
+        // No tokens: dS0 = dS_T; there is nothing else to return.
+        if (dS0 && !ds_in_place) {
+            if (dS_T) return from_cuda(cudaMemcpyAsync(dS0, dS_T, rds0.n, cudaMemcpyDeviceToDevice, stream));
+            return from_cuda(cudaMemsetAsync(dS0, 0, rds0.n, stream));
+        }
+        return GDN_OK;
+    }
+
+    size_t o_dq = 0, o_dk = 0, o_b = 0, o_g = 0;
+    gdn::backward_workspace_layout(s.B, s.T, s.Hv, s.dk, &o_dq, &o_dk, &o_b, &o_g);
+    char *w = static_cast<char *>(ws);
+    gdn::BackwardParams p{};
+    p.B = s.B; p.T = s.T; p.Hqk = s.Hqk; p.Hv = s.Hv; p.group = s.Hv / s.Hqk;
+    p.q = q; p.k = k; p.v = v; p.dy = dy; p.alpha = alpha; p.beta = beta; p.S0 = S0; p.dS_T = dS_T;
+    p.dq = dq; p.dk = dk; p.dv = dv; p.dlog_alpha = dlog_alpha; p.dbeta = dbeta; p.dS0 = dS0;
+    p.ckpt = reinterpret_cast<float *>(w);
+    p.part_dq = reinterpret_cast<float *>(w + o_dq);
+    p.part_dk = reinterpret_cast<float *>(w + o_dk);
+    p.part_dbeta = reinterpret_cast<float *>(w + o_b);
+    p.part_dlog_alpha = reinterpret_cast<float *>(w + o_g);
+    return from_cuda(gdn::launch_backward(p, s.dk, static_cast<gdn_dtype>(s.dtype), stream, num_sms));
+}
+
 gdn_status gdn_read_device_status(void *ws, void *stream_) {
     if (!ws) return GDN_ERR_INVALID_ARG;
     cudaStream_t stream = static_cast<cudaStream_t>(stream_);

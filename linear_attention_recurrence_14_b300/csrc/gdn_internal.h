@@ -51,4 +51,30 @@ int plan_segments(int64_t pairs, int64_t nchunks, int num_sms, int requested);
 // Chunked tensor-core prefill (bf16).  Builds the TMA descriptors and launches.
 cudaError_t launch_chunked(const ChunkedParams &p, cudaStream_t stream, int num_sms);
 
+// Tokens between two checkpoints of the backward pass (and its chunk length).
+constexpr int kBackwardCheckpointTokens = 8;
+
+struct BackwardParams {
+    int64_t B, T;
+    int Hqk, Hv, group;
+    const void *q, *k, *v, *dy;          // dtype of the shape
+    const float *alpha, *beta;           // [B, T, Hv]
+    const float *S0, *dS_T;              // [B, Hv, d, d] or nullptr (zero)
+    float *dq, *dk;                      // [B, T, Hqk, d]
+    float *dv;                           // [B, T, Hv, d]
+    float *dlog_alpha, *dbeta;           // [B, T, Hv]
+    float *dS0;                          // [B, Hv, d, d] or nullptr (not returned)
+    float *ckpt;                         // workspace: slab states every few tokens
+    float *part_dq, *part_dk;            // workspace: [B, T, Hv, d / 32, d] per-slab partial sums
+    float *part_dbeta, *part_dlog_alpha; // workspace: [B, T, Hv, d / 32]
+};
+
+// Bytes of backward workspace for this shape (d = dk = dv) and the offsets of
+// its partial-sum regions (the checkpoints start at offset 0).
+size_t backward_workspace_layout(int64_t B, int64_t T, int Hv, int d, size_t *off_part_dq, size_t *off_part_dk,
+                                 size_t *off_part_b, size_t *off_part_g);
+
+// Backward of the recurrence: the per-slab kernel, then the reduction of its partial sums.
+cudaError_t launch_backward(const BackwardParams &p, int d, gdn_dtype dtype, cudaStream_t stream, int num_sms);
+
 }  // namespace gdn

@@ -28,7 +28,8 @@ ALGO_NAMES = {ALGO_AUTO: "auto", ALGO_CHUNKED: "chunked", ALGO_SEQUENTIAL: "sequ
 EXPORTS = ("gdn_status_string", "gdn_prefill_workspace_bytes", "gdn_prefill", "gdn_prefill_ex",
            "gdn_decode_step", "gdn_read_device_status", "gdn_device_supported", "gdn_abi_version",
            "gdn_prefill_noalloc", "gdn_layer_prologue", "gdn_layer_epilogue", "gdn_prefill_host_workspace_bytes",
-           "gdn_prefill_host", "gdn_prefill_cw", "gdn_decode_step_cw")
+           "gdn_prefill_host", "gdn_prefill_cw", "gdn_decode_step_cw", "gdn_backward_workspace_bytes",
+           "gdn_backward")
 NOALLOC_SCRATCH_BYTES = 256 + 8 * 1024 * 1024
 
 
@@ -101,6 +102,10 @@ def lib() -> ctypes.CDLL:
             L.gdn_prefill_cw.argtypes = [sp, vp, vp, vp, fp, fp, fp, vp, fp, vp]
             L.gdn_decode_step_cw.restype = ctypes.c_int
             L.gdn_decode_step_cw.argtypes = [sp, vp, vp, vp, fp, fp, fp, vp, vp]
+            L.gdn_backward_workspace_bytes.restype = c_size
+            L.gdn_backward_workspace_bytes.argtypes = [sp]
+            L.gdn_backward.restype = ctypes.c_int
+            L.gdn_backward.argtypes = [sp, vp, vp, vp, fp, fp, fp, vp, fp, fp, fp, fp, fp, fp, fp, vp, c_size, vp]
             L.gdn_device_supported.restype = ctypes.c_int
             L.gdn_abi_version.restype = ctypes.c_int
             _lib = L
@@ -328,6 +333,55 @@ def decode_step_cw(q, k, v, alpha, beta, S, *, y=None, stream=None):
                                   _ptr(y), _stream(stream))
     _check(rc, "gdn_decode_step_cw")
     return y
+
+
+def backward_workspace_bytes(shape: GdnShape) -> int:
+    return int(lib().gdn_backward_workspace_bytes(ctypes.byref(shape)))
+
+
+def new_backward_workspace(shape: GdnShape, device) -> torch.Tensor:
+    """A workspace of the size gdn_backward needs (uint8; its contents need no initialisation)."""
+    return torch.empty(max(backward_workspace_bytes(shape), 256), dtype=torch.uint8, device=device)
+
+
+def backward(q, k, v, alpha, beta, S0, dy, dS_T=None, *, dS0=True, out=None, workspace=None, stream=None):
+    """Run gdn_backward; returns a dict with dq, dk [B,T,Hqk,d], dv [B,T,Hv,d], dlog_alpha, dbeta [B,T,Hv]
+    (fp32) and dS0 [B,Hv,d,d] (fp32; None when dS0=False).
+
+    dlog_alpha is alpha * dL/dalpha.  dy has the dtype of q, k, v; dS_T (fp32) may be None (zero).
+    out: optional dict of preallocated outputs with the same keys.
+    """
+    _require(dict(q=q, k=k, v=v, alpha=alpha, beta=beta, S0=S0, dy=dy, dS_T=dS_T, workspace=workspace))
+    if dy.dtype != q.dtype:
+        raise TypeError(f"dy is {dy.dtype}, expected {q.dtype}")
+    shape = shape_of(q, v)
+    B, T, Hqk, d = q.shape
+    Hv = v.shape[2]
+    dev = v.device
+    o = dict(out or {})
+    f32 = dict(dtype=torch.float32, device=dev)
+    o.setdefault("dq", torch.empty((B, T, Hqk, d), **f32))
+    o.setdefault("dk", torch.empty((B, T, Hqk, d), **f32))
+    o.setdefault("dv", torch.empty((B, T, Hv, d), **f32))
+    o.setdefault("dlog_alpha", torch.empty((B, T, Hv), **f32))
+    o.setdefault("dbeta", torch.empty((B, T, Hv), **f32))
+    if dS0 and "dS0" not in o:
+        o["dS0"] = torch.empty((B, Hv, d, d), **f32)
+    o.setdefault("dS0", None)
+    _require(o)
+    if workspace is None:
+        workspace = new_backward_workspace(shape, dev)
+    rc = lib().gdn_backward(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(beta), _ptr(S0),
+                            _ptr(dy), _ptr(dS_T), _ptr(o["dq"]), _ptr(o["dk"]), _ptr(o["dv"]), _ptr(o["dlog_alpha"]),
+                            _ptr(o["dbeta"]), _ptr(o["dS0"]), _ptr(workspace),
+                            workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(rc, "gdn_backward")
+    return o
+
+
+def backward_launches(shape: GdnShape) -> int:
+    """Kernel launches one gdn_backward call enqueues (the per-slab kernel and the reduction)."""
+    return 2 if shape.B * shape.T * shape.Hv > 0 else 0
 
 
 def prefill_launches(shape: GdnShape, algorithm=ALGO_AUTO, segments=0) -> int:

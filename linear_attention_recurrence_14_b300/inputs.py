@@ -18,6 +18,10 @@ Recipe (the five workloads below):
   * S0 ~ N(0, s0_std^2) fp32, or absent (zero state) when s0_std == 0.
 Every tensor has its own generator seeded from (seed, tensor name), drawn in
 the fixed order a, b, q, k, v, S0.
+
+Upstream gradients for the backward pass (no workload of the sources fixes
+them): dy ~ N(0, 1) in the workload dtype and dS_T ~ N(0, ds_std^2) fp32
+(absent when ds_std == 0), each from its own named generator.
 """
 from __future__ import annotations
 
@@ -88,6 +92,18 @@ def make_prefill_inputs(B, T, Hqk, Hv, d, dtype="bf16", decay_scale=0.05, s0_std
     if s0_std > 0:
         S0 = _randn((B, Hv, dk, dv), seed, "S0", device) * s0_std
     return PrefillInputs(q.contiguous(), k.contiguous(), v.contiguous(), alpha.contiguous(), beta.contiguous(), S0)
+
+
+@dataclass
+class BackwardGrads:
+    dy: torch.Tensor             # [B, T, Hv, dv], workload dtype
+    dS_T: torch.Tensor | None    # [B, Hv, dk, dv] fp32
+
+
+def make_backward_grads(B, T, Hv, d, dtype="bf16", ds_std=1.0, seed=0, device="cpu") -> BackwardGrads:
+    dy = _randn((B, T, Hv, d), seed, "dy", device).to(torch_dtype(dtype)).contiguous()
+    dS_T = _randn((B, Hv, d, d), seed, "dS_T", device) * ds_std if ds_std > 0 else None
+    return BackwardGrads(dy, dS_T)
 
 
 @dataclass

@@ -200,3 +200,45 @@ def test_channelwise_entry_points_reject_bad_arguments(L):
     assert L.gdn_prefill_cw(s, *args, None, vp(BASE), vp(BASE + 6 * MB), None) == E["GDN_ERR_ALIASING"]
     # decode: T must be 1
     assert L.gdn_decode_step_cw(s, *args, vp(BASE + 6 * MB), vp(BASE + 5 * MB), None) == E["GDN_ERR_INVALID_ARG"]
+
+
+def test_backward_workspace_and_arguments(L):
+    E = {v: k for k, v in gdn.STATUS_NAMES.items()}
+    r = lambda n: (n + 255) // 256 * 256  # noqa: E731
+    # checkpoints every 8 tokens, per-slab (32 value columns) partial sums of dq, dk, dbeta, dlog(alpha)
+    for B, T, Hv, d in [(2, 1000, 4, 128), (1, 7, 2, 64), (3, 8, 2, 128)]:
+        s = shape(B=B, T=T, Hqk=2, Hv=Hv, d=d)
+        nc, ns = (T + 7) // 8, d // 32
+        want = r(B * Hv * nc * d * d * 4) + 2 * r(B * T * Hv * ns * d * 4) + 2 * r(B * T * Hv * ns * 4)
+        assert gdn.backward_workspace_bytes(s) == want
+    assert gdn.backward_workspace_bytes(shape(T=0)) == 0
+    assert gdn.backward_workspace_bytes(shape(Hqk=3, Hv=4)) == 0
+    s = shape(B=1, T=64, Hqk=2, Hv=4, d=128)
+    n = gdn.backward_workspace_bytes(s)
+    vp = lambda x: None if x is None else ctypes.c_void_p(x)  # noqa: E731
+    # inputs at BASE + i*64MB (i = 0..7), outputs at BASE + (8 + i)*64MB, workspace at BASE + 16*64MB
+    ins = dict(q=0, k=1, v=2, alpha=3, beta=4, S0=5, dy=6, dS_T=7)
+    outs = dict(dq=8, dk=9, dv=10, dlog_alpha=11, dbeta=12, dS0=13)
+    at = {**{k_: BASE + i * 64 * MB for k_, i in ins.items()}, **{k_: BASE + i * 64 * MB for k_, i in outs.items()}}
+
+    def call(shp=s, ws=BASE + 16 * 64 * MB, ws_bytes=n, **over):
+        a = {**at, **over}
+        return L.gdn_backward(ctypes.byref(shp), *(vp(a[k_]) for k_ in ins), *(vp(a[k_]) for k_ in outs),
+                              vp(ws), ws_bytes, None)
+    assert call(shp=shape(Hqk=3, Hv=4)) == E["GDN_ERR_INVALID_ARG"]
+    assert call(shp=gdn.GdnShape(1, 64, 1, 1, 96, 96, 1)) == E["GDN_ERR_UNSUPPORTED"]
+    for name in ("q", "dy", "dq", "dlog_alpha", "dbeta"):
+        assert call(**{name: None}) == E["GDN_ERR_INVALID_ARG"], name
+    assert call(ws=None) == E["GDN_ERR_WORKSPACE"]
+    assert call(ws_bytes=n - 1) == E["GDN_ERR_WORKSPACE"]
+    assert call(ws=BASE + 16 * 64 * MB + 16) == E["GDN_ERR_ALIGNMENT"]
+    assert call(dy=at["dy"] + 8) == E["GDN_ERR_ALIGNMENT"]
+    assert call(dv=at["dv"] + 4) == E["GDN_ERR_ALIGNMENT"]
+    assert call(dbeta=at["dbeta"] + 2) == E["GDN_ERR_ALIGNMENT"]
+    # an output on an input, two outputs on each other, the workspace on an output
+    assert call(dq=at["q"]) == E["GDN_ERR_ALIASING"]
+    assert call(dk=at["dq"] + 256) == E["GDN_ERR_ALIASING"]
+    assert call(ws=at["dv"]) == E["GDN_ERR_ALIASING"]
+    assert call(dS0=at["S0"]) == E["GDN_ERR_ALIASING"]
+    # dS0 may be the very buffer of dS_T: past the host checks (no GPU here, so a CUDA/device status)
+    assert call(dS0=at["dS_T"]) not in (E["GDN_ERR_ALIASING"], E["GDN_ERR_INVALID_ARG"], E["GDN_ERR_ALIGNMENT"])

@@ -102,3 +102,14 @@ def test_backward_pins_reject_mutation(name, tmp_path):
     spec.loader.exec_module(mod)
     with pytest.raises(AssertionError):
         test_backward_matches_central_differences((1, 4, 1, 2, 3, 3), bw=mod)
+
+
+def test_backward_linearity_identities():
+    # (y, S_T) is linear in (v, S0) jointly and y is linear in q, so for L = <dy, y> + <dS_T, S_T>:
+    # <dv, v> + <dS0, S0> = L and <dq, q> = <dy, y>.
+    inp, dy, dST = _inputs(2, 11, 1, 2, 5, 4, seed=21)
+    g = BW.recurrence_grad(inp["q"], inp["k"], inp["v"], inp["alpha"], inp["beta"], inp["S0"], dy, dST)
+    ydy = np.sum(g["y"] * dy)
+    L = ydy + np.sum(g["S_T"] * dST)
+    assert abs(np.sum(g["dv"] * inp["v"]) + np.sum(g["dS0"] * inp["S0"]) - L) < 1e-11 * max(1, abs(L))
+    assert abs(np.sum(g["dq"] * inp["q"]) - ydy) < 1e-11 * max(1, abs(ydy))
