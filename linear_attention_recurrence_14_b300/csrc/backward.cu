@@ -61,7 +61,7 @@ struct BwLayout {
     static constexpr int R = D / kBwWarps;
     static constexpr size_t kScratch = size_t(kCk) * D * kSlab * 4;   // chunk states [kCk][R/4][256] float4
     static constexpr size_t kE = size_t(kCk) * kBwThreads * 4;        // e_t per thread [kCk][256]
-    static constexpr size_t kYdy = 64;                                // y.dy per token (slab part)
+    static constexpr size_t kYdy = size_t(3) * kCk * kSlab * 4;      // per-lane y.dy, g.e, g.v per token
     static constexpr size_t kRed = (2 * 2 * kBwWarps * kSlab + 2 * kBwWarps + kBwWarps) * 4;
     static constexpr size_t kStK = size_t(kCk) * D * sizeof(TIn);      // staged q or k rows
     static constexpr size_t kStV = size_t(kCk) * kSlab * sizeof(TIn);  // staged v or dy slab
@@ -205,6 +205,12 @@ __device__ __forceinline__ float lane_reduce_scatter(float (&x)[N], int lane) {
     return r;
 }
 
+// Sum of the 8 warps' partials of one column (a fixed tree order).
+__device__ __forceinline__ float sum_warps(const float *p) {
+    return ((p[0] + p[kSlab]) + (p[2 * kSlab] + p[3 * kSlab])) +
+           ((p[4 * kSlab] + p[5 * kSlab]) + (p[6 * kSlab] + p[7 * kSlab]));
+}
+
 template <int D, typename TIn>
 __global__ void __launch_bounds__(kBwThreads, 1) backward_kernel(BackwardParams p) {
     using L = BwLayout<D, TIn>;
@@ -212,11 +218,14 @@ __global__ void __launch_bounds__(kBwThreads, 1) backward_kernel(BackwardParams 
     constexpr int R4 = R / 4;        // float4 groups of a thread's state column
     constexpr int NS = D / kSlab;    // slabs per head
     static_assert(R % 4 == 0 && NS * kSlab == D, "unsupported head dim");
+    static_assert(kCk == 8, "the per-chunk tail scans 8 tokens");
 
     extern __shared__ __align__(128) unsigned char smem[];
     float4 *scratch = reinterpret_cast<float4 *>(smem + L::kOffScratch);
     float *ebuf = reinterpret_cast<float *>(smem + L::kOffE);
-    float *ydyb = reinterpret_cast<float *>(smem + L::kOffYdy);
+    float *ydl = reinterpret_cast<float *>(smem + L::kOffYdy);     // [kCk][32] y.dy per lane (warp 0)
+    float *gel = ydl + kCk * kSlab;                                 // [kCk][32] g.e per lane
+    float *gvl = gel + kCk * kSlab;                                 // [kCk][32] g.v per lane
     float *red_k = reinterpret_cast<float *>(smem + L::kOffRed);   // [2][8][32]
     float *red_q = red_k + 2 * kBwWarps * kSlab;                    // [2][8][32]
     float *red_kq = red_q + 2 * kBwWarps * kSlab;                   // [2][8]
@@ -235,6 +244,8 @@ __global__ void __launch_bounds__(kBwThreads, 1) backward_kernel(BackwardParams 
     const int64_t T = p.T;
     const int64_t NC = (T + kCk - 1) / kCk;
     float4 *ck = reinterpret_cast<float4 *>(p.ckpt) + cta * NC * R4 * kBwThreads;   // [NC][R4][256]
+    const int64_t row_base = (b * T * p.Hv + h) * NS + slab;   // partial-sum row of token 0
+    const int64_t row_step = int64_t(p.Hv) * NS;                // rows between consecutive tokens
 
     float S[R], G[R], Sn[R];
 #pragma unroll
@@ -243,8 +254,8 @@ __global__ void __launch_bounds__(kBwThreads, 1) backward_kernel(BackwardParams 
         G[r] = 0.f;
         Sn[r] = 0.f;
     }
-    double Dacc = 0.0;   // D_t of this slab (thread 0 only)
-    int64_t it = 0;      // token counter: parity of the cross-warp buffers
+    double Dc = 0.0;   // D at the first token of the chunk last walked (every lane of warp 0)
+    int64_t it = 0;    // token counter: parity of the cross-warp buffers
 
     stage_chunk<D, TIn>(p, stage, b, h, hk, slab, 0, static_cast<int>(T < kCk ? T : kCk));
 
@@ -281,14 +292,15 @@ __global__ void __launch_bounds__(kBwThreads, 1) backward_kernel(BackwardParams 
                 lds_row<TIn, R>(st.k + s * D + r0, kr);
                 const float vj = to_f(st.v[s * kSlab + lane]);
                 const float a = st.a[s], bt = st.b[s];
-                float pk = 0.f;
+                float pk0 = 0.f, pk1 = 0.f;
 #pragma unroll
-                for (int r = 0; r < R; ++r) pk = fmaf(S[r], kr[r], pk);
-                red_k[(buf * kBwWarps + warp) * kSlab + lane] = pk;
+                for (int r = 0; r < R; r += 2) {
+                    pk0 = fmaf(S[r], kr[r], pk0);
+                    pk1 = fmaf(S[r + 1], kr[r + 1], pk1);
+                }
+                red_k[(buf * kBwWarps + warp) * kSlab + lane] = pk0 + pk1;
                 __syncthreads();
-                float rk = 0.f;
-#pragma unroll
-                for (int w = 0; w < kBwWarps; ++w) rk += red_k[(buf * kBwWarps + w) * kSlab + lane];
+                const float rk = sum_warps(red_k + buf * kBwWarps * kSlab + lane);
                 const float e = vj - a * rk;
 #pragma unroll
                 for (int r = 0; r < R; ++r) S[r] = fmaf(a, S[r], bt * kr[r] * e);
@@ -307,8 +319,9 @@ __global__ void __launch_bounds__(kBwThreads, 1) backward_kernel(BackwardParams 
             part = warp_sum(part);
             if (lane == 0) red_d[warp] = part;
             __syncthreads();
-            if (tid == 0) {
-                for (int w = 0; w < kBwWarps; ++w) Dacc += static_cast<double>(red_d[w]);
+            if (warp == 0) {
+#pragma unroll
+                for (int w = 0; w < kBwWarps; ++w) Dc += static_cast<double>(red_d[w]);
             }
         }
 #pragma unroll
@@ -321,7 +334,7 @@ __global__ void __launch_bounds__(kBwThreads, 1) backward_kernel(BackwardParams 
             }
         }
 
-        // Rebuild the chunk: the state entering each token, e_t, y_t . dy_t.
+        // Rebuild the chunk: the state entering each token, e_t, and y_t . dy_t per lane.
         for (int s = 0; s < n; ++s) {
             const int buf = static_cast<int>(it++ & 1);
 #pragma unroll
@@ -333,36 +346,40 @@ __global__ void __launch_bounds__(kBwThreads, 1) backward_kernel(BackwardParams 
             const float vj = to_f(st.v[s * kSlab + lane]);
             const float dyj = to_f(st.dy[s * kSlab + lane]);
             const float a = st.a[s], bt = st.b[s];
-            float pk = 0.f, pq = 0.f, kq = 0.f;
+            float pk0 = 0.f, pk1 = 0.f, pq0 = 0.f, pq1 = 0.f, kq0 = 0.f, kq1 = 0.f;
 #pragma unroll
-            for (int r = 0; r < R; ++r) {
-                pk = fmaf(S[r], kr[r], pk);
-                pq = fmaf(S[r], qr[r], pq);
-                kq = fmaf(kr[r], qr[r], kq);
+            for (int r = 0; r < R; r += 2) {
+                pk0 = fmaf(S[r], kr[r], pk0);
+                pk1 = fmaf(S[r + 1], kr[r + 1], pk1);
+                pq0 = fmaf(S[r], qr[r], pq0);
+                pq1 = fmaf(S[r + 1], qr[r + 1], pq1);
+                kq0 = fmaf(kr[r], qr[r], kq0);
+                kq1 = fmaf(kr[r + 1], qr[r + 1], kq1);
             }
-            red_k[(buf * kBwWarps + warp) * kSlab + lane] = pk;
-            red_q[(buf * kBwWarps + warp) * kSlab + lane] = pq;
-            if (lane == 0) red_kq[buf * kBwWarps + warp] = kq;
+            red_k[(buf * kBwWarps + warp) * kSlab + lane] = pk0 + pk1;
+            red_q[(buf * kBwWarps + warp) * kSlab + lane] = pq0 + pq1;
+            if (lane == 0) red_kq[buf * kBwWarps + warp] = kq0 + kq1;
             __syncthreads();
-            float rk = 0.f, rq = 0.f, kqa = 0.f;
-#pragma unroll
-            for (int w = 0; w < kBwWarps; ++w) {
-                rk += red_k[(buf * kBwWarps + w) * kSlab + lane];
-                rq += red_q[(buf * kBwWarps + w) * kSlab + lane];
-                kqa += red_kq[buf * kBwWarps + w];
-            }
+            const float rk = sum_warps(red_k + buf * kBwWarps * kSlab + lane);
+            const float rq = sum_warps(red_q + buf * kBwWarps * kSlab + lane);
+            const float *kqp = red_kq + buf * kBwWarps;
+            const float kqa = ((kqp[0] + kqp[1]) + (kqp[2] + kqp[3])) + ((kqp[4] + kqp[5]) + (kqp[6] + kqp[7]));
             const float e = vj - a * rk;
             const float y = a * rq + bt * kqa * e;
             ebuf[s * kBwThreads + tid] = e;
-            if (warp == 0) {
-                const float yd = warp_sum(y * dyj);
-                if (lane == 0) ydyb[s] = yd;
-            }
+            if (warp == 0) ydl[s * kSlab + lane] = y * dyj;
 #pragma unroll
             for (int r = 0; r < R; ++r) S[r] = fmaf(a, S[r], bt * kr[r] * e);
         }
 
-        // Walk the chunk backwards.
+        // Walk the chunk backwards.  The column sums of token s (the dk and dq
+        // partials) are finished during token s-1, before its barrier.
+        float xp[2 * R];
+#pragma unroll
+        for (int r = 0; r < 2 * R; ++r) xp[r] = 0.f;
+        int64_t pend = -1;   // partial-sum row of the token whose column sums are pending
+        const bool writer = lane % (32 / (2 * R)) == 0;
+        const int idx = lane / (32 / (2 * R));
         for (int s = n - 1; s >= 0; --s) {
             const int buf = static_cast<int>(it++ & 1);
             const int64_t t = t0 + s;
@@ -380,48 +397,83 @@ __global__ void __launch_bounds__(kBwThreads, 1) backward_kernel(BackwardParams 
             const float dyj = to_f(st.dy[s * kSlab + lane]);
             const float a = st.a[s], bt = st.b[s];
 
-            float pg = 0.f;
+            float pg0 = 0.f, pg1 = 0.f;
 #pragma unroll
-            for (int r = 0; r < R; ++r) {
+            for (int r = 0; r < R; r += 2) {
                 G[r] = fmaf(qr[r], dyj, G[r]);
-                pg = fmaf(G[r], kr[r], pg);
+                G[r + 1] = fmaf(qr[r + 1], dyj, G[r + 1]);
+                pg0 = fmaf(G[r], kr[r], pg0);
+                pg1 = fmaf(G[r + 1], kr[r + 1], pg1);
             }
-            red_k[(buf * kBwWarps + warp) * kSlab + lane] = pg;
+            red_k[(buf * kBwWarps + warp) * kSlab + lane] = pg0 + pg1;
+            {
+                const float xs = lane_reduce_scatter<2 * R>(xp, lane);
+                if (pend >= 0 && writer) {
+                    if (idx < R)
+                        p.part_dk[pend * D + r0 + idx] = xs;
+                    else
+                        p.part_dq[pend * D + r0 + idx - R] = xs;
+                }
+            }
             __syncthreads();
-            float gk = 0.f;
-#pragma unroll
-            for (int w = 0; w < kBwWarps; ++w) gk += red_k[(buf * kBwWarps + w) * kSlab + lane];
+            const float gk = sum_warps(red_k + buf * kBwWarps * kSlab + lane);
             const float de = bt * gk;
 
             // Column-local parts of dk_t (rows 0..R-1) and dq_t (rows R..2R-1).
-            float x[2 * R];
 #pragma unroll
             for (int r = 0; r < R; ++r) {
-                x[r] = bt * G[r] * e - a * Sp[r] * de;
-                x[R + r] = fmaf(a, Sp[r], bt * kr[r] * e) * dyj;
+                xp[r] = bt * G[r] * e - a * Sp[r] * de;
+                xp[R + r] = fmaf(a, Sp[r], bt * kr[r] * e) * dyj;
             }
-            const float xs = lane_reduce_scatter<2 * R>(x, lane);
-            const int idx = lane / (32 / (2 * R));
-            const int64_t prow = ((b * T + t) * p.Hv + h) * NS + slab;
-            if (lane % (32 / (2 * R)) == 0) {
-                if (idx < R)
-                    p.part_dk[prow * D + r0 + idx] = xs;
-                else
-                    p.part_dq[prow * D + r0 + idx - R] = xs;
-            }
+            pend = row_base + t * row_step;
 #pragma unroll
             for (int r = 0; r < R; ++r) G[r] = a * fmaf(-kr[r], de, G[r]);
 
             if (warp == 0) {
                 p.dv[((b * T + t) * p.Hv + h) * D + col] = de;
-                const float ge = warp_sum(gk * e);
-                const float gv = warp_sum(gk * vj);
-                if (lane == 0) {
-                    Dacc += static_cast<double>(ydyb[s]) - static_cast<double>(bt) * static_cast<double>(gv);
-                    p.part_dlog_alpha[prow] = static_cast<float>(Dacc);
-                    p.part_dbeta[prow] = ge;
-                }
+                gel[s * kSlab + lane] = gk * e;
+                gvl[s * kSlab + lane] = gk * vj;
             }
+        }
+        {
+            const float xs = lane_reduce_scatter<2 * R>(xp, lane);
+            if (writer) {
+                if (idx < R)
+                    p.part_dk[pend * D + r0 + idx] = xs;
+                else
+                    p.part_dq[pend * D + r0 + idx - R] = xs;
+            }
+        }
+
+        // Per-chunk tail (warp 0): lane sums of y.dy, g.e, g.v for the n
+        // tokens, then dbeta and D_t = D_{t+1} + y.dy - beta g.v by a suffix
+        // scan over the chunk, carried in fp64 from chunk to chunk.
+        if (warp == 0) {
+            float z[32];
+#pragma unroll
+            for (int s = 0; s < kCk; ++s) {
+                z[s] = s < n ? ydl[s * kSlab + lane] : 0.f;
+                z[kCk + s] = s < n ? gel[s * kSlab + lane] : 0.f;
+                z[2 * kCk + s] = s < n ? gvl[s * kSlab + lane] : 0.f;
+                z[3 * kCk + s] = 0.f;
+            }
+            const float tot = lane_reduce_scatter<32>(z, lane);   // lane l: quantity l / 8 of token l % 8
+            const int s = lane & (kCk - 1);
+            const float ge = __shfl_sync(0xffffffffu, tot, s + kCk);
+            const float gv = __shfl_sync(0xffffffffu, tot, s + 2 * kCk);
+            float c = (lane < kCk && s < n) ? tot - st.b[s] * gv : 0.f;
+#pragma unroll
+            for (int o = 1; o < kCk; o <<= 1) {
+                const float u = __shfl_down_sync(0xffffffffu, c, o);
+                if (s + o < kCk) c += u;
+            }
+            const double Dt = Dc + static_cast<double>(c);
+            if (lane < n) {
+                const int64_t row = row_base + (t0 + lane) * row_step;
+                p.part_dlog_alpha[row] = static_cast<float>(Dt);
+                p.part_dbeta[row] = ge;
+            }
+            Dc = __shfl_sync(0xffffffffu, Dt, 0);
         }
     }
 
