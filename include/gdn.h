@@ -260,7 +260,8 @@ gdn_status gdn_prefill_host(const gdn_shape *shape, int64_t tokens_per_piece,
  * exponential of its gate pre-activation; the kernel obtains it from a scalar
  * recursion that never divides by alpha, so it stays finite as alpha -> 0.
  *
- * Scalar decay only.  All arithmetic is fp32 on CUDA cores, token by token:
+ * Scalar decay only; Hv * dk <= 2^24 (else GDN_ERR_UNSUPPORTED).  All
+ * arithmetic is fp32 on CUDA cores, token by token:
  * the kernel recomputes the forward states from checkpoints taken every 8
  * tokens.  ws: device memory of gdn_backward_workspace_bytes(shape) bytes,
  * 256-byte aligned (no initial contents needed): the checkpoints

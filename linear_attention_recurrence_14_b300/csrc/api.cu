@@ -315,6 +315,8 @@ gdn_status gdn_backward(const gdn_shape *shape, const void *q, const void *k, co
     int64_t n_qk, n_v, n_gate, n_state;
     gdn_status st = check_shape(shape, &n_qk, &n_v, &n_gate, &n_state);
     if (st != GDN_OK) return st;
+    // Per-token offsets inside the kernel are 32-bit: bound the head count times the head dim.
+    if (static_cast<int64_t>(shape->Hv) * shape->dk > (int64_t(1) << 24)) return GDN_ERR_UNSUPPORTED;
     size_t need = 0;
     st = backward_workspace(shape, &need);
     if (st != GDN_OK) return st;

@@ -71,7 +71,10 @@ struct BwLayout {
     static constexpr size_t kOffYdy = kOffE + kE;
     static constexpr size_t kOffRed = kOffYdy + kYdy;
     static constexpr size_t kOffStage = kOffRed + ((kRed + 127) / 128) * 128;
-    static constexpr size_t kTotal = kOffStage + 2 * kStBuf;
+    static constexpr bool kConvert = sizeof(TIn) != 4;                  // bf16 rows converted once per chunk
+    static constexpr size_t kKQf = kConvert ? size_t(2) * kCk * D * 4 : 0;
+    static constexpr size_t kOffKQf = kOffStage + 2 * kStBuf;
+    static constexpr size_t kTotal = kOffKQf + kKQf;
     static_assert(kStK % 16 == 0 && kStV % 16 == 0 && kStBuf % 16 == 0, "staging regions must stay 16-byte aligned");
     static_assert(kTotal <= 227 * 1024, "shared memory over the per-CTA limit");
 };
@@ -255,7 +258,7 @@ __global__ void __launch_bounds__(kBwThreads, 1) backward_kernel(BackwardParams 
         Sn[r] = 0.f;
     }
     double Dc = 0.0;   // D at the first token of the chunk last walked (every lane of warp 0)
-    int64_t it = 0;    // token counter: parity of the cross-warp buffers
+    unsigned it = 0;   // token counter: parity of the cross-warp buffers
 
     stage_chunk<D, TIn>(p, stage, b, h, hk, slab, 0, static_cast<int>(T < kCk ? T : kCk));
 
@@ -275,6 +278,30 @@ __global__ void __launch_bounds__(kBwThreads, 1) backward_kernel(BackwardParams 
             stage_chunk<D, TIn>(p, stage + ((ni < NC ? ni : ni - 1) & 1) * L::kStBuf, b, h, hk, slab, nci * kCk, nn);
         }
         const Staged<D, TIn> st(stage + bi * L::kStBuf);
+        // The chunk's k and q rows as fp32 ([2][kCk][D]: k then q).
+        const float *kf;
+        if constexpr (L::kConvert) {
+            float *dst = reinterpret_cast<float *>(smem + L::kOffKQf);
+            constexpr int kPieces = 2 * kCk * D / 8;   // 8 bf16 (16 bytes) per piece; k and q are adjacent
+            for (int pc = tid; pc < kPieces; pc += kBwThreads) {
+                const uint4 raw = reinterpret_cast<const uint4 *>(st.k)[pc];
+                const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+                float f[8];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const __nv_bfloat162 pr = *reinterpret_cast<const __nv_bfloat162 *>(&w[j]);
+                    f[2 * j] = __low2float(pr);
+                    f[2 * j + 1] = __high2float(pr);
+                }
+                reinterpret_cast<float4 *>(dst)[2 * pc] = make_float4(f[0], f[1], f[2], f[3]);
+                reinterpret_cast<float4 *>(dst)[2 * pc + 1] = make_float4(f[4], f[5], f[6], f[7]);
+            }
+            __syncthreads();
+            kf = dst;
+        } else {
+            kf = reinterpret_cast<const float *>(st.k);
+        }
+        const float *qf = kf + kCk * D;
 
         if (fwd) {
             // Forward sweep: checkpoint the state entering this chunk.
@@ -289,7 +316,7 @@ __global__ void __launch_bounds__(kBwThreads, 1) backward_kernel(BackwardParams 
             for (int s = 0; s < n; ++s) {
                 const int buf = static_cast<int>(it++ & 1);
                 float kr[R];
-                lds_row<TIn, R>(st.k + s * D + r0, kr);
+                lds_row<float, R>(kf + s * D + r0, kr);
                 const float vj = to_f(st.v[s * kSlab + lane]);
                 const float a = st.a[s], bt = st.b[s];
                 float pk0 = 0.f, pk1 = 0.f;
@@ -301,9 +328,9 @@ __global__ void __launch_bounds__(kBwThreads, 1) backward_kernel(BackwardParams 
                 red_k[(buf * kBwWarps + warp) * kSlab + lane] = pk0 + pk1;
                 __syncthreads();
                 const float rk = sum_warps(red_k + buf * kBwWarps * kSlab + lane);
-                const float e = vj - a * rk;
+                const float be = bt * (vj - a * rk);
 #pragma unroll
-                for (int r = 0; r < R; ++r) S[r] = fmaf(a, S[r], bt * kr[r] * e);
+                for (int r = 0; r < R; ++r) S[r] = fmaf(a, S[r], kr[r] * be);
             }
             continue;
         }
@@ -341,8 +368,8 @@ __global__ void __launch_bounds__(kBwThreads, 1) backward_kernel(BackwardParams 
             for (int j = 0; j < R4; ++j)
                 scratch[(s * R4 + j) * kBwThreads + tid] = make_float4(S[4 * j], S[4 * j + 1], S[4 * j + 2], S[4 * j + 3]);
             float kr[R], qr[R];
-            lds_row<TIn, R>(st.k + s * D + r0, kr);
-            lds_row<TIn, R>(st.q + s * D + r0, qr);
+            lds_row<float, R>(kf + s * D + r0, kr);
+            lds_row<float, R>(qf + s * D + r0, qr);
             const float vj = to_f(st.v[s * kSlab + lane]);
             const float dyj = to_f(st.dy[s * kSlab + lane]);
             const float a = st.a[s], bt = st.b[s];
@@ -365,11 +392,12 @@ __global__ void __launch_bounds__(kBwThreads, 1) backward_kernel(BackwardParams 
             const float *kqp = red_kq + buf * kBwWarps;
             const float kqa = ((kqp[0] + kqp[1]) + (kqp[2] + kqp[3])) + ((kqp[4] + kqp[5]) + (kqp[6] + kqp[7]));
             const float e = vj - a * rk;
-            const float y = a * rq + bt * kqa * e;
+            const float be = bt * e;
+            const float y = fmaf(kqa, be, a * rq);
             ebuf[s * kBwThreads + tid] = e;
             if (warp == 0) ydl[s * kSlab + lane] = y * dyj;
 #pragma unroll
-            for (int r = 0; r < R; ++r) S[r] = fmaf(a, S[r], bt * kr[r] * e);
+            for (int r = 0; r < R; ++r) S[r] = fmaf(a, S[r], kr[r] * be);
         }
 
         // Walk the chunk backwards.  The column sums of token s (the dk and dq
@@ -377,12 +405,18 @@ __global__ void __launch_bounds__(kBwThreads, 1) backward_kernel(BackwardParams 
         float xp[2 * R];
 #pragma unroll
         for (int r = 0; r < 2 * R; ++r) xp[r] = 0.f;
-        int64_t pend = -1;   // partial-sum row of the token whose column sums are pending
+        int pend = -1;   // token (within the chunk) whose column sums are pending
         const bool writer = lane % (32 / (2 * R)) == 0;
         const int idx = lane / (32 / (2 * R));
+        // Partial-sum rows and dv of the chunk's first token; consecutive tokens are row_step rows apart.
+        const int64_t prow0 = row_base + t0 * row_step;
+        const int row_stride = static_cast<int>(row_step) * D;
+        float *const pdk0 = p.part_dk + prow0 * D + r0;
+        float *const pdq0 = p.part_dq + prow0 * D + r0;
+        float *const dv0 = p.dv + ((b * T + t0) * p.Hv + h) * D + col;
+        const int dv_stride = p.Hv * D;
         for (int s = n - 1; s >= 0; --s) {
             const int buf = static_cast<int>(it++ & 1);
-            const int64_t t = t0 + s;
             float Sp[R];
 #pragma unroll
             for (int j = 0; j < R4; ++j) {
@@ -391,8 +425,8 @@ __global__ void __launch_bounds__(kBwThreads, 1) backward_kernel(BackwardParams 
             }
             const float e = ebuf[s * kBwThreads + tid];
             float kr[R], qr[R];
-            lds_row<TIn, R>(st.k + s * D + r0, kr);
-            lds_row<TIn, R>(st.q + s * D + r0, qr);
+            lds_row<float, R>(kf + s * D + r0, kr);
+            lds_row<float, R>(qf + s * D + r0, qr);
             const float vj = to_f(st.v[s * kSlab + lane]);
             const float dyj = to_f(st.dy[s * kSlab + lane]);
             const float a = st.a[s], bt = st.b[s];
@@ -410,27 +444,29 @@ __global__ void __launch_bounds__(kBwThreads, 1) backward_kernel(BackwardParams 
                 const float xs = lane_reduce_scatter<2 * R>(xp, lane);
                 if (pend >= 0 && writer) {
                     if (idx < R)
-                        p.part_dk[pend * D + r0 + idx] = xs;
+                        pdk0[pend * row_stride + idx] = xs;
                     else
-                        p.part_dq[pend * D + r0 + idx - R] = xs;
+                        pdq0[pend * row_stride + idx - R] = xs;
                 }
             }
             __syncthreads();
             const float gk = sum_warps(red_k + buf * kBwWarps * kSlab + lane);
             const float de = bt * gk;
 
-            // Column-local parts of dk_t (rows 0..R-1) and dq_t (rows R..2R-1).
+            // Column-local parts of dk_t = b G e - a S_{t-1} de (rows 0..R-1) and of
+            // dq_t = S_t dy = (a S_{t-1} + b k e^T) dy (rows R..2R-1).
+            const float be = bt * e, ade = a * de, ady = a * dyj, bedy = be * dyj;
 #pragma unroll
             for (int r = 0; r < R; ++r) {
-                xp[r] = bt * G[r] * e - a * Sp[r] * de;
-                xp[R + r] = fmaf(a, Sp[r], bt * kr[r] * e) * dyj;
+                xp[r] = fmaf(G[r], be, -(Sp[r] * ade));
+                xp[R + r] = fmaf(Sp[r], ady, kr[r] * bedy);
             }
-            pend = row_base + t * row_step;
+            pend = s;
 #pragma unroll
             for (int r = 0; r < R; ++r) G[r] = a * fmaf(-kr[r], de, G[r]);
 
             if (warp == 0) {
-                p.dv[((b * T + t) * p.Hv + h) * D + col] = de;
+                dv0[s * dv_stride] = de;
                 gel[s * kSlab + lane] = gk * e;
                 gvl[s * kSlab + lane] = gk * vj;
             }
@@ -439,9 +475,9 @@ __global__ void __launch_bounds__(kBwThreads, 1) backward_kernel(BackwardParams 
             const float xs = lane_reduce_scatter<2 * R>(xp, lane);
             if (writer) {
                 if (idx < R)
-                    p.part_dk[pend * D + r0 + idx] = xs;
+                    pdk0[pend * row_stride + idx] = xs;
                 else
-                    p.part_dq[pend * D + r0 + idx - R] = xs;
+                    pdq0[pend * row_stride + idx - R] = xs;
             }
         }
 

@@ -227,6 +227,7 @@ def test_backward_workspace_and_arguments(L):
                               vp(ws), ws_bytes, None)
     assert call(shp=shape(Hqk=3, Hv=4)) == E["GDN_ERR_INVALID_ARG"]
     assert call(shp=gdn.GdnShape(1, 64, 1, 1, 96, 96, 1)) == E["GDN_ERR_UNSUPPORTED"]
+    assert call(shp=gdn.GdnShape(1, 64, 1, 1 << 18, 128, 128, 1)) == E["GDN_ERR_UNSUPPORTED"]   # Hv * dk > 2^24
     for name in ("q", "dy", "dq", "dlog_alpha", "dbeta"):
         assert call(**{name: None}) == E["GDN_ERR_INVALID_ARG"], name
     assert call(ws=None) == E["GDN_ERR_WORKSPACE"]
