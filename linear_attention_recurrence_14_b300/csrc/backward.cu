@@ -19,16 +19,18 @@
 //   D_t = y_t . dy_t - b_t k_t^T G_t v_t + D_{t+1},   D_{T+1} = <dS_T, S_T>,
 //
 // so no term of it needs the state S_{t-1} of the reverse step.  Only dk_t
-// (through S~ de) does.
+// (through S~ de) does.  The kernel evaluates the recursion once per chunk of
+// kCk tokens (a suffix scan over the chunk), carrying D in fp64 from chunk to
+// chunk.
 //
 // Work split: the columns of S (the value dimension) evolve independently in
 // the forward map, so one CTA owns one (batch, value head, slab of 32 value
 // columns); lane l of each warp owns column l of the slab and warp w owns key
 // rows [w R, (w+1) R).  Sums over key rows (S^T k, G^T k) are per-thread sums
-// plus a cross-warp sum in shared memory; sums over value columns (dk, dq) are
-// partial over the slab and are finished by the reduce kernel, which also sums
-// the value heads that share a query/key head.  All its sums run in a fixed
-// order, so results are deterministic.
+// plus a cross-warp sum in shared memory; sums over value columns (dk, dq) run
+// as a lane reduce-scatter, are partial over the slab and are finished by the
+// reduce kernel, which also sums the value heads that share a query/key head.
+// All its sums run in a fixed order, so results are deterministic.
 //
 // States in reverse order: a forward sweep over the whole sequence stores the
 // slab's state every kCk tokens (HBM checkpoints).  Then, for each chunk of
