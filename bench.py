@@ -19,7 +19,9 @@ ranks; `e2e` is the same metric through the C ABI with host buffers
 host copies of y and S_T inside the timed region, overlapped with the
 prefill piece by piece); `roofline` is the prefill kernel against measured
 HBM bandwidth (its binding roof) with its tensor-core fraction beside it;
-`cpu_baseline` is the fp64 oracle timed on a bounded sample on the host cores.
+`cpu_baseline` is the fp64 oracle timed on a bounded sample on the host cores;
+the decode, layer and backward sections carry their own oracle timing the same
+way (a bounded sample, its rate scaled to the section's workload).
 
 `--impl reference` times the fp64 oracle instead (the only reference
 implementation there is), on a bounded sample of the same workload.
@@ -221,6 +223,89 @@ def time_oracle_prefill(w: dict, seed: int, target_s: float, device="cpu"):
     sample = (f"oracle fp64 on B={w['B']} x T={Ts} tokens x {w['Hv']} value heads of the "
               f"{PREFILL_WORKLOAD} workload ({dt:.2f} s)")
     return tokens / dt, sample, threads, dt
+
+
+def _oracle_timed(fn, what: str) -> dict:
+    """A bounded oracle timing beside a GPU section; a failure is reported in the line, not raised."""
+    try:
+        return fn()
+    except Exception as exc:  # noqa: BLE001
+        return {"kind": "oracle", "error": f"{what}: {type(exc).__name__}: {exc}"}
+
+
+def _grow(n: int, dt: float, target_s: float, cap: int) -> int:
+    return min(cap, int(n * min(16.0, max(2.0, target_s / max(dt, 1e-3)))))
+
+
+def time_oracle_decode(w: dict, seed: int, target_s: float, sample_b: int = 16) -> dict:
+    """The fp64 oracle stepping sample_b of the decode workload's sequences (all heads, state carried);
+    the rate is scaled to the whole batch: steps/s of the full workload."""
+    import oracle
+    from linear_attention_recurrence_14_b300.inputs import make_decode_inputs
+
+    oracle.build()
+    threads = os.cpu_count() or 1
+    Bs = min(sample_b, w["B"])
+    steps = 1
+    while True:
+        d = make_decode_inputs(Bs, steps, w["Hqk"], w["Hv"], w["d"], w["dtype"], w["decay_scale"], w["s0_std"],
+                               seed=seed, device="cpu")
+        S = d.S0
+        t0 = time.perf_counter()
+        for i in range(steps):
+            _, S = oracle.recurrence(d.q[i], d.k[i], d.v[i], d.alpha[i], d.beta[i], S, threads=threads)
+        dt = time.perf_counter() - t0
+        if dt >= 0.5 * target_s or steps >= w["steps"]:
+            break
+        steps = _grow(steps, dt, target_s, w["steps"])
+    return {"value": steps / dt * Bs / w["B"], "unit": "steps/s", "cores": threads, "kind": "oracle",
+            "sample": f"oracle fp64, {steps} decode step(s) of {Bs} of the {w['B']} sequences x {w['Hv']} value "
+                      f"heads ({dt:.2f} s); rate scaled to the whole batch"}
+
+
+def time_oracle_layer(B, Hqk, Hv, d, K, T_full, seed: int, target_s: float) -> dict:
+    """The numpy fp64 layer steps (prologue, then epilogue) on the first T_s tokens: tokens/s of both."""
+    import oracle.layer as olayer
+    from linear_attention_recurrence_14_b300.inputs import make_layer_inputs
+
+    Ts = 64
+    while True:
+        x = make_layer_inputs(B, Ts, Hqk, Hv, d, K, seed=seed, device="cpu", with_state=True)
+        t0 = time.perf_counter()
+        olayer.prologue(x.xq, x.xk, x.xv, x.wq, x.wk, x.wv, x.a_raw, x.b_raw, x.A, x.b_alpha,
+                        x.state_q, x.state_k, x.state_v)
+        olayer.epilogue(x.y, x.z, x.norm_w, 1e-6)
+        dt = time.perf_counter() - t0
+        if dt >= 0.5 * target_s or Ts >= T_full:
+            break
+        Ts = _grow(Ts, dt, target_s, T_full)
+    return {"value": B * Ts / dt, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"numpy fp64 prologue + epilogue on B={B} x T={Ts} tokens, all heads ({dt:.2f} s)"}
+
+
+def time_oracle_backward(x, g, seed: int, target_s: float) -> dict:
+    """The fp64 backward oracle on one (batch, value head) over the first T_s tokens; the rate is scaled
+    to all value heads (the oracle runs heads one after another): tokens/s of the whole shape."""
+    import oracle.backward as obw
+
+    B, T, Hqk, d = x.q.shape
+    Hv = x.v.shape[2]
+    group = Hv // Hqk
+    cpu = lambda t, n: t[:1, :n].detach().cpu()  # noqa: E731
+    Ts = 64
+    while True:
+        q, k = cpu(x.q, Ts)[:, :, :1], cpu(x.k, Ts)[:, :, :1]
+        v, a, b, dy = (cpu(t, Ts)[:, :, :1] for t in (x.v, x.alpha, x.beta, g.dy))
+        dST = None if g.dS_T is None else g.dS_T[:1, :1].detach().cpu()
+        t0 = time.perf_counter()
+        obw.recurrence_grad(q, k, v, a, b, None, dy, dST)
+        dt = time.perf_counter() - t0
+        if dt >= 0.5 * target_s or Ts >= T:
+            break
+        Ts = _grow(Ts, dt, target_s, T)
+    return {"value": Ts / (dt * Hv), "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"numpy fp64 backward of one value head (of {Hv}, group {group}) over T={Ts} tokens "
+                      f"({dt:.2f} s); rate divided by the head count"}
 
 
 # ----------------------------------------------------------------- main arms
@@ -501,6 +586,9 @@ def time_layer(args, peaks, seed, dev, ws, local):
                                       "frac": gbs / peaks["hbm_gbs"], "traffic": None, "bytes_per_launch": nbytes,
                                       "peak_source": peaks["source"]},
                          "gpu_launches": 1}
+    if local == 0 and not args.no_cpu_baseline:
+        res["cpu_baseline"] = _oracle_timed(
+            lambda: time_oracle_layer(B, Hqk, Hv, d, K, T, seed, args.oracle_seconds), "layer oracle")
     res["config"] = "B=1, T=65536, Hqk=16, Hv=32, d=128, 4 taps, bf16 features, fp32 gates; median of 20 launches"
     res["l2"] = "inputs larger than L2 (2.2 GB prologue, 1.6 GB epilogue), no flush"
     res["clocks"] = clk.summary()
@@ -569,7 +657,9 @@ def time_backward(args, peaks, seed, dev, ws, local):
             "gpu_launches": gdn.backward_launches(shape),
             "config": "training-shape backward: B=2, H=16, T=4096, d=128, bf16 q/k/v/dy, fp32 gates, state and "
                       "gradients; median of 10 calls",
-            "l2": "inputs and workspace larger than L2 (1.3 GB), no flush", "clocks": clocks}
+            "l2": "inputs and workspace larger than L2 (1.3 GB), no flush", "clocks": clocks,
+            "cpu_baseline": _oracle_timed(lambda: time_oracle_backward(x, g, seed, args.oracle_seconds),
+                                          "backward oracle") if local == 0 and not args.no_cpu_baseline else None}
 
 
 def time_decode(args, peaks, seed, dev, ws, local, channelwise=False):
@@ -636,6 +726,8 @@ def time_decode(args, peaks, seed, dev, ws, local, channelwise=False):
                      "launch_ms": kern_s * 1e3, "peak_source": peaks["source"]},
         "clocks": clk.summary(),
         "l2": "state 512 MiB > L2, no flush",
+        "cpu_baseline": _oracle_timed(lambda: time_oracle_decode(w, seed, args.oracle_seconds), "decode oracle")
+        if local == 0 and not args.no_cpu_baseline and not channelwise else None,
     }
 
 
@@ -650,6 +742,8 @@ def main(argv=None):
     ap.add_argument("--segments", type=int, default=0, help="0 = chosen by the library")
     ap.add_argument("--decode-steps", type=int, default=128)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--oracle-seconds", type=float, default=3.0,
+                    help="target time of each oracle sample beside the decode, layer and backward sections")
     ap.add_argument("--traffic", type=float, default=None, help="ncu dram bytes per prefill launch, if measured")
     ap.add_argument("--decode-traffic", type=float, default=None, help="ncu dram bytes per decode launch")
     ap.add_argument("--no-e2e", action="store_true")
