@@ -185,13 +185,17 @@ def prefill(q, k, v, alpha, beta, S0=None, *, y=None, S_T=None, workspace=None, 
         y = torch.empty_like(v)
     if S_T is None:
         S_T = torch.empty((shape.B, shape.Hv, shape.dk, shape.dv), dtype=torch.float32, device=v.device)
-    if workspace is None:
+    own_ws = workspace is None
+    if own_ws:
         workspace = new_workspace(shape, v.device)
     opts = GdnPrefillOptions(segments, log_eps, max_warmup_chunks, algorithm, test_stall_chunk)
     rc = lib().gdn_prefill_ex(ctypes.byref(shape), ctypes.byref(opts), _ptr(q), _ptr(k), _ptr(v), _ptr(alpha),
                               _ptr(beta), _ptr(S0), _ptr(y), _ptr(S_T), _ptr(workspace),
                               workspace.numel() * workspace.element_size(), _stream(stream))
     _check(rc, "gdn_prefill_ex")
+    if own_ws and stream is not None:
+        # allocated on the current stream but used on `stream`: keep it from being reused too early
+        workspace.record_stream(stream)
     return y, S_T
 
 
@@ -369,13 +373,16 @@ def backward(q, k, v, alpha, beta, S0, dy, dS_T=None, *, dS0=True, out=None, wor
         o["dS0"] = torch.empty((B, Hv, d, d), **f32)
     o.setdefault("dS0", None)
     _require(o)
-    if workspace is None:
+    own_ws = workspace is None
+    if own_ws:
         workspace = new_backward_workspace(shape, dev)
     rc = lib().gdn_backward(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(beta), _ptr(S0),
                             _ptr(dy), _ptr(dS_T), _ptr(o["dq"]), _ptr(o["dk"]), _ptr(o["dv"]), _ptr(o["dlog_alpha"]),
                             _ptr(o["dbeta"]), _ptr(o["dS0"]), _ptr(workspace),
                             workspace.numel() * workspace.element_size(), _stream(stream))
     _check(rc, "gdn_backward")
+    if own_ws and stream is not None:
+        workspace.record_stream(stream)
     return o
 
 
