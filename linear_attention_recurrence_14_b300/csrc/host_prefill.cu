@@ -200,6 +200,14 @@ extern "C" gdn_status gdn_prefill_host(const gdn_shape *shape, int64_t tokens_pe
         // the caller's stream continues once every copy is done
         if (fail(cudaEventRecord(ev_done, d2h)) || fail(cudaStreamWaitEvent(comp, ev_done, 0))) break;
     } while (false);
+    if (result != GDN_OK) {
+        // The caller's stream was not chained behind the copies already queued:
+        // let them finish before returning, so that no copy still reads or
+        // writes the caller's host buffers once the call has failed.
+        if (h2d) cudaStreamSynchronize(h2d);
+        if (d2h) cudaStreamSynchronize(d2h);
+        cudaGetLastError();
+    }
     // Release: the runtime keeps streams and events alive until their work completes.
     for (int i = 0; i < 2; ++i) {
         if (ev_h2d[i]) cudaEventDestroy(ev_h2d[i]);
