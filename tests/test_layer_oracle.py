@@ -157,3 +157,55 @@ def test_prologue_features_brute_force_tiny():
                 assert abs(v[0, t, h, e] - u[e]) < 1e-14
                 assert abs(q[0, t, h, e] - u[e] / nrm) < 1e-14
     assert st.shape == (B, K - 1, H * d)
+
+
+def test_prologue_whole_brute_force_tiny():
+    # The whole prologue as the reading notes' "Feature parameterization" and
+    # "Gating dynamics" write it, one element at a time with its own loops:
+    # q = L2Norm(SiLU(conv_q)), k = L2Norm(SiLU(conv_k)), v = SiLU(conv_v) (no
+    # norm), alpha = exp(-e^A softplus(a + b_alpha)), beta = sigma(b), each
+    # convolution reading its own incoming state, and the three outgoing states
+    # (the last K-1 inputs of each stream).  Every input is distinct, so a
+    # swapped state, tap set, gate input or a normalised v fails it.
+    B, T, Hqk, Hv, d, K = 2, 3, 1, 2, 4, 4          # T < K-1 + 1: the outgoing state mixes state and input
+    r = rng(17)
+    xq, xk = r.standard_normal((B, T, Hqk, d)), r.standard_normal((B, T, Hqk, d))
+    xv = r.standard_normal((B, T, Hv, d))
+    wq, wk, wv = r.standard_normal((Hqk * d, K)), r.standard_normal((Hqk * d, K)), r.standard_normal((Hv * d, K))
+    sq, sk = r.standard_normal((B, K - 1, Hqk * d)), r.standard_normal((B, K - 1, Hqk * d))
+    sv = r.standard_normal((B, K - 1, Hv * d))
+    a_raw, b_raw = r.standard_normal((B, T, Hv)), r.standard_normal((B, T, Hv))
+    A, b_alpha = r.standard_normal(Hv) * 0.5, r.standard_normal(Hv) * 0.5
+    out = L.prologue(xq, xk, xv, wq, wk, wv, a_raw, b_raw, A, b_alpha, sq, sk, sv)
+
+    def stream_value(x, w, st, b, t, h, e):
+        # conv input at time tt: the carried state for tt < 0, else the projection
+        c = h * d + e
+        acc = 0.0
+        for i in range(K):
+            tt = t - (K - 1) + i
+            val = st[b, K - 1 + tt, c] if tt < 0 else x[b, tt, h, e]
+            acc += w[c, i] * val
+        return acc / (1.0 + math.exp(-acc))
+
+    for b in range(B):
+        for t in range(T):
+            for name, x, w, st, H, norm in (("q", xq, wq, sq, Hqk, True), ("k", xk, wk, sk, Hqk, True),
+                                            ("v", xv, wv, sv, Hv, False)):
+                for h in range(H):
+                    u = [stream_value(x, w, st, b, t, h, e) for e in range(d)]
+                    scale = 1.0 / math.sqrt(sum(z * z for z in u) + 1e-6) if norm else 1.0
+                    for e in range(d):
+                        assert abs(out[name][b, t, h, e] - u[e] * scale) < 1e-13, (name, b, t, h, e)
+            for h in range(Hv):
+                zz = a_raw[b, t, h] + b_alpha[h]
+                sp = math.log1p(math.exp(zz))
+                assert abs(out["alpha"][b, t, h] - math.exp(-math.exp(A[h]) * sp)) < 1e-14
+                assert abs(out["beta"][b, t, h] - 1.0 / (1.0 + math.exp(-b_raw[b, t, h]))) < 1e-15
+        # outgoing states: the last K-1 conv inputs, oldest first
+        for name, x, st, H in (("state_q", xq, sq, Hqk), ("state_k", xk, sk, Hqk), ("state_v", xv, sv, Hv)):
+            for j in range(K - 1):
+                tt = T - (K - 1) + j
+                for c in range(H * d):
+                    want = st[b, K - 1 + tt, c] if tt < 0 else x[b, tt, c // d, c % d]
+                    assert out[name][b, j, c] == want, (name, b, j, c)

@@ -32,6 +32,17 @@ MUTATIONS = {
     "l2_wrong_axis": ("np.sum(u * u, axis=-1, keepdims=True)", "np.sum(u * u)"),
     # output gate applied as SiLU instead of sigmoid
     "silu_gate": ("return sigmoid(z) * rmsnorm_zc(y, w_norm, eps)", "return silu(z) * rmsnorm_zc(y, w_norm, eps)"),
+    # the prologue's wiring: v normalised like q and k
+    "v_normalised": ("v, sv = feature(xv, wv, state_v, False)", "v, sv = feature(xv, wv, state_v, True)"),
+    # the incoming convolution states of q and k swapped
+    "qk_states_swapped": ("q, sq = feature(xq, wq, state_q, True)\n    k, sk = feature(xk, wk, state_k, True)",
+                          "q, sq = feature(xq, wq, state_k, True)\n    k, sk = feature(xk, wk, state_q, True)"),
+    # q convolved with k's taps
+    "q_reads_k_taps": ("q, sq = feature(xq, wq, state_q, True)", "q, sq = feature(xq, wk, state_q, True)"),
+    # the decay and write gates fed each other's pre-activations
+    "gate_inputs_swapped": ("alpha, beta = gates(a_raw, b_raw, A, b_alpha)", "alpha, beta = gates(b_raw, a_raw, A, b_alpha)"),
+    # the outgoing states of q and k returned under each other's names
+    "qk_states_out_swapped": ("state_q=sq, state_k=sk", "state_q=sk, state_k=sq"),
 }
 
 PIN_TESTS = [
@@ -46,6 +57,7 @@ PIN_TESTS = [
     pins.test_rmsnorm_zero_centred_closed_forms,
     pins.test_epilogue_gate_limits,
     pins.test_prologue_features_brute_force_tiny,
+    pins.test_prologue_whole_brute_force_tiny,
 ]
 
 
