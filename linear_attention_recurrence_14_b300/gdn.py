@@ -187,7 +187,9 @@ def prefill(q, k, v, alpha, beta, S0=None, *, y=None, S_T=None, workspace=None, 
         S_T = torch.empty((shape.B, shape.Hv, shape.dk, shape.dv), dtype=torch.float32, device=v.device)
     own_ws = workspace is None
     if own_ws:
-        workspace = new_workspace(shape, v.device)
+        # The zero fill must precede the prefill on the stream it runs on.
+        with torch.cuda.stream(stream if stream is not None else torch.cuda.current_stream(v.device)):
+            workspace = new_workspace(shape, v.device)
     opts = GdnPrefillOptions(segments, log_eps, max_warmup_chunks, algorithm, test_stall_chunk)
     rc = lib().gdn_prefill_ex(ctypes.byref(shape), ctypes.byref(opts), _ptr(q), _ptr(k), _ptr(v), _ptr(alpha),
                               _ptr(beta), _ptr(S0), _ptr(y), _ptr(S_T), _ptr(workspace),
