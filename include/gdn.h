@@ -175,18 +175,19 @@ gdn_status gdn_read_device_status(void *ws, void *stream);
  * library keeps until the process exits.  Inputs, outputs, layouts and
  * results are those of gdn_prefill.
  *
- * Limit: a shape whose gdn_prefill_workspace_bytes exceeds
- * GDN_NOALLOC_SCRATCH_BYTES (more than 128 (batch, value head) pairs at
- * d = 128, 512 at d = 64) returns GDN_ERR_WORKSPACE before anything runs.
+ * Limit: only an in-place bf16 call (S_T == S0, chunked path) stages its
+ * final states in the array, so only such a call is limited: one whose
+ * B*Hv*dk*dv*4 + 256 bytes exceed GDN_NOALLOC_SCRATCH_BYTES (more than 128
+ * (batch, value head) pairs at d = 128, 512 at d = 64) returns
+ * GDN_ERR_WORKSPACE before anything runs.  Other calls use the 256-byte status
+ * area alone and take any shape gdn_prefill takes.
  * The first call on a device looks up the array's device address (once per
  * device, with that device current); make that first call before any stream
- * capture.  Every call clears the status area with cudaMemsetAsync on
- * `stream` and then enqueues the prefill.  All calls share the one array, so
- * calls whose execution overlaps on the GPU (different streams without
- * ordering between them) race on it and must not be issued.  Bounded waits
- * on the device still end the kernel if they time out, but the status word
- * is not readable through this entry point: callers that need
- * gdn_read_device_status use gdn_prefill with their own workspace.
+ * capture.  All calls share the one array, so calls whose execution overlaps
+ * on the GPU (different streams without ordering between them) race on it
+ * and must not be issued.  The array starts zeroed; errors detected on the
+ * device (a bounded wait that timed out) accumulate in its status area until
+ * gdn_prefill_noalloc_status reads and clears them.
  */
 #define GDN_NOALLOC_SCRATCH_BYTES (256u + 8u * 1024u * 1024u)
 
@@ -194,6 +195,13 @@ gdn_status gdn_prefill_noalloc(const gdn_shape *shape,
                                const void *q, const void *k, const void *v,
                                const float *alpha, const float *beta,
                                const float *S0, void *y, float *S_T, void *stream);
+
+/*
+ * gdn_read_device_status for the array of gdn_prefill_noalloc: synchronise
+ * `stream` and return GDN_OK, GDN_ERR_TIMEOUT or GDN_ERR_DEVICE for the
+ * errors the no-alloc calls recorded since the last read, clearing them.
+ */
+gdn_status gdn_prefill_noalloc_status(void *stream);
 
 /*
  * Channel-wise decay: the decay gate is a vector over the key dimension,

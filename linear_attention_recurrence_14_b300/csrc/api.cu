@@ -76,6 +76,100 @@ gdn_status from_cuda(cudaError_t e) {
     return GDN_ERR_CUDA;
 }
 
+
+// The prefill behind gdn_prefill_ex and gdn_prefill_noalloc: every argument
+// check, then the launch.  ws (ws_bytes) holds the 256-byte status area and,
+// after it, the staging area of an in-place chunked call; a call that needs
+// the staging area and finds it too small returns GDN_ERR_WORKSPACE.
+gdn_status prefill_core(const gdn_shape *shape, const gdn_prefill_options *options, const void *q, const void *k,
+                        const void *v, const float *alpha, const float *beta, const float *S0, void *y, float *S_T,
+                        void *ws, size_t ws_bytes, void *stream_) {
+    int64_t n_qk, n_v, n_gate, n_state;
+    gdn_status st = check_shape(shape, &n_qk, &n_v, &n_gate, &n_state);
+    if (st != GDN_OK) return st;
+    const gdn_shape &s = *shape;
+    const size_t esz = s.dtype == GDN_BF16 ? 2 : 4;
+    const bool has_tokens = s.B * s.T > 0;
+
+    gdn_prefill_options opt{0, 0.f, 0, GDN_ALGO_AUTO, 0};
+    if (options) opt = *options;
+    if (opt.segments < 0 || opt.max_warmup_chunks < 0 || !(opt.log_eps <= 0.f)) return GDN_ERR_INVALID_ARG;
+    if (opt.algorithm < GDN_ALGO_AUTO || opt.algorithm > GDN_ALGO_SEQUENTIAL) return GDN_ERR_INVALID_ARG;
+    if (opt.test_stall_chunk < 0) return GDN_ERR_INVALID_ARG;
+    const int algorithm = opt.algorithm;
+    const int segments = opt.segments;
+
+    if (has_tokens && (!q || !k || !v || !alpha || !beta || !y)) return GDN_ERR_INVALID_ARG;
+    if (!ws || ws_bytes < kStatusBytes) return GDN_ERR_WORKSPACE;
+
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(y, 16) || !aligned(S0, 16) ||
+        !aligned(S_T, 16) || !aligned(alpha, 4) || !aligned(beta, 4) || !aligned(ws, 256))
+        return GDN_ERR_ALIGNMENT;
+
+    const Range rq{q, static_cast<size_t>(n_qk) * esz}, rk{k, static_cast<size_t>(n_qk) * esz};
+    const Range rv{v, static_cast<size_t>(n_v) * esz}, ry{y, static_cast<size_t>(n_v) * esz};
+    const Range ra{alpha, static_cast<size_t>(n_gate) * 4}, rb{beta, static_cast<size_t>(n_gate) * 4};
+    const Range rs0{S0, static_cast<size_t>(n_state) * 4}, rst{S_T, static_cast<size_t>(n_state) * 4};
+    const Range rws{ws, ws_bytes};
+    for (const Range &in : {rq, rk, rv, ra, rb, rs0, rst, rws})
+        if (overlap(ry, in)) return GDN_ERR_ALIASING;
+    for (const Range &in : {rq, rk, rv, ra, rb, rws})
+        if (overlap(rst, in)) return GDN_ERR_ALIASING;
+    for (const Range &in : {rq, rk, rv, ra, rb, rs0})
+        if (overlap(rws, in)) return GDN_ERR_ALIASING;
+    const bool in_place = S0 && S_T && S0 == S_T;
+    if (!in_place && overlap(rst, rs0)) return GDN_ERR_ALIASING;
+
+    const bool chunked = algorithm == GDN_ALGO_CHUNKED || (algorithm == GDN_ALGO_AUTO && s.dtype == GDN_BF16);
+    if (chunked && s.dtype != GDN_BF16) return GDN_ERR_UNSUPPORTED;
+    // Only an in-place chunked call stages its final states.
+    const bool stages = chunked && in_place && has_tokens;
+    if (stages && ws_bytes < kStatusBytes + static_cast<size_t>(n_state) * sizeof(float)) return GDN_ERR_WORKSPACE;
+
+    int num_sms = 0;
+    st = check_device(&num_sms);
+    if (st != GDN_OK) return st;
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+
+    if (s.B * s.Hv == 0) return GDN_OK;
+    if (!has_tokens) {
+        // Empty sequences: the final state is the initial state.
+        if (S_T && !in_place) {
+            if (S0)
+                return from_cuda(cudaMemcpyAsync(S_T, S0, rst.n, cudaMemcpyDeviceToDevice, stream));
+            return from_cuda(cudaMemsetAsync(S_T, 0, rst.n, stream));
+        }
+        return GDN_OK;
+    }
+
+    if (!chunked) {
+        // Token-sequential path: each CTA reads its own head's S0 before it
+        // writes that head's S_T, so in-place needs no staging.
+        gdn::RecurrentParams p{};
+        p.B = s.B; p.T = s.T; p.Hqk = s.Hqk; p.Hv = s.Hv; p.group = s.Hv / s.Hqk;
+        p.q = q; p.k = k; p.v = v; p.alpha = alpha; p.beta = beta;
+        p.S_in = S0; p.S_out = S_T; p.y = y;
+        return from_cuda(gdn::launch_recurrent(p, s.dk, s.dv, static_cast<gdn_dtype>(s.dtype), stream));
+    }
+
+    gdn::ChunkedParams p{};
+    p.B = s.B; p.T = s.T; p.Hqk = s.Hqk; p.Hv = s.Hv; p.group = s.Hv / s.Hqk; p.d = s.dk;
+    p.q = q; p.k = k; p.v = v; p.alpha = alpha; p.beta = beta; p.S0 = S0; p.y = y;
+    p.status = static_cast<uint32_t *>(ws);
+    float *staging = reinterpret_cast<float *>(static_cast<char *>(ws) + kStatusBytes);
+    // Runs of one head are processed by different CTAs, so a run that reads S0
+    // may start after the head's last run wrote S_T: stage in-place results.
+    p.S_T = in_place ? staging : S_T;
+    p.segments = segments;
+    p.log_eps = opt.log_eps < 0.f ? opt.log_eps : kDefaultLogEps;
+    p.max_warmup_chunks = opt.max_warmup_chunks > 0 ? opt.max_warmup_chunks : kDefaultMaxWarmupChunks;
+    p.test_stall_chunk = opt.test_stall_chunk;
+    st = from_cuda(gdn::launch_chunked(p, stream, num_sms));
+    if (st != GDN_OK) return st;
+    if (in_place) return from_cuda(cudaMemcpyAsync(S_T, staging, rst.n, cudaMemcpyDeviceToDevice, stream));
+    return GDN_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -112,89 +206,13 @@ gdn_status gdn_prefill_ex(const gdn_shape *shape, const gdn_prefill_options *opt
                           const void *q, const void *k, const void *v,
                           const float *alpha, const float *beta,
                           const float *S0, void *y, float *S_T,
-                          void *ws, size_t ws_bytes, void *stream_) {
+                          void *ws, size_t ws_bytes, void *stream) {
     int64_t n_qk, n_v, n_gate, n_state;
     gdn_status st = check_shape(shape, &n_qk, &n_v, &n_gate, &n_state);
     if (st != GDN_OK) return st;
-    const gdn_shape &s = *shape;
-    const size_t esz = s.dtype == GDN_BF16 ? 2 : 4;
-    const bool has_tokens = s.B * s.T > 0;
-
-    gdn_prefill_options opt{0, 0.f, 0, GDN_ALGO_AUTO, 0};
-    if (options) opt = *options;
-    if (opt.segments < 0 || opt.max_warmup_chunks < 0 || !(opt.log_eps <= 0.f)) return GDN_ERR_INVALID_ARG;
-    if (opt.algorithm < GDN_ALGO_AUTO || opt.algorithm > GDN_ALGO_SEQUENTIAL) return GDN_ERR_INVALID_ARG;
-    if (opt.test_stall_chunk < 0) return GDN_ERR_INVALID_ARG;
-    const int algorithm = opt.algorithm;
-    const int segments = opt.segments;
-
-    if (has_tokens && (!q || !k || !v || !alpha || !beta || !y)) return GDN_ERR_INVALID_ARG;
     if (!ws) return GDN_ERR_WORKSPACE;
     if (ws_bytes < kStatusBytes + static_cast<size_t>(n_state) * sizeof(float)) return GDN_ERR_WORKSPACE;
-
-    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(y, 16) || !aligned(S0, 16) ||
-        !aligned(S_T, 16) || !aligned(alpha, 4) || !aligned(beta, 4) || !aligned(ws, 256))
-        return GDN_ERR_ALIGNMENT;
-
-    const Range rq{q, static_cast<size_t>(n_qk) * esz}, rk{k, static_cast<size_t>(n_qk) * esz};
-    const Range rv{v, static_cast<size_t>(n_v) * esz}, ry{y, static_cast<size_t>(n_v) * esz};
-    const Range ra{alpha, static_cast<size_t>(n_gate) * 4}, rb{beta, static_cast<size_t>(n_gate) * 4};
-    const Range rs0{S0, static_cast<size_t>(n_state) * 4}, rst{S_T, static_cast<size_t>(n_state) * 4};
-    const Range rws{ws, ws_bytes};
-    for (const Range &in : {rq, rk, rv, ra, rb, rs0, rst, rws})
-        if (overlap(ry, in)) return GDN_ERR_ALIASING;
-    for (const Range &in : {rq, rk, rv, ra, rb, rws})
-        if (overlap(rst, in)) return GDN_ERR_ALIASING;
-    for (const Range &in : {rq, rk, rv, ra, rb, rs0})
-        if (overlap(rws, in)) return GDN_ERR_ALIASING;
-    const bool in_place = S0 && S_T && S0 == S_T;
-    if (!in_place && overlap(rst, rs0)) return GDN_ERR_ALIASING;
-
-    int num_sms = 0;
-    st = check_device(&num_sms);
-    if (st != GDN_OK) return st;
-    cudaStream_t stream = static_cast<cudaStream_t>(stream_);
-
-    if (s.B * s.Hv == 0) return GDN_OK;
-    if (!has_tokens) {
-        // Empty sequences: the final state is the initial state.
-        if (S_T && !in_place) {
-            if (S0)
-                return from_cuda(cudaMemcpyAsync(S_T, S0, rst.n, cudaMemcpyDeviceToDevice, stream));
-            return from_cuda(cudaMemsetAsync(S_T, 0, rst.n, stream));
-        }
-        return GDN_OK;
-    }
-
-    const bool chunked = algorithm == GDN_ALGO_CHUNKED || (algorithm == GDN_ALGO_AUTO && s.dtype == GDN_BF16);
-    if (chunked && s.dtype != GDN_BF16) return GDN_ERR_UNSUPPORTED;
-
-    if (!chunked) {
-        // Token-sequential path: each CTA reads its own head's S0 before it
-        // writes that head's S_T, so in-place needs no staging.
-        gdn::RecurrentParams p{};
-        p.B = s.B; p.T = s.T; p.Hqk = s.Hqk; p.Hv = s.Hv; p.group = s.Hv / s.Hqk;
-        p.q = q; p.k = k; p.v = v; p.alpha = alpha; p.beta = beta;
-        p.S_in = S0; p.S_out = S_T; p.y = y;
-        return from_cuda(gdn::launch_recurrent(p, s.dk, s.dv, static_cast<gdn_dtype>(s.dtype), stream));
-    }
-
-    gdn::ChunkedParams p{};
-    p.B = s.B; p.T = s.T; p.Hqk = s.Hqk; p.Hv = s.Hv; p.group = s.Hv / s.Hqk; p.d = s.dk;
-    p.q = q; p.k = k; p.v = v; p.alpha = alpha; p.beta = beta; p.S0 = S0; p.y = y;
-    p.status = static_cast<uint32_t *>(ws);
-    float *staging = reinterpret_cast<float *>(static_cast<char *>(ws) + kStatusBytes);
-    // Runs of one head are processed by different CTAs, so a run that reads S0
-    // may start after the head's last run wrote S_T: stage in-place results.
-    p.S_T = in_place ? staging : S_T;
-    p.segments = segments;
-    p.log_eps = opt.log_eps < 0.f ? opt.log_eps : kDefaultLogEps;
-    p.max_warmup_chunks = opt.max_warmup_chunks > 0 ? opt.max_warmup_chunks : kDefaultMaxWarmupChunks;
-    p.test_stall_chunk = opt.test_stall_chunk;
-    st = from_cuda(gdn::launch_chunked(p, stream, num_sms));
-    if (st != GDN_OK) return st;
-    if (in_place) return from_cuda(cudaMemcpyAsync(S_T, staging, rst.n, cudaMemcpyDeviceToDevice, stream));
-    return GDN_OK;
+    return prefill_core(shape, options, q, k, v, alpha, beta, S0, y, S_T, ws, ws_bytes, stream);
 }
 
 gdn_status gdn_prefill(const gdn_shape *shape, const void *q, const void *k, const void *v,
@@ -440,20 +458,28 @@ gdn_status noalloc_scratch(void **out) {
 extern "C" gdn_status gdn_prefill_noalloc(const gdn_shape *shape, const void *q, const void *k, const void *v,
                                           const float *alpha, const float *beta, const float *S0, void *y,
                                           float *S_T, void *stream) {
-    const size_t need = gdn_prefill_workspace_bytes(shape);
-    if (need == 0) return GDN_ERR_INVALID_ARG;
-    if (need > GDN_NOALLOC_SCRATCH_BYTES) return GDN_ERR_WORKSPACE;
+    int64_t n_qk, n_v, n_gate, n_state;
+    const gdn_status st0 = check_shape(shape, &n_qk, &n_v, &n_gate, &n_state);
+    if (st0 != GDN_OK) return st0;
+    // Only an in-place chunked (bf16) call needs the staging area; the limit is checked
+    // here, before anything else, so that such a shape is refused without side effects.
+    const bool stages = shape->dtype == GDN_BF16 && S0 && S0 == S_T && shape->B * shape->T > 0;
+    if (stages && kStatusBytes + static_cast<size_t>(n_state) * sizeof(float) > GDN_NOALLOC_SCRATCH_BYTES)
+        return GDN_ERR_WORKSPACE;
     int num_sms = 0;
     gdn_status st = check_device(&num_sms);
     if (st != GDN_OK) return st;
     void *scratch = nullptr;
     st = noalloc_scratch(&scratch);
     if (st != GDN_OK) return st;
-    // The status word must start each call at zero; the array keeps the last call's contents.
-    if (cudaMemsetAsync(scratch, 0, 256, static_cast<cudaStream_t>(stream)) != cudaSuccess) {
-        cudaGetLastError();
-        return GDN_ERR_CUDA;
-    }
-    return gdn_prefill_ex(shape, nullptr, q, k, v, alpha, beta, S0, y, S_T, scratch, GDN_NOALLOC_SCRATCH_BYTES,
-                          stream);
+    // The array starts zeroed and its status word is cleared only by
+    // gdn_prefill_noalloc_status, so device-side errors of every call are kept.
+    return prefill_core(shape, nullptr, q, k, v, alpha, beta, S0, y, S_T, scratch, GDN_NOALLOC_SCRATCH_BYTES, stream);
+}
+
+extern "C" gdn_status gdn_prefill_noalloc_status(void *stream) {
+    void *scratch = nullptr;
+    const gdn_status st = noalloc_scratch(&scratch);
+    if (st != GDN_OK) return st;
+    return gdn_read_device_status(scratch, stream);
 }

@@ -171,6 +171,23 @@ __device__ __forceinline__ void bwait_teardown(uint64_t *bar, uint32_t parity) {
 // All lanes of the warp agree: true only if every lane's wait succeeded.
 __device__ __forceinline__ bool warp_ok(bool ok) { return __all_sync(0xffffffffu, ok); }
 
+// All `count` threads of named barrier `id` agree (the barrier's AND
+// reduction, which is also a barrier): warps that meet at that named barrier
+// take every abort decision together, so none of them is left waiting there
+// for a warp that has already left its loop.
+__device__ __forceinline__ bool bar_and(uint32_t id, uint32_t count, bool ok) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "barrier.cta.red.and.pred q, %2, %3, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"(static_cast<uint32_t>(ok)), "r"(id), "r"(count)
+        : "memory");
+    return r != 0;
+}
+
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t *>(&v);
@@ -763,8 +780,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             float *sg = reinterpret_cast<float *>(sm + OFF_GATES) + buf * kGateFloats;
             float *s_g = sg, *s_u = sg + 64, *s_w = sg + 128, *s_b = sg + 192, *s_bu = sg + 256, *s_misc = sg + 320;
             float *cs = reinterpret_cast<float *>(sm + OFF_CHAIN) + (j % kChainSlots) * kChainFloats;
+            // Abort decisions are reduced over both gate warps (named barrier 4).
             const bool ok = bwait(&bars[B_GEMPTY + buf], ((j >> 1) & 1) ^ 1, abort_flag, p.status);
-            if (!warp_ok(ok)) break;
+            if (!bar_and(4, 64, ok)) break;
             const float a_cur = a_nxt, b_cur = b_nxt;
             load_gates(j + 1);
             // g = inclusive cumsum of log alpha over the chunk
@@ -802,7 +820,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // T (TREADY(j-1)).
             bool ok2 = j == 0 || bwait(&bars[B_TREADY], (j - 1) & 1, abort_flag, p.status);
             ok2 = ok2 && bwait(&bars[B_GRAM + (j & 1)], (j >> 1) & 1, abort_flag, p.status);
-            if (!warp_ok(ok2)) break;
+            if (!bar_and(4, 64, ok2)) break;
             tc_fence_after();
             const uint32_t gw = tb + TM_GW + (j & 1) * 64;
             if (fastc)
@@ -836,7 +854,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool ok = bwait(&bars[B_GFULL + gbuf], (j >> 1) & 1, abort_flag, p.status);
             ok = ok && bwait(&bars[B_FULL + s], (j / kStages) & 1, abort_flag, p.status);
             ok = ok && bwait(&bars[B_GRAM + (j & 1)], (j >> 1) & 1, abort_flag, p.status);
-            if (!warp_ok(ok)) return false;
+            if (!bar_and(2, 128, ok)) return false;
             if (l >= 64) return true;
             const uint32_t gw = tb + TM_GW + (j & 1) * 64;
             uint8_t *pbuf = sm + OFF_P + s * kPBytes;
@@ -880,10 +898,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float *sg = reinterpret_cast<const float *>(sm + OFF_GATES) + gbuf * kGateFloats;
                 const float *s_g = sg, *s_b = sg + 192, *s_bu = sg + 256, *s_misc = sg + 320;
                 const bool fast = s_misc[2] != 0.f;
-                {
-                    const bool ok = bwait(&bars[B_SOLVED], j & 1, abort_flag, p.status);
-                    if (!warp_ok(ok)) break;
-                }
+                // Abort decisions of this warpgroup are reduced over its 128 threads
+                // (named barrier 2, which the merges below also use).
+                if (!bar_and(2, 128, bwait(&bars[B_SOLVED], j & 1, abort_flag, p.status))) break;
                 // The factors F_IK (three tiles per warp) and bf16 T1, T2 of diagonal
                 // block lw; then the off-diagonal blocks T_IJ by block column: column 0
                 // split over warps 0 and 3 (one 8-column tile each), column 1 on warp 1,
@@ -902,10 +919,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // The W^T, U~^T MMAs of chunk j have read T1, T2 (rewritten by the next
                 // merges) and K (exact path: K~ = diag(lambda) K in place).  Waiting here
                 // also keeps this warpgroup at most one TREADY phase ahead of the MMA thread.
-                {
-                    const bool ok = bwait(&bars[B_WU], j & 1, abort_flag, p.status);
-                    if (!warp_ok(ok)) break;
-                }
+                if (!bar_and(2, 128, bwait(&bars[B_WU], j & 1, abort_flag, p.status))) break;
                 tc_fence_after();
                 {
                     // -W^T row l (key index l, 64 tokens) as one swizzled 128-byte row of

@@ -29,7 +29,7 @@ EXPORTS = ("gdn_status_string", "gdn_prefill_workspace_bytes", "gdn_prefill", "g
            "gdn_decode_step", "gdn_read_device_status", "gdn_device_supported", "gdn_abi_version",
            "gdn_prefill_noalloc", "gdn_layer_prologue", "gdn_layer_epilogue", "gdn_prefill_host_workspace_bytes",
            "gdn_prefill_host", "gdn_prefill_cw", "gdn_decode_step_cw", "gdn_backward_workspace_bytes",
-           "gdn_backward")
+           "gdn_backward", "gdn_prefill_noalloc_status")
 NOALLOC_SCRATCH_BYTES = 256 + 8 * 1024 * 1024
 
 
@@ -88,6 +88,8 @@ def lib() -> ctypes.CDLL:
             L.gdn_prefill_noalloc.argtypes = [sp, vp, vp, vp, fp, fp, fp, vp, fp, vp]
             L.gdn_decode_step.restype = ctypes.c_int
             L.gdn_decode_step.argtypes = [sp, vp, vp, vp, fp, fp, fp, vp, vp]
+            L.gdn_prefill_noalloc_status.restype = ctypes.c_int
+            L.gdn_prefill_noalloc_status.argtypes = [vp]
             L.gdn_read_device_status.restype = ctypes.c_int
             L.gdn_read_device_status.argtypes = [vp, vp]
             L.gdn_layer_prologue.restype = ctypes.c_int
@@ -213,6 +215,11 @@ def prefill_noalloc(q, k, v, alpha, beta, S0=None, *, y=None, S_T=None, stream=N
                                    _ptr(S0), _ptr(y), _ptr(S_T), _stream(stream))
     _check(rc, "gdn_prefill_noalloc")
     return y, S_T
+
+
+def noalloc_status(stream=None) -> int:
+    """Synchronise and return (and clear) the device status the no-alloc calls recorded."""
+    return int(lib().gdn_prefill_noalloc_status(_stream(stream)))
 
 
 def decode_step(q, k, v, alpha, beta, S, *, y=None, stream=None):

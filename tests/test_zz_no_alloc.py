@@ -48,6 +48,8 @@ def test_noalloc_matches_workspace_entry_point_twice(dtype, d, T, G):
         torch.cuda.synchronize()
         assert rel_err(y, y_ref.double().cpu().numpy()) <= tol
         assert rel_err(S_T, S_ref.double().cpu().numpy()) <= tol
+    # no device-side error recorded in the array's status area
+    assert gdn.noalloc_status() == gdn.GDN_OK
 
 
 def test_noalloc_in_place_state():
@@ -65,12 +67,30 @@ def test_noalloc_in_place_state():
         assert rel_err(S, S_ref.double().cpu().numpy()) <= TOL[torch.bfloat16]
 
 
+def test_noalloc_out_of_place_needs_no_staging():
+    # 130 (batch, value head) pairs at d = 128: an in-place call would not fit the
+    # staging area, but an out-of-place call uses only the status area.
+    x = make_prefill_inputs(130, 70, 1, 1, 128, "bf16", decay_scale=0.05, s0_std=0.02, seed=47, device="cuda")
+    y_ref, S_ref = gdn.prefill(x.q, x.k, x.v, x.alpha, x.beta, x.S0)
+    y = torch.full_like(x.v, float("nan"))
+    S_T = torch.full_like(S_ref, float("nan"))
+    assert _noalloc_abi(x, y, S_T) == gdn.GDN_OK
+    torch.cuda.synchronize()
+    assert rel_err(y, y_ref.double().cpu().numpy()) <= TOL[torch.bfloat16]
+    assert rel_err(S_T, S_ref.double().cpu().numpy()) <= TOL[torch.bfloat16]
+    assert gdn.noalloc_status() == gdn.GDN_OK
+
+
 def test_noalloc_rejects_shapes_beyond_its_scratch():
-    # 129 (batch, value head) pairs at d = 128 need more than the fixed scratch:
-    # refused on the host before anything is enqueued.
+    # In place (S_T == S0), 129 (batch, value head) pairs at d = 128 would need more
+    # staging than the fixed array holds: refused on the host before anything is
+    # enqueued (the pointers are never dereferenced).
     shape = gdn.GdnShape(129, 64, 1, 1, 128, 128, gdn.GDN_BF16)
     assert gdn.workspace_bytes(shape) > gdn.NOALLOC_SCRATCH_BYTES
     base = 1 << 32
-    args = [ctypes.c_void_p(base + i * (1 << 24)) for i in range(8)]
-    rc = gdn.lib().gdn_prefill_noalloc(ctypes.byref(shape), *args, None)
+    q, k, v, a, b, S, y = (ctypes.c_void_p(base + i * (1 << 24)) for i in range(7))
+    rc = gdn.lib().gdn_prefill_noalloc(ctypes.byref(shape), q, k, v, a, b, S, y, S, None)
     assert rc == 4  # GDN_ERR_WORKSPACE
+    # head dims the kernels do not implement: the shape check's own status
+    shape = gdn.GdnShape(1, 64, 1, 1, 96, 96, gdn.GDN_BF16)
+    assert gdn.lib().gdn_prefill_noalloc(ctypes.byref(shape), q, k, v, a, b, S, y, S, None) == 2  # GDN_ERR_UNSUPPORTED
