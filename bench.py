@@ -11,7 +11,12 @@ and reports it under "decode", and the layer steps around the recurrence
 (fused prologue: short convolution, SiLU, L2Norm, gates; fused epilogue:
 sigmoid gate times zero-centred RMSNorm) on the prefill shape under "layer",
 and the backward pass (gradients of the recurrence) on the training-shape
-workload (B=2, H=16, T=4096, d=128, bf16) under "backward".
+workload (B=2, H=16, T=4096, d=128, bf16) under "backward".  The other
+prefill workloads are timed beside it: the training shape ("prefill_train"),
+the long-context prefill (B=1, H=16, T=2^20, "prefill_long") and the grouped
+shape with gates that barely decay ("prefill_weak_decay"), each with its
+rooflines and an oracle sample.  The line ends with "summary", the headline
+number of every section.
 
 Printed: one JSON line (rank 0).  `value` is prefill tokens/s summed over all
 ranks; `e2e` is the same metric through the C ABI with host buffers
@@ -198,7 +203,7 @@ def max_over_ranks(x: float, ws: int, device) -> float:
 
 
 # ----------------------------------------------------------------- oracle timing
-def time_oracle_prefill(w: dict, seed: int, target_s: float, device="cpu"):
+def time_oracle_prefill(w: dict, seed: int, target_s: float, device="cpu", label: str = PREFILL_WORKLOAD):
     """Time the fp64 oracle on the first T_s tokens of the workload (all heads).
 
     Returns (tokens/s, sample description, threads).  T_s is grown until one
@@ -221,7 +226,7 @@ def time_oracle_prefill(w: dict, seed: int, target_s: float, device="cpu"):
         Ts = min(w["T"], int(Ts * min(16.0, max(2.0, target_s / max(dt, 1e-3)))))
     tokens = w["B"] * Ts
     sample = (f"oracle fp64 on B={w['B']} x T={Ts} tokens x {w['Hv']} value heads of the "
-              f"{PREFILL_WORKLOAD} workload ({dt:.2f} s)")
+              f"{label} workload ({dt:.2f} s)")
     return tokens / dt, sample, threads, dt
 
 
@@ -440,6 +445,12 @@ def run_ours(args, ws, rank, local):
     x = None
     torch.cuda.empty_cache()
 
+    # ------------------------------------------------------------- the other prefill workloads
+    prefills = {}
+    if not args.no_prefill_configs:
+        for name, nlaunch in (("train", 20), ("weak", 5), ("long", 3)):
+            prefills[name] = time_prefill_section(args, peaks, seed, dev, ws, local, name, nlaunch)
+
     # ------------------------------------------------------------- decode
     dec = dec_cw = None
     if not args.no_decode:
@@ -475,10 +486,104 @@ def run_ours(args, ws, rank, local):
                    "algorithm": gdn.ALGO_NAMES[args.algorithm], "segments": args.segments,
                    "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"},
         "roofline": roofline, "clocks": clocks, "e2e": e2e, "cpu_baseline": cpu, "gpu_launches": gpu_launches,
-        "decode": dec, "decode_channelwise": dec_cw, "layer": layer, "backward": bwd, "check": check,
+        "check": check, "layer": layer, "backward": bwd,
+        "prefill_train": prefills.get("train"), "prefill_long": prefills.get("long"),
+        "prefill_weak_decay": prefills.get("weak"), "decode": dec, "decode_channelwise": dec_cw,
     }
+    # Last, so that a reader of the line's tail sees every section: its headline numbers.
+    line["summary"] = summarize(line)
     if rank == 0:
         print(json.dumps(line), flush=True)
+
+
+def time_prefill_section(args, peaks, seed, dev, ws, local, name: str, launches_timed: int = 10) -> dict:
+    """gdn_prefill on another prefill workload (name in WORKLOADS): the median of `launches_timed`
+    launches (CUDA events on the launching stream), its HBM and tensor-core rooflines, clocks, and
+    the oracle on a bounded prefix of the same workload."""
+    import torch
+
+    from linear_attention_recurrence_14_b300 import gdn
+    from linear_attention_recurrence_14_b300.inputs import WORKLOADS, make_prefill_inputs
+
+    w = dict(WORKLOADS[name])
+    x = make_prefill_inputs(w["B"], w["T"], w["Hqk"], w["Hv"], w["d"], w["dtype"], w["decay_scale"], w["s0_std"],
+                            seed=seed, device=dev)
+    shape = gdn.shape_of(x.q, x.v)
+    y = torch.empty_like(x.v)
+    S_T = torch.empty((w["B"], w["Hv"], w["d"], w["d"]), dtype=torch.float32, device=dev)
+    wsb = gdn.new_workspace(shape, dev)
+
+    def fn():
+        gdn.prefill(x.q, x.k, x.v, x.alpha, x.beta, x.S0, y=y, S_T=S_T, workspace=wsb)
+
+    for _ in range(max(3, args.warmup)):
+        fn()
+    torch.cuda.synchronize()
+    if gdn.read_device_status(wsb) != 0:
+        raise SystemExit(f"device status error in the {name} prefill")
+    stream = torch.cuda.current_stream()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(launches_timed)]
+    barrier(ws)
+    with ClockSampler(local) as clk:
+        for a, b in evs:
+            a.record(stream)
+            fn()
+            b.record(stream)
+        torch.cuda.synchronize()
+    if gdn.read_device_status(wsb) != 0:
+        raise SystemExit(f"device status error in the {name} prefill")
+    ms = max_over_ranks(statistics.median(a.elapsed_time(b) for a, b in evs), ws, dev)
+    nbytes = prefill_bytes(w)
+    flops = useful_flops_per_token_head(w["d"], w["Hv"] // w["Hqk"]) * w["B"] * w["T"] * w["Hv"]
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    tf = flops / (ms * 1e-3) / 1e12
+    out = {
+        "workload": f"{name}: B={w['B']}, T={w['T']}, Hqk={w['Hqk']}, Hv={w['Hv']}, d={w['d']}, {w['dtype']} q/k/v, "
+                    f"gate scale {w['decay_scale']}, S0 std {w['s0_std']}",
+        "ms": ms, "tokens_per_s": w["B"] * w["T"] * ws / (ms * 1e-3), "gpu_launches": 1,
+        "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": gbs / peaks["hbm_gbs"], "traffic": None, "bytes_per_launch": nbytes,
+                     "peak_source": peaks["source"],
+                     "tensor": {"achieved": tf, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                                "frac": tf / peaks["bf16_tflops"], "flops_per_launch": flops}},
+        "clocks": clk.summary(),
+        "l2": f"inputs {nbytes / 1e9:.2f} GB per launch" + (" (larger than L2, no flush)" if nbytes > 126e6 else
+                                                            " (fit in L2: timed back to back)"),
+    }
+    del x, y, S_T, wsb
+    torch.cuda.empty_cache()
+    if local == 0 and not args.no_cpu_baseline:
+        def oracle_rate():
+            v, sample, threads, _ = time_oracle_prefill(w, seed, args.oracle_seconds, label=name)
+            return {"value": v, "unit": "tokens/s", "cores": threads, "kind": "oracle", "sample": sample}
+        out["cpu_baseline"] = _oracle_timed(oracle_rate, f"{name} oracle")
+    return out
+
+
+def summarize(line: dict) -> dict:
+    """Headline numbers of every section of the line, rounded: times (ms), rates, and the
+    fraction of the binding roof (HBM, or the fp32 FMA peak for the backward)."""
+    def g(d, *path):
+        for k in path:
+            if not isinstance(d, dict) or d.get(k) is None:
+                return None
+            d = d[k]
+        return float(f"{d:.4g}") if isinstance(d, (int, float)) else d
+    out = {"grouped_ms": g(line, "roofline", "launch_ms"), "grouped_hbm": g(line, "roofline", "frac"),
+           "grouped_tc": g(line, "roofline", "tensor", "frac"), "e2e_ms": g(line, "e2e", "ms_per_step"),
+           "check_err": g(line, "check", "max_rel_err_y")}
+    for key, short in (("prefill_train", "train"), ("prefill_long", "long"), ("prefill_weak_decay", "weak")):
+        out[f"{short}_ms"] = g(line, key, "ms")
+        out[f"{short}_hbm"] = g(line, key, "roofline", "frac")
+    out["decode_steps_s"] = g(line, "decode", "value")
+    out["decode_hbm"] = g(line, "decode", "roofline", "frac")
+    out["decode_cw_steps_s"] = g(line, "decode_channelwise", "value")
+    out["decode_cw_hbm"] = g(line, "decode_channelwise", "roofline", "frac")
+    out["prologue_hbm"] = g(line, "layer", "prologue", "roofline", "frac")
+    out["epilogue_hbm"] = g(line, "layer", "epilogue", "roofline", "frac")
+    out["backward_ms"] = g(line, "backward", "ms")
+    out["backward_alu"] = g(line, "backward", "roofline", "frac")
+    return {k: v for k, v in out.items() if v is not None}
 
 
 def spot_check(x, y, S_T, w):
@@ -750,6 +855,8 @@ def main(argv=None):
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-layer", action="store_true")
     ap.add_argument("--no-backward", action="store_true")
+    ap.add_argument("--no-prefill-configs", action="store_true",
+                    help="skip the training-shape, long-context and weak-decay prefill sections")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-check", dest="check", action="store_false")
     args = ap.parse_args(argv)

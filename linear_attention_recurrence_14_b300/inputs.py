@@ -4,7 +4,7 @@ This module holds the input recipe only -- no arithmetic of the recurrence.
 Both the tests (for the CUDA path and for the fp64 oracle) and the benchmark
 draw their inputs from here, so the two sides always see the same values.
 
-Recipe (the five workloads below):
+Recipe (the workloads below):
   * q, k ~ N(0, 1) per element, then L2-normalised per (token, head) in fp32
     and stored in the workload dtype.  The Qwen3.8-Next reading notes
     (jianyuh.github.io, section 2.1, "Feature parameterization") normalise q
@@ -30,7 +30,7 @@ from dataclasses import dataclass
 
 import torch
 
-# Named workloads: shapes and gate scales of the five reference workloads.
+# Named workloads: shapes and gate scales of the five reference workloads, and a weak-decay variant.
 WORKLOADS = {
     # B=1, H=2, T=256, d=64, fp32, gate scale 0.1, zero initial state.
     "tiny": dict(kind="prefill", B=1, T=256, Hqk=2, Hv=2, d=64, dtype="f32", decay_scale=0.1, s0_std=0.0),
@@ -42,6 +42,10 @@ WORKLOADS = {
     "decode": dict(kind="decode", B=256, steps=128, Hqk=16, Hv=32, d=128, dtype="bf16", decay_scale=0.05, s0_std=0.02),
     # B=1, H=16, T=2^20, d=128, bf16, gate scale 0.01, zero initial state.
     "long": dict(kind="prefill", B=1, T=1 << 20, Hqk=16, Hv=16, d=128, dtype="bf16", decay_scale=0.01, s0_std=0.0),
+    # The grouped shape with gates that barely decay (gate scale 1.2e-4: mean log alpha
+    # about -1e-4 per token, alpha ~ 1 - 1e-4), the regime where no short window of
+    # preceding tokens forgets the state.
+    "weak": dict(kind="prefill", B=1, T=65536, Hqk=16, Hv=32, d=128, dtype="bf16", decay_scale=1.2e-4, s0_std=0.02),
 }
 
 _DTYPES = {"f32": torch.float32, "bf16": torch.bfloat16}
