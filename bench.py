@@ -540,7 +540,8 @@ def time_prefill_section(args, peaks, seed, dev, ws, local, name: str, launches_
     out = {
         "workload": f"{name}: B={w['B']}, T={w['T']}, Hqk={w['Hqk']}, Hv={w['Hv']}, d={w['d']}, {w['dtype']} q/k/v, "
                     f"gate scale {w['decay_scale']}, S0 std {w['s0_std']}",
-        "ms": ms, "tokens_per_s": w["B"] * w["T"] * ws / (ms * 1e-3), "gpu_launches": 1,
+        "ms": ms, "tokens_per_s": w["B"] * w["T"] * ws / (ms * 1e-3),
+        "gpu_launches": gdn.prefill_launches(shape) * launches_timed,
         "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": gbs / peaks["hbm_gbs"], "traffic": None, "bytes_per_launch": nbytes,
                      "peak_source": peaks["source"],

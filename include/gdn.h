@@ -87,8 +87,17 @@ typedef struct {
  *   64 tokens) over which sum(log alpha) <= log_eps.  With unit keys and
  *   beta in [0,1] every step is a contraction of norm <= alpha_t, so the state
  *   so rebuilt differs from the exact one by at most exp(log_eps) times the
- *   state norm at the window start.  When no such window exists the run
- *   restarts from token 0 and the initial state (exact).
+ *   state norm at the window start.  When no such window exists (gates at
+ *   or near 1) the run's entering state is computed exactly instead: each
+ *   run is an affine map of the state it enters with (the product of the
+ *   per-token transitions alpha_t (I - beta_t k_t k_t^T) plus the values it
+ *   writes); a transition pass computes every run's map, a combine kernel
+ *   chains them per head from S0, and the output pass starts each run from
+ *   its exact state (four launches; the exact sequence split).  The split is
+ *   taken for sequences of at least 256 chunks when the workspace holds the
+ *   runs' maps (always with gdn_prefill_workspace_bytes; the fixed scratch of
+ *   gdn_prefill_noalloc holds them for small shapes only); otherwise such a
+ *   run restarts from token 0 and the initial state (also exact).
  * log_eps: natural log of that bound (0 = default, -20 ln 2); must be <= 0.
  * max_warmup_chunks: window limit (0 = default, 64).
  * algorithm: GDN_ALGO_AUTO (bf16 -> chunked, fp32 -> sequential),
@@ -117,10 +126,23 @@ const char *gdn_status_string(gdn_status status);
 
 /*
  * Bytes of device workspace gdn_prefill needs for this shape: a 256-byte
- * status area plus B*Hv*dk*dv fp32 values used to stage S_T when it aliases
- * S0.  Returns 0 for an invalid shape.
+ * status area, B*Hv*dk*dv fp32 values used to stage S_T when it aliases S0,
+ * and, for bf16 shapes of more than one chunk, the exact sequence split's
+ * per-run flags and fp32 run maps (3*dk*dv values per run, for up to
+ * ceil(320 / (B*Hv)) runs per head).  Returns 0 for an invalid shape.
  */
 size_t gdn_prefill_workspace_bytes(const gdn_shape *shape);
+
+/*
+ * Kernels that one gdn_prefill call with this shape and these options
+ * enqueues on a workspace of gdn_prefill_workspace_bytes(shape): 0 for an
+ * empty problem, 4 when the chunked path takes the exact sequence split (how
+ * many of its runs need it is decided on the device; runs that do not leave
+ * the extra kernels at once), else 1.  Host-side copies (an in-place S_T, an
+ * empty sequence's S_T) are not kernels.  Returns -1 for an invalid shape or
+ * options or when no supported device is current.
+ */
+int gdn_prefill_launches(const gdn_shape *shape, const gdn_prefill_options *options);
 
 /*
  * Prefill: run the recurrence over T tokens of each (batch, value head) from

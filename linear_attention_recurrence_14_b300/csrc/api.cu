@@ -53,20 +53,31 @@ bool overlap(Range a, Range b) {
     return a0 < b0 + b.n && b0 < a0 + a.n;
 }
 
+// The current device's compute capability check and SM count, queried once
+// per device (the attributes do not change while the process runs).
 gdn_status check_device(int *num_sms) {
+    constexpr int kMaxDev = 64;
+    static std::mutex lock;
+    static int cached_sms[kMaxDev] = {};    // 0 = not queried, -1 = unsupported
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) {
         cudaGetLastError();
         return GDN_ERR_CUDA;
     }
-    int major = 0, minor = 0;
-    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
-        cudaGetLastError();
-        return GDN_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDev) return GDN_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> guard(lock);
+    if (cached_sms[dev] == 0) {
+        int major = 0, minor = 0, sms = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+            cudaGetLastError();
+            return GDN_ERR_CUDA;
+        }
+        cached_sms[dev] = (major == 10 && minor == 3) ? sms : -1;
     }
-    if (major != 10 || minor != 3) return GDN_ERR_UNSUPPORTED;
+    if (cached_sms[dev] < 0) return GDN_ERR_UNSUPPORTED;
+    *num_sms = cached_sms[dev];
     return GDN_OK;
 }
 
@@ -74,6 +85,27 @@ gdn_status from_cuda(cudaError_t e) {
     if (e == cudaSuccess) return GDN_OK;
     cudaGetLastError();
     return GDN_ERR_CUDA;
+}
+
+size_t round256(size_t x) { return (x + 255) / 256 * 256; }
+
+// Workspace layout of a prefill: status area, staging of in-place final states,
+// then (bf16, chunked path) the exact sequence split's per-head flags and its
+// segment states for up to about two waves of segments.  Returns the total.
+size_t exact_split_layout(const gdn_shape &s, int64_t n_state, size_t *off_flag, size_t *off_seg, size_t *seg_bytes) {
+    const size_t base = kStatusBytes + static_cast<size_t>(n_state) * sizeof(float);
+    *off_flag = round256(base);
+    *off_seg = *off_flag;
+    *seg_bytes = 0;
+    const int64_t pairs = s.B * s.Hv;
+    const int64_t nchunks = (s.T + 63) / 64;
+    if (s.dtype != GDN_BF16 || pairs == 0 || nchunks <= 1) return base;
+    int64_t segs = (2 * gdn::kExactSplitSmBound + pairs - 1) / pairs;
+    if (segs > nchunks) segs = nchunks;
+    if (segs <= 1) return base;
+    *off_seg = *off_flag + round256(static_cast<size_t>(pairs) * segs * sizeof(int));
+    *seg_bytes = static_cast<size_t>(pairs) * segs * 3 * s.dk * s.dv * sizeof(float);
+    return *off_seg + *seg_bytes;
 }
 
 
@@ -164,6 +196,13 @@ gdn_status prefill_core(const gdn_shape *shape, const gdn_prefill_options *optio
     p.log_eps = opt.log_eps < 0.f ? opt.log_eps : kDefaultLogEps;
     p.max_warmup_chunks = opt.max_warmup_chunks > 0 ? opt.max_warmup_chunks : kDefaultMaxWarmupChunks;
     p.test_stall_chunk = opt.test_stall_chunk;
+    size_t off_flag = 0, off_seg = 0, seg_bytes = 0;
+    const size_t full = exact_split_layout(s, n_state, &off_flag, &off_seg, &seg_bytes);
+    if (seg_bytes > 0 && ws_bytes >= full) {
+        p.exact_flag = reinterpret_cast<int *>(static_cast<char *>(ws) + off_flag);
+        p.seg_state = reinterpret_cast<float *>(static_cast<char *>(ws) + off_seg);
+        p.seg_state_bytes = seg_bytes;
+    }
     st = from_cuda(gdn::launch_chunked(p, stream, num_sms));
     if (st != GDN_OK) return st;
     if (in_place) return from_cuda(cudaMemcpyAsync(S_T, staging, rst.n, cudaMemcpyDeviceToDevice, stream));
@@ -196,10 +235,34 @@ int gdn_device_supported(void) {
     return check_device(&sms) == GDN_OK ? 1 : 0;
 }
 
+int gdn_prefill_launches(const gdn_shape *shape, const gdn_prefill_options *options) {
+    int64_t n_qk, n_v, n_gate, n_state;
+    if (check_shape(shape, &n_qk, &n_v, &n_gate, &n_state) != GDN_OK) return -1;
+    const gdn_shape &s = *shape;
+    gdn_prefill_options opt{0, 0.f, 0, GDN_ALGO_AUTO, 0};
+    if (options) opt = *options;
+    if (opt.segments < 0 || opt.algorithm < GDN_ALGO_AUTO || opt.algorithm > GDN_ALGO_SEQUENTIAL) return -1;
+    if (s.B * s.T * s.Hv == 0) return 0;
+    const bool chunked =
+        opt.algorithm == GDN_ALGO_CHUNKED || (opt.algorithm == GDN_ALGO_AUTO && s.dtype == GDN_BF16);
+    if (!chunked) return 1;
+    if (s.dtype != GDN_BF16) return -1;
+    int num_sms = 0;
+    if (check_device(&num_sms) != GDN_OK) return -1;
+    const int64_t pairs = s.B * s.Hv, nchunks = (s.T + 63) / 64;
+    int P = gdn::plan_segments(pairs, nchunks, num_sms, opt.segments);
+    const int64_t len = (nchunks + P - 1) / P;
+    P = static_cast<int>((nchunks + len - 1) / len);
+    size_t off_flag = 0, off_seg = 0, seg_bytes = 0;
+    exact_split_layout(s, n_state, &off_flag, &off_seg, &seg_bytes);
+    return gdn::takes_exact_split(pairs, nchunks, P, s.dk, seg_bytes) ? 4 : 1;
+}
+
 size_t gdn_prefill_workspace_bytes(const gdn_shape *shape) {
     int64_t n_qk, n_v, n_gate, n_state;
     if (check_shape(shape, &n_qk, &n_v, &n_gate, &n_state) != GDN_OK) return 0;
-    return kStatusBytes + static_cast<size_t>(n_state) * sizeof(float);
+    size_t off_flag = 0, off_seg = 0, seg_bytes = 0;
+    return exact_split_layout(*shape, n_state, &off_flag, &off_seg, &seg_bytes);
 }
 
 gdn_status gdn_prefill_ex(const gdn_shape *shape, const gdn_prefill_options *options,

@@ -139,6 +139,15 @@ struct Dev {
     __nv_bfloat16 *y;
     float *S_T;
     uint32_t *status;
+    // Exact sequence split (see launch_chunked): pass 1 runs every segment's
+    // transition (kind 0: from the zero state, or S0 for segment 0, with the
+    // real values; kind 1: from the identity with the values zero), pass 0 is
+    // the output pass; heads with exact_flag set start each segment from the
+    // state the combine kernel wrote.  seg_state: [pairs][nseg][3][d][d] fp32,
+    // slots B (kind 0 end), M (kind 1 end), In (entering state).
+    int pass;
+    const int *exact_flag;
+    float *seg_state;
 };
 
 // Slow path of a bounded wait (out of line: one copy for every call site).
@@ -166,6 +175,13 @@ __device__ __forceinline__ void bwait_teardown(uint64_t *bar, uint32_t parity) {
     while (!mbar_try_wait_sleep(bar, parity, 20000u)) {
         if (globaltimer_ns() - t0 > kWaitLimitNs) return;
     }
+}
+
+// True when some segment of head `pr` has no warm-up window (flags of the plan).
+__device__ __forceinline__ bool head_needs_split(const int *flag, int pr, int nseg) {
+    int any = 0;
+    for (int sgm = 1; sgm < nseg; ++sgm) any |= flag[static_cast<int64_t>(pr) * nseg + sgm];
+    return any != 0;
 }
 
 // All lanes of the warp agree: true only if every lane's wait succeeded.
@@ -534,8 +550,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int lane = tid & 31;
 
     const int pairs = p.B * p.Hv;
-    const int seg = blockIdx.x / pairs;
-    const int pr = blockIdx.x % pairs;
+    const int bx = static_cast<int>(blockIdx.x % static_cast<unsigned>(pairs * p.nseg));
+    const int kind = p.pass == 1 ? static_cast<int>(blockIdx.x / static_cast<unsigned>(pairs * p.nseg)) : -1;
+    const int seg = bx / pairs;
+    const int pr = bx % pairs;
+    const bool exact = p.exact_flag != nullptr && head_needs_split(p.exact_flag, pr, p.nseg);
+    // Transition pass: only heads that need the exact split, only segments whose
+    // transition is used (not the last; segment 0 starts from S0, so no M).
+    if (p.pass == 1 && (!exact || seg == p.nseg - 1 || (kind == 1 && seg == 0))) return;
     const int b = pr / p.Hv;
     const int hv = pr % p.Hv;
     const int hk = hv / p.group;
@@ -581,8 +603,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     // start, eight chunks per round, until the decay over the window reaches
     // exp(log_eps), chunk 0 is reached (exact start from S0) or the window
     // limit is hit (exact restart from token 0).
-    if (tid == 128 && seg == 0) misc->c_w = 0;
-    if (warp >= 4 && warp < 12 && seg > 0) {
+    // (No window on the transition pass or for an exactly split head: each
+    // segment starts at its own first chunk.)
+    const bool windowed = p.pass == 0 && !exact;
+    if (tid == 128 && (seg == 0 || !windowed)) misc->c_w = windowed ? 0 : c_begin;
+    if (warp >= 4 && warp < 12 && seg > 0 && windowed) {
         const int gw = warp - 4;
         float acc = 0.f;
         for (int r = 0;; ++r) {
@@ -632,7 +657,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int c_w = misc->c_w;
     const int n = c_end - c_w;
     const int n_s = n;
-    const bool use_s0 = c_w == 0 && p.S0 != nullptr;
+    const bool use_s0 = c_w == 0 && p.S0 != nullptr && kind != 1;
+    const bool zero_v = kind == 1;   // the identity run propagates the state with v = 0
 
     const uint32_t smb = smem_u32(sm);
     auto kq_addr = [&](int s) { return smb + OFF_KQ + s * kKQBytes; };
@@ -696,7 +722,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             auto wu = [&](int j) {
                 const int s = j % kStages;
                 mma_run_t<4, false>(tb + TM_GW + (j & 1) * 64, smem_mnmajor(kq_addr(s) + 8192, 16384u), smem_kmajor(t1, 0u), ID_MK, 0u);
-                mma_run_t<4, false>(tb + TM_ZU, smem_mnmajor(vw_addr(s), 8192u), smem_kmajor(t2, 0u), ID_MK, 0u);
+                if (!zero_v)
+                    mma_run_t<4, false>(tb + TM_ZU, smem_mnmajor(vw_addr(s), 8192u), smem_kmajor(t2, 0u), ID_MK, 0u);
             };
             bool ok = true;
             do {
@@ -724,7 +751,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // U^T = U~^T + S^T (-W)^T   (-W^T stored [dk][tokens], MN-major)
                     const MmaOperand sa{0ull, sb, 0u, 8u, 3u};          // S^T bf16: 8 columns per K step
                     const MmaOperand ua{0ull, zu, 32u, 8u, 1u};         // U^T bf16: tokens 0-31 at 0-15, 32-63 at 32-47
-                    mma_run_t<8, true>(zu, sa, smem_mnmajor(vw_addr(s), 16u), ID_TSM, 1u);
+                    mma_run_t<8, true>(zu, sa, smem_mnmajor(vw_addr(s), 16u), ID_TSM, zero_v ? 0u : 1u);
                     mma_commit_w(&bars[B_UFULL]);
                     // Gram of chunk j+2 into the GW buffer W^T(j) occupied (read before
                     // OPS(j)); it runs while the chain converts U^T, before MMA2 is issued.
@@ -958,13 +985,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         float S[64];
 #pragma unroll
         for (int m = 0; m < 64; ++m) S[m] = 0.f;
-        if (use_s0 && x < d && 64 * h < d) {
-            const float *src = p.S0 + (static_cast<int64_t>(b) * p.Hv + hv) * d * d + static_cast<int64_t>(64 * h) * d + x;
+        const float *s_in = nullptr;   // state entering this run, [d][d]
+        if (use_s0) s_in = p.S0 + (static_cast<int64_t>(b) * p.Hv + hv) * d * d;
+        if (p.pass == 0 && exact && seg > 0)
+            s_in = p.seg_state + ((static_cast<int64_t>(pr) * p.nseg + seg) * 3 + 2) * d * d;
+        if (s_in && x < d && 64 * h < d) {
+            const float *src = s_in + static_cast<int64_t>(64 * h) * d + x;
 #pragma unroll
             for (int m = 0; m < 64; ++m) {
                 S[m] = __ldg(src);
                 src += d;
             }
+        }
+        if (kind == 1) {
+#pragma unroll
+            for (int m = 0; m < 64; ++m) S[m] = (64 * h + m == x && x < d) ? 1.f : 0.f;
         }
         // j = -1 writes the initial state; j >= 0 processes chunk j and writes the next state.
 #pragma unroll 1
@@ -1039,7 +1074,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             tc_fence_before();
             mbar_arrive(&bars[B_YFREE]);
-            if (c >= c_begin && x < d) {
+            if (c >= c_begin && x < d && p.pass == 0) {
                 const int64_t tstart = static_cast<int64_t>(c) * kC + 32 * h;
                 uint16_t *yp = reinterpret_cast<uint16_t *>(p.y) + ((static_cast<int64_t>(b) * p.T + tstart) * p.Hv + hv) * d + x;
                 const int ystride = p.Hv * d;
@@ -1051,8 +1086,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
         }
-        if (last_seg && !*abort_flag && x < d && 64 * h < d) {
-            float *dst = p.S_T + (static_cast<int64_t>(b) * p.Hv + hv) * d * d + static_cast<int64_t>(64 * h) * d + x;
+        // Where this run's final state goes.  The indices are recomputed from a
+        // fresh read of the block index, so that they are not kept in registers
+        // across the chunk loop above.
+        float *s_out = nullptr;
+        {
+            uint32_t cta;
+            asm volatile("mov.u32 %0, %%ctaid.x;" : "=r"(cta));
+            const uint32_t per_pass = static_cast<uint32_t>(p.B * p.Hv * p.nseg);
+            const int bxr = static_cast<int>(cta % per_pass), pr_r = bxr % (p.B * p.Hv), seg_r = bxr / (p.B * p.Hv);
+            if (p.pass == 1)
+                s_out = p.seg_state + ((static_cast<int64_t>(pr_r) * p.nseg + seg_r) * 3 + cta / per_pass) * d * d;
+            else if (seg_r == p.nseg - 1)
+                s_out = p.S_T + static_cast<int64_t>(pr_r) * d * d;
+        }
+        if (s_out && !*abort_flag && x < d && 64 * h < d) {
+            float *dst = s_out + static_cast<int64_t>(64 * h) * d + x;
 #pragma unroll
             for (int m = 0; m < 64; ++m) {
                 *dst = S[m];
@@ -1074,6 +1123,126 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         tmem_dealloc(tb, 512);
     }
+}
+
+// Which segments have no warm-up window: one CTA (8 warps) per (batch, value
+// head, segment after the first), walking back from the segment start eight
+// chunks per round as the chunk kernel's warm-up search does.  flag[pair][seg]
+// is set when no window of at most max_warmup chunks reaches exp(log_eps)
+// (and token 0 is not reached within the limit); a head with any flag set
+// takes the exact split.
+__global__ void __launch_bounds__(256) segment_plan_kernel(const Dev p, int *flag) {
+    const int pairs = p.B * p.Hv;
+    const int pr = blockIdx.x % pairs, seg = 1 + static_cast<int>(blockIdx.x / pairs);
+    const int b = pr / p.Hv, hv = pr % p.Hv;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int c_begin = seg * p.seg_chunks;
+    __shared__ float wsum[8];
+    __shared__ int verdict;
+    float acc = 0.f;
+    for (int r = 0;; ++r) {
+        const int m = r * 8 + warp + 1;
+        const int cc = c_begin - m;
+        float part = 0.f;
+        if (cc >= 0 && m <= p.max_warmup) {
+            const int64_t t = static_cast<int64_t>(cc) * kC + lane;
+            const float *al = p.alpha + (static_cast<int64_t>(b) * p.T + t) * p.Hv + hv;
+            part = logf(__ldg(al)) + logf(__ldg(al + 32 * static_cast<int64_t>(p.Hv)));
+        }
+        part = warp_sum(part);
+        if (lane == 0) wsum[warp] = part;
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            int v = -1;   // -1 undecided, 0 window found (or token 0 reached), 1 none within the limit
+            for (int w = 0; w < 8 && v < 0; ++w) {
+                const int mm = r * 8 + w + 1;
+                if (mm > p.max_warmup) {
+                    v = 1;
+                    break;
+                }
+                acc += wsum[w];
+                if (acc <= p.log_eps || c_begin - mm == 0) v = 0;
+            }
+            verdict = v;
+        }
+        __syncthreads();
+        const int v = verdict;
+        if (v >= 0) {
+            if (threadIdx.x == 0) flag[static_cast<int64_t>(pr) * p.nseg + seg] = v;
+            return;
+        }
+        __syncthreads();
+    }
+}
+
+// Entering states of the segments of each flagged head: with B_s and M_s the
+// ends of segment s's two transition runs (B_0 from the true initial state),
+// S_1 = B_0 and S_{s+1} = M_s S_s + B_s, each state [d][d] fp32, row-major.
+// One CTA (512 threads) per (batch, value head); S_s and M_s are staged in
+// shared memory; each thread owns one column x and the rows r0 + (512/d) u.
+template <int D>
+__global__ void __launch_bounds__(512) segment_combine_kernel(const int *flag, float *seg_state, int nseg) {
+    extern __shared__ float4 smem4[];
+    float *st = reinterpret_cast<float *>(smem4);   // S_s, D x D
+    float *mt = st + D * D;                         // M_s, D x D
+    const int pr = blockIdx.x;
+    if (!head_needs_split(flag, pr, nseg)) return;
+    constexpr int kRows = D * D / 512;              // rows per thread
+    constexpr int kStep = 512 / D;
+    const int tid = threadIdx.x;
+    const int64_t dd = static_cast<int64_t>(D) * D;
+    float *base = seg_state + static_cast<int64_t>(pr) * nseg * 3 * dd;
+    for (int e = tid; e < D * D; e += 512) st[e] = base[e];   // S_1 = B_0
+    __syncthreads();
+    const int x = tid % D, r0 = tid / D;
+    for (int sgm = 1; sgm < nseg; ++sgm) {
+        float *slot = base + static_cast<int64_t>(sgm) * 3 * dd;
+        for (int e = tid; e < D * D; e += 512) {
+            slot[2 * dd + e] = st[e];   // entering state of segment sgm
+            mt[e] = slot[dd + e];       // M_sgm
+        }
+        if (sgm == nseg - 1) break;
+        __syncthreads();
+        float acc[kRows];
+#pragma unroll
+        for (int u = 0; u < kRows; ++u) acc[u] = slot[static_cast<int64_t>(r0 + kStep * u) * D + x];   // B_sgm
+#pragma unroll 1
+        for (int k = 0; k < D; k += 4) {
+            const float s0 = st[k * D + x], s1 = st[(k + 1) * D + x], s2 = st[(k + 2) * D + x], s3 = st[(k + 3) * D + x];
+#pragma unroll
+            for (int u = 0; u < kRows; ++u) {
+                const float4 m4 = *reinterpret_cast<const float4 *>(mt + (r0 + kStep * u) * D + k);
+                acc[u] = fmaf(m4.x, s0, fmaf(m4.y, s1, fmaf(m4.z, s2, fmaf(m4.w, s3, acc[u]))));
+            }
+        }
+        __syncthreads();
+#pragma unroll
+        for (int u = 0; u < kRows; ++u) st[(r0 + kStep * u) * D + x] = acc[u];
+        __syncthreads();
+    }
+}
+
+// Dynamic shared memory limits of the kernels above, set once per device.
+cudaError_t set_smem_attributes() {
+    constexpr int kMaxDevices = 64;
+    static std::once_flag once[kMaxDevices];
+    static cudaError_t result[kMaxDevices];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::call_once(once[dev], [dev] {
+        cudaError_t r = cudaFuncSetAttribute(gdn_chunked_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(kSmemBytes));
+        if (r == cudaSuccess)
+            r = cudaFuncSetAttribute(segment_combine_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     2 * 128 * 128 * 4);
+        if (r == cudaSuccess)
+            r = cudaFuncSetAttribute(segment_combine_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     2 * 64 * 64 * 4);
+        result[dev] = r;
+    });
+    return result[dev];
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 get_encoder() {
@@ -1132,6 +1301,13 @@ int plan_segments(int64_t pairs, int64_t nchunks, int num_sms, int requested) {
     return best;
 }
 
+bool takes_exact_split(int64_t pairs, int64_t nchunks, int P, int d, size_t seg_state_bytes) {
+    // Only for long sequences: below kExactSplitMinChunks chunks per head a
+    // restart from token 0 costs less than the split's three extra launches.
+    const size_t need = static_cast<size_t>(pairs) * P * 3 * d * d * sizeof(float);
+    return P > 1 && nchunks >= kExactSplitMinChunks && need <= seg_state_bytes;
+}
+
 cudaError_t launch_chunked(const ChunkedParams &p, cudaStream_t stream, int num_sms) {
     if (p.d != 64 && p.d != 128) return cudaErrorInvalidValue;
     if (p.T > 0xffffffffLL || p.B > 0x7fffffffLL) return cudaErrorInvalidValue;
@@ -1170,9 +1346,31 @@ cudaError_t launch_chunked(const ChunkedParams &p, cudaStream_t stream, int num_
     dv.S_T = p.S_T;
     dv.status = p.status;
 
-    cudaError_t e = cudaFuncSetAttribute(gdn_chunked_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(kSmemBytes));
+    dv.pass = 0;
+    dv.exact_flag = nullptr;
+    dv.seg_state = nullptr;
+
+    cudaError_t e = set_smem_attributes();
     if (e != cudaSuccess) return e;
+    // Exact sequence split, for the heads whose gates do not decay within the
+    // warm-up limit: each segment is an affine map of its entering state, so its
+    // two transition runs and a short combine give every segment its exact start.
+    // Heads that do not need it leave the extra passes at once.
+    if (p.exact_flag && p.seg_state && takes_exact_split(pairs, nchunks, P, p.d, p.seg_state_bytes)) {
+        dv.exact_flag = p.exact_flag;
+        dv.seg_state = p.seg_state;
+        segment_plan_kernel<<<static_cast<unsigned>(pairs * (P - 1)), 256, 0, stream>>>(dv, p.exact_flag);
+        dv.pass = 1;
+        gdn_chunked_kernel<<<static_cast<unsigned>(2 * grid), kThreads, kSmemBytes, stream>>>(mq, mk, mv, dv);
+        const size_t comb_smem = 2 * static_cast<size_t>(p.d) * p.d * sizeof(float);
+        if (p.d == 128)
+            segment_combine_kernel<128><<<static_cast<unsigned>(pairs), 512, comb_smem, stream>>>(p.exact_flag,
+                                                                                                 p.seg_state, P);
+        else
+            segment_combine_kernel<64><<<static_cast<unsigned>(pairs), 512, comb_smem, stream>>>(p.exact_flag,
+                                                                                                p.seg_state, P);
+        dv.pass = 0;
+    }
     gdn_chunked_kernel<<<static_cast<unsigned>(grid), kThreads, kSmemBytes, stream>>>(mq, mk, mv, dv);
     return cudaGetLastError();
 }

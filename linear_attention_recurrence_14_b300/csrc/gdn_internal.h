@@ -42,11 +42,29 @@ struct ChunkedParams {
     float log_eps;
     int max_warmup_chunks;
     int test_stall_chunk;        // > 0: never load this chunk (fault-injection test hook)
+    // Exact sequence split (workspace, optional): per-head flags and the
+    // segments' transition and entering states; used when P * pairs * 3 * d * d
+    // floats fit in seg_state_bytes.
+    int *exact_flag;             // [B * Hv][segments]: segment has no warm-up window
+    float *seg_state;            // [B * Hv][segments][3][d][d]
+    size_t seg_state_bytes;
 };
+
+// Segment count bound for which gdn_prefill_workspace_bytes reserves the
+// exact-split states: segments * B * Hv stays within about two waves of a
+// GPU with up to this many SMs.
+constexpr int kExactSplitSmBound = 160;
+// Sequences of fewer chunks (of 64 tokens) per head never take the exact split.
+constexpr int kExactSplitMinChunks = 256;
 
 // Number of sequence segments per (batch, value head) the chunked prefill uses
 // (requested > 0 is taken as is, capped at the chunk count).
 int plan_segments(int64_t pairs, int64_t nchunks, int num_sms, int requested);
+
+// Whether a chunked prefill of P segments per head takes the exact sequence
+// split (plan, transition pass, combine, then the output pass: four launches
+// instead of one), given segment-state room of seg_state_bytes.
+bool takes_exact_split(int64_t pairs, int64_t nchunks, int P, int d, size_t seg_state_bytes);
 
 // Chunked tensor-core prefill (bf16).  Builds the TMA descriptors and launches.
 cudaError_t launch_chunked(const ChunkedParams &p, cudaStream_t stream, int num_sms);

@@ -29,7 +29,7 @@ EXPORTS = ("gdn_status_string", "gdn_prefill_workspace_bytes", "gdn_prefill", "g
            "gdn_decode_step", "gdn_read_device_status", "gdn_device_supported", "gdn_abi_version",
            "gdn_prefill_noalloc", "gdn_layer_prologue", "gdn_layer_epilogue", "gdn_prefill_host_workspace_bytes",
            "gdn_prefill_host", "gdn_prefill_cw", "gdn_decode_step_cw", "gdn_backward_workspace_bytes",
-           "gdn_backward", "gdn_prefill_noalloc_status")
+           "gdn_backward", "gdn_prefill_noalloc_status", "gdn_prefill_launches")
 NOALLOC_SCRATCH_BYTES = 256 + 8 * 1024 * 1024
 
 
@@ -79,6 +79,8 @@ def lib() -> ctypes.CDLL:
             L.gdn_status_string.argtypes = [ctypes.c_int]
             L.gdn_prefill_workspace_bytes.restype = c_size
             L.gdn_prefill_workspace_bytes.argtypes = [sp]
+            L.gdn_prefill_launches.restype = ctypes.c_int
+            L.gdn_prefill_launches.argtypes = [sp, ctypes.POINTER(GdnPrefillOptions)]
             L.gdn_prefill.restype = ctypes.c_int
             L.gdn_prefill.argtypes = [sp, vp, vp, vp, fp, fp, fp, vp, fp, vp, c_size, vp]
             L.gdn_prefill_ex.restype = ctypes.c_int
@@ -401,8 +403,13 @@ def backward_launches(shape: GdnShape) -> int:
 
 
 def prefill_launches(shape: GdnShape, algorithm=ALGO_AUTO, segments=0) -> int:
-    """Kernel launches one gdn_prefill call enqueues for this shape (both paths launch one kernel)."""
-    return 1 if shape.B * shape.T * shape.Hv > 0 else 0
+    """Kernels one gdn_prefill call enqueues for this shape with a full workspace
+    (gdn_prefill_launches: 4 with the exact sequence split, else 1; 0 when empty)."""
+    opts = GdnPrefillOptions(segments, 0.0, 0, algorithm, 0)
+    n = lib().gdn_prefill_launches(ctypes.byref(shape), ctypes.byref(opts))
+    if n < 0:
+        raise GdnError(GDN_ERR_INVALID_ARG, "gdn_prefill_launches")
+    return n
 
 
 def read_device_status(workspace, stream=None) -> int:

@@ -45,8 +45,15 @@ def shape(B=1, T=64, Hqk=2, Hv=4, d=128, dtype=gdn.GDN_BF16):
 
 
 def test_workspace_bytes(L):
-    s = shape(B=2, Hv=4, d=128)
+    s = shape(B=2, Hv=4, d=128)   # one chunk: status and staging only
     assert gdn.workspace_bytes(s) == 256 + 2 * 4 * 128 * 128 * 4
+    # several chunks (bf16): the exact sequence split's segment flags and states, for at
+    # most ceil(320 / (B * Hv)) segments (about two waves of a GPU of up to 160 SMs)
+    r = lambda n: (n + 255) // 256 * 256  # noqa: E731
+    s = shape(B=2, T=64 * 100, Hv=4, d=128)
+    assert gdn.workspace_bytes(s) == r(256 + 8 * 128 * 128 * 4) + r(8 * 40 * 4) + 8 * 40 * 3 * 128 * 128 * 4
+    s = shape(B=2, T=64 * 100, Hv=4, d=128, dtype=gdn.GDN_F32)
+    assert gdn.workspace_bytes(s) == 256 + 8 * 128 * 128 * 4
     assert gdn.workspace_bytes(shape(Hqk=3, Hv=4)) == 0
     assert L.gdn_prefill_workspace_bytes(None) == 0
 
@@ -163,7 +170,9 @@ def test_host_prefill_workspace_and_arguments(L):
     s = shape(B=2, T=1000, Hqk=2, Hv=4, d=128)
     # pieces of 256 tokens: prefill workspace, two states, two slots of (q, k, v, y, alpha, beta)
     r = lambda n: (n + 255) // 256 * 256  # noqa: E731
-    inner = r(256 + 2 * 4 * 128 * 128 * 4)
+    # gdn_prefill's workspace for one piece: status, staging, and the exact split's segment flags
+    # and segment states (4 chunks: 4 segments x 8 heads x 3 states of 128 x 128 fp32)
+    inner = r(r(256 + 2 * 4 * 128 * 128 * 4) + r(8 * 4 * 4) + 8 * 4 * 3 * 128 * 128 * 4)
     state = r(2 * 4 * 128 * 128 * 4)
     slot = 2 * r(2 * 256 * 2 * 128 * 2) + 2 * r(2 * 256 * 4 * 128 * 2) + 2 * r(2 * 256 * 4 * 4)
     assert gdn.host_workspace_bytes(s, 256) == inner + 2 * state + 2 * slot

@@ -178,3 +178,61 @@ def test_chunked_matches_sequential_kernel_and_decode():
     assert rel_err(yd, ref) <= 1e-2
     assert rel_err(Sc, Ss.double().cpu().numpy()) <= BF16_TOL
     assert rel_err(S, Ss.double().cpu().numpy()) <= 1e-3
+
+
+# ----------------------------------------------------------------------------
+# Exact sequence split.  When a segment's preceding tokens do not forget the
+# state within the warm-up limit (gates at or near 1), every segment is an
+# affine map of its entering state (the reading notes' transition form,
+# S_t = alpha_t (I - beta_t k_t k_t^T) S_{t-1} + beta_t k_t v_t^T, composed over the
+# segment): its two transition runs (from zero with the values, from the
+# identity without them) and a short combine give each segment its exact start.
+# The split is taken from 256 chunks of 64 tokens per sequence up; shorter
+# sequences restart such segments from token 0.
+
+def _oracle_check(x, y, S_T):
+    yo, So = oracle.recurrence(x.q, x.k, x.v, x.alpha, x.beta, x.S0)
+    assert rel_err(y, yo) <= BF16_TOL
+    assert rel_err(S_T, So) <= BF16_TOL
+
+
+@pytest.mark.parametrize("segments", [3, 7])
+@pytest.mark.parametrize("decay", [1.2e-4, 0.0])   # alpha ~ 1 - 1e-4, and alpha == 1 exactly
+def test_exact_split_for_gates_that_do_not_decay(segments, decay):
+    x = make_prefill_inputs(1, 64 * 256 + 5, 2, 4, 128, "bf16", decay_scale=decay, s0_std=0.02, seed=53, device="cuda")
+    y, S_T = _chunked(x, segments=segments)
+    _oracle_check(x, y, S_T)
+
+
+def test_exact_split_mixed_heads_and_in_place_state():
+    # Per head: strong decay (windows exist, no split) and no decay (split) in one call,
+    # grouped value heads, a ragged tail, d = 64, and S_T written in place over S0.
+    x = make_prefill_inputs(2, 64 * 256 + 17, 1, 4, 64, "bf16", decay_scale=0.05, s0_std=0.05, seed=59, device="cuda")
+    x.alpha[:, :, 1] = 1.0
+    x.alpha[:, :, 3] = 1.0 - 1e-5
+    xr = make_prefill_inputs(2, 64 * 256 + 17, 1, 4, 64, "bf16", decay_scale=0.05, s0_std=0.05, seed=59, device="cuda")
+    xr.alpha.copy_(x.alpha)
+    S = x.S0.clone()
+    ws = gdn.new_workspace(gdn.shape_of(x.q, x.v), "cuda")
+    y, S_T = gdn.prefill(x.q, x.k, x.v, x.alpha, x.beta, S, S_T=S, workspace=ws, algorithm=gdn.ALGO_CHUNKED,
+                         segments=5)
+    assert gdn.read_device_status(ws) == 0
+    assert S_T.data_ptr() == S.data_ptr()
+    _oracle_check(xr, y, S_T)
+
+
+def test_exact_split_matches_the_single_pass():
+    # The split must agree with one sequential pass of the same kernel (segments = 1)
+    # far more closely than with the oracle: only the rounding order differs.
+    x = make_prefill_inputs(1, 64 * 260, 1, 2, 128, "bf16", decay_scale=0.0, s0_std=0.02, seed=61, device="cuda")
+    y1, S1 = _chunked(x, segments=1)
+    y9, S9 = _chunked(x, segments=9)
+    assert rel_err(y9, y1.double().cpu().numpy()) <= BF16_TOL
+    assert rel_err(S9, S1.double().cpu().numpy()) <= BF16_TOL
+
+
+def test_short_sequence_restarts_instead_of_splitting():
+    # Below 256 chunks a segment without a window restarts from token 0: still exact.
+    x = make_prefill_inputs(1, 64 * 40 + 5, 2, 4, 128, "bf16", decay_scale=0.0, s0_std=0.02, seed=67, device="cuda")
+    y, S_T = _chunked(x, segments=5)
+    _oracle_check(x, y, S_T)
