@@ -87,19 +87,21 @@ def test_backward_is_deterministic_and_satisfies_linearity_identities():
     assert abs(float((a["dq"].double() * x.q.double()).sum()) - ydy) <= 1e-4 * max(1.0, abs(ydy))
 
 
-def test_backward_training_shape_sampled_head():
-    # B=2, H=16, T=4096, d=128, bf16: the whole shape runs; one (batch, head) is checked against the oracle.
+def test_backward_training_shape_sampled_heads():
+    # B=2, H=16, T=4096, d=128, bf16: the whole shape runs; eight (batch, head) pairs
+    # spread over both sequences, including the first and the last head, are checked
+    # against the oracle.
     x = workload_inputs("train", seed=0, device="cuda")
     g = make_backward_grads(2, 4096, 16, 128, "bf16", ds_std=1.0, seed=0, device="cuda")
     out = gdn.backward(x.q, x.k, x.v, x.alpha, x.beta, x.S0, g.dy, g.dS_T)
     torch.cuda.synchronize()
-    b, h = 1, 5
-    sl = lambda t: None if t is None else t[b:b + 1, :, h:h + 1].contiguous()  # noqa: E731
-    ref = obw.recurrence_grad(sl(x.q), sl(x.k), sl(x.v), sl(x.alpha), sl(x.beta), None, sl(g.dy),
-                              g.dS_T[b:b + 1, h:h + 1])
-    ref["dlog_alpha"] = sl(x.alpha).double().cpu().numpy() * ref["dalpha"]
-    got = {n: sl(out[n]) for n in ("dq", "dk", "dv", "dlog_alpha", "dbeta")}
-    got["dS0"] = out["dS0"][b:b + 1, h:h + 1]
-    _check(got, ref)
     for n in ("dq", "dk", "dv", "dlog_alpha", "dbeta", "dS0"):
         assert torch.isfinite(out[n]).all(), n
+    for b, heads in ((0, [0, 5, 10, 15]), (1, [2, 7, 12, 15])):
+        sl = lambda t: t[b:b + 1, :, heads].contiguous()  # noqa: E731
+        ref = obw.recurrence_grad(sl(x.q), sl(x.k), sl(x.v), sl(x.alpha), sl(x.beta), None, sl(g.dy),
+                                  g.dS_T[b:b + 1, heads])
+        ref["dlog_alpha"] = sl(x.alpha).double().cpu().numpy() * ref["dalpha"]
+        got = {n: sl(out[n]) for n in ("dq", "dk", "dv", "dlog_alpha", "dbeta")}
+        got["dS0"] = out["dS0"][b:b + 1, heads]
+        _check(got, ref)
