@@ -11,6 +11,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <mutex>
 
 #include "gdn_internal.h"
 #include "gdn_layer.h"
@@ -33,194 +34,286 @@ __device__ __forceinline__ float warp_allsum(float v) {
 // otherwise limited by these per-element instructions, not by HBM.
 __device__ __forceinline__ float sigmoidf_(float u) { return __fdividef(1.f, 1.f + __expf(-u)); }
 
+// The PTX approximate instructions with denormals flushed to zero (no
+// denormal fix-up code around them): 2^x, 1/x and 1/sqrt(x).
+__device__ __forceinline__ float ex2_ftz(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+__device__ __forceinline__ float rcp_ftz(float x) {
+    float y;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+__device__ __forceinline__ float rsqrt_ftz(float x) {
+    float y;
+    asm("rsqrt.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// sigma(u) = 1 / (1 + 2^(-u log2 e)) from those instructions: for very
+// negative u the power overflows to +inf and sigma is 0; for very positive u
+// it flushes to 0 and sigma is 1.
+__device__ __forceinline__ float sigmoid_ftz(float u) {
+    constexpr float kLog2e = 1.4426950408889634f;
+    return rcp_ftz(1.f + ex2_ftz(-kLog2e * u));
+}
+
 // log(1 + e^u), stable for either sign of u.
 __device__ __forceinline__ float softplusf_(float u) { return fmaxf(u, 0.f) + log1pf(__expf(-fabsf(u))); }
 
-// CPL consecutive bf16 channels <-> floats (CPL = 2: one 32-bit word; 4: two).
-template <int CPL>
-__device__ __forceinline__ void load_bf16(const __nv_bfloat16 *p, float (&f)[CPL]) {
-    // read-only path (the inputs never alias the outputs), so loads may be
-    // issued ahead of earlier stores
-    if constexpr (CPL == 4) {
-        const uint2 r = __ldg(reinterpret_cast<const uint2 *>(p));
-        const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&r.x));
-        const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&r.y));
-        f[0] = a.x; f[1] = a.y; f[2] = b.x; f[3] = b.y;
-    } else {
-        const unsigned int r = __ldg(reinterpret_cast<const unsigned int *>(p));
-        const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&r));
-        f[0] = a.x; f[1] = a.y;
-    }
-}
-
-template <int CPL>
-struct RawOf {
-    using type = uint32_t;
-};
-template <>
-struct RawOf<4> {
-    using type = uint2;
-};
-
-// CPL bf16 channels from shared memory.
-template <int CPL>
-__device__ __forceinline__ void load_smem(const __nv_bfloat16 *p, float (&f)[CPL]) {
-    const typename RawOf<CPL>::type r = *reinterpret_cast<const typename RawOf<CPL>::type *>(p);
-    const __nv_bfloat162 *h2 = reinterpret_cast<const __nv_bfloat162 *>(&r);
+// Eight bf16 channels (one 16-byte word) -> floats.
+__device__ __forceinline__ void unpack8(const uint4 &r, float (&f)[8]) {
+    const uint32_t w[4] = {r.x, r.y, r.z, r.w};
 #pragma unroll
-    for (int e = 0; e < CPL / 2; ++e) {
-        const float2 a = __bfloat1622float2(h2[e]);
-        f[2 * e] = a.x;
-        f[2 * e + 1] = a.y;
+    for (int e = 0; e < 4; ++e) {
+        f[2 * e] = __uint_as_float(w[e] << 16);
+        f[2 * e + 1] = __uint_as_float(w[e] & 0xffff0000u);
     }
 }
 
-template <int CPL>
-__device__ __forceinline__ void store_bf16(__nv_bfloat16 *p, const float (&f)[CPL]) {
-    if constexpr (CPL == 4) {
-        const __nv_bfloat162 a = __floats2bfloat162_rn(f[0], f[1]), b = __floats2bfloat162_rn(f[2], f[3]);
-        uint2 r;
-        r.x = *reinterpret_cast<const uint32_t *>(&a);
-        r.y = *reinterpret_cast<const uint32_t *>(&b);
-        *reinterpret_cast<uint2 *>(p) = r;
-    } else {
-        *reinterpret_cast<__nv_bfloat162 *>(p) = __floats2bfloat162_rn(f[0], f[1]);
+// Eight floats -> bf16 (round to nearest even), one 16-byte word.
+__device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
+    uint32_t w[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        const __nv_bfloat162 h = __floats2bfloat162_rn(f[2 * e], f[2 * e + 1]);
+        w[e] = *reinterpret_cast<const uint32_t *>(&h);
     }
+    return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
 struct ProloguePlan {
     int64_t B, T;
     int Hqk, Hv, d, kconv, ntiles;
+    int gq, gv, ngroups;   // head groups of q (and of k), of v, and their sum
+    int64_t items;         // B * ntiles * ngroups
     gdn_prologue_io io;
 };
 
-// One CTA (4 warps): one (batch, head) row of one of q, k, v over a tile of
-// kTile tokens.  The tile's input rows, with kMaxConv-1 rows of history in
-// front, are first copied into shared memory with asynchronous 16-byte copies
-// (all in flight at once: the kernel is HBM-bound, not latency-bound); then
-// each warp computes kTile/4 tokens from shared memory, one row per step, and
-// stores its rows straight to global memory.  CTAs are ordered by memory
-// (consecutive CTAs take consecutive heads of one tile).
-constexpr int kHalo = kMaxConv - 1;
+constexpr int kWarps = 8;   // prologue warps per CTA
+constexpr int kRing = 24;   // input rows in flight per lane (a multiple of 4)
+constexpr size_t kPrologueSmem = static_cast<size_t>(kWarps) * kRing * 32 * sizeof(uint4);
 
 __device__ __forceinline__ void cp_async16(void *smem, const void *gmem) {
     const uint32_t sa = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(sa), "l"(gmem) : "memory");
 }
 
-__device__ __forceinline__ void cp_async_wait_all() {
-    asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
-template <int CPL>
-__global__ void __launch_bounds__(128) prologue_kernel(ProloguePlan p) {
-    extern __shared__ __align__(16) unsigned char smem_raw[];
-    __nv_bfloat16 *rows = reinterpret_cast<__nv_bfloat16 *>(smem_raw);   // [kHalo + kTile][d]
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int64_t job = blockIdx.x;
-    const int nrows = 2 * p.Hqk + p.Hv;
-    const int row = static_cast<int>(job % nrows);
-    const int tile = static_cast<int>((job / nrows) % p.ntiles);
-    const int64_t b = job / (static_cast<int64_t>(p.ntiles) * nrows);
-    const int which = row < p.Hqk ? 0 : (row < 2 * p.Hqk ? 1 : 2);   // q, k, v
-    const int h = which == 0 ? row : (which == 1 ? row - p.Hqk : row - 2 * p.Hqk);
-    const int H = which == 2 ? p.Hv : p.Hqk;
-    const int d = p.d, K = p.kconv;
-    const int64_t C = static_cast<int64_t>(H) * d;
-    const __nv_bfloat16 *x = static_cast<const __nv_bfloat16 *>(which == 0 ? p.io.xq : which == 1 ? p.io.xk : p.io.xv);
-    const float *w = which == 0 ? p.io.wq : which == 1 ? p.io.wk : p.io.wv;
-    const __nv_bfloat16 *sin = static_cast<const __nv_bfloat16 *>(
-        which == 0 ? p.io.state_q_in : which == 1 ? p.io.state_k_in : p.io.state_v_in);
-    __nv_bfloat16 *sout = static_cast<__nv_bfloat16 *>(
-        which == 0 ? p.io.state_q_out : which == 1 ? p.io.state_k_out : p.io.state_v_out);
-    __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(which == 0 ? p.io.q : which == 1 ? p.io.k : p.io.v);
-    const int64_t t0 = static_cast<int64_t>(tile) * kTile;
-    const int64_t t1 = t0 + kTile < p.T ? t0 + kTile : p.T;
-    const int nr = static_cast<int>(t1 - t0) + kHalo;   // rows in shared memory: tokens t0-kHalo .. t1-1
-
-    // Stage the rows: 16-byte pieces, d/8 per row.
-    const int per_row = d / 8;
-    for (int idx = tid; idx < nr * per_row; idx += 128) {
-        const int i = idx / per_row, c = idx % per_row;
-        const int64_t t = t0 - kHalo + i;
-        __nv_bfloat16 *dst = rows + i * d + c * 8;
-        const int64_t off = static_cast<int64_t>(h) * d + c * 8;
-        if (t >= 0) {
-            cp_async16(dst, x + (b * p.T + t) * C + off);
-        } else if (sin && t >= -(K - 1)) {
-            *reinterpret_cast<uint4 *>(dst) = *reinterpret_cast<const uint4 *>(sin + (b * (K - 1) + (K - 1 + t)) * C + off);
-        } else {
-            *reinterpret_cast<uint4 *>(dst) = make_uint4(0u, 0u, 0u, 0u);
-        }
+// One token of the prologue for this lane's eight channels: the new input row
+// goes into ring slot S (token mod 4); the convolution reads the three
+// previous rows from the other slots; then SiLU, the L2 norm over the head
+// (a sum over the LPR lanes of the head) when NORM, and the bf16 store.
+template <int LPR, int S, bool NORM>
+__device__ __forceinline__ void prologue_token(float (&ring)[4][8], const float (&tap)[kMaxConv][8], const uint4 &raw,
+                                               bool store, __nv_bfloat16 *dst) {
+    float cur[8], u[8];
+    unpack8(raw, cur);
+    float ss = 0.f;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+        float a = tap[0][e] * cur[e];
+        a = fmaf(tap[1][e], ring[(S + 3) & 3][e], a);
+        a = fmaf(tap[2][e], ring[(S + 2) & 3][e], a);
+        a = fmaf(tap[3][e], ring[(S + 1) & 3][e], a);
+        ring[S][e] = cur[e];
+        u[e] = a * sigmoid_ftz(a);
+        if constexpr (NORM) ss = fmaf(u[e], u[e], ss);
     }
-    cp_async_wait_all();
-    __syncthreads();
-
-    const int64_t ch = static_cast<int64_t>(h) * d + lane * CPL;   // first channel of this lane
-    const int cl = lane * CPL;                                      // ... within the head
-    // back[e][j]: the tap applied to the input j tokens back (0 = current; 0 beyond K)
-    float back[CPL][kMaxConv];
+    if constexpr (NORM) {
 #pragma unroll
-    for (int e = 0; e < CPL; ++e)
+        for (int o = LPR / 2; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+        const float inv = rsqrt_ftz(ss + kL2Eps);
 #pragma unroll
-        for (int j = 0; j < kMaxConv; ++j) back[e][j] = (j < K && t1 > t0) ? w[(ch + e) * K + (K - 1 - j)] : 0.f;
-    const bool normalise = which < 2;
-    constexpr int kPerWarp = kTile / 4;
-    const int64_t ta = t0 + warp * kPerWarp;
-    const int64_t tb = ta + kPerWarp < t1 ? ta + kPerWarp : t1;
-    // win[j][e]: the input j+1 tokens back; one shared-memory row read per token
-    float win[kMaxConv - 1][CPL];
-    if (ta < tb) {
-#pragma unroll
-        for (int j = 0; j < kMaxConv - 1; ++j) load_smem<CPL>(rows + (static_cast<int>(ta - t0) + kHalo - 1 - j) * d + cl, win[j]);
+        for (int e = 0; e < 8; ++e) u[e] *= inv;
     }
+    if (store) *reinterpret_cast<uint4 *>(dst) = pack8(u);
+}
+
+// The first kRing - 4 input rows of a tile for one lane, in commit groups of
+// four rows (rows past n are not copied), issued before the item's other
+// loads so that their latency overlaps them.
+__device__ __forceinline__ void prologue_start(uint4 *lane_ring, const __nv_bfloat16 *xp, int rs, int n) {
+#pragma unroll
+    for (int g0 = 0; g0 < kRing - 4; g0 += 4) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            if (g0 + i < n) cp_async16(lane_ring + (g0 + i) * 32, xp + static_cast<int64_t>(g0 + i) * rs);
+        cp_async_commit();
+    }
+}
+
+// The rows of one tile for one lane, four tokens per step.  The lane streams
+// its own 16 bytes of every input row through a private ring of kRing rows
+// in shared memory (asynchronous copies, one commit group per four rows),
+// kRing - 4 rows ahead of the rows it computes.  n: tokens this lane loads
+// and stores (0 for an idle lane); len: tokens of the tile (the same for the
+// whole warp, so the shuffles of the L2 norm see every lane).  FULL: a whole
+// tile (len == n == kTile), taken with one check per group of four rows (the
+// groups fetched ahead of the tile's end are not copied: they may lie past
+// the end of the sequence).
+template <int LPR, bool NORM, bool FULL>
+__device__ __forceinline__ void prologue_rows(float (&ring)[4][8], const float (&tap)[kMaxConv][8], uint4 *lane_ring,
+                                              const __nv_bfloat16 *xp, __nv_bfloat16 *op, int rs, int n, int len) {
+    const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
+    const int64_t rs1 = rs;
+    // rows 0 .. kRing-5 were issued by prologue_start
+    const __nv_bfloat16 *src = xp + (kRing - 4) * rs1;   // next row to copy
+    int wslot = kRing - 4;                               // its ring slot (a multiple of 4)
+    auto issue = [&](int i0) {       // rows i0 .. i0+3 of the tile, one commit group
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            if (FULL ? i0 < kTile : i0 + i < n) cp_async16(lane_ring + (wslot + i) * 32, src + i * rs1);
+        cp_async_commit();
+        src += 4 * rs1;
+        wslot = wslot + 4 == kRing ? 0 : wslot + 4;
+    };
+    int rslot = 0;                   // ring slot of the rows computed next
+    __nv_bfloat16 *o = op;
 #pragma unroll 1
-    for (int64_t t = ta; t < tb; ++t) {
-        const int i = static_cast<int>(t - t0) + kHalo;
-        float u[CPL];
-        float acc[CPL], cur[CPL];
-        load_smem<CPL>(rows + i * d + cl, cur);
+    for (int i0 = 0; i0 < (FULL ? kTile : len); i0 += 4) {
+        issue(i0 + kRing - 4);
+        cp_async_wait<kRing / 4 - 1>();   // rows i0 .. i0+3 have landed
+        uint4 cur[4];
 #pragma unroll
-        for (int e = 0; e < CPL; ++e) {
-            acc[e] = back[e][0] * cur[e];
-#pragma unroll
-            for (int j = 0; j < kMaxConv - 1; ++j) acc[e] = fmaf(back[e][j + 1], win[j][e], acc[e]);
-        }
-#pragma unroll
-        for (int j = kMaxConv - 2; j > 0; --j)
-#pragma unroll
-            for (int e = 0; e < CPL; ++e) win[j][e] = win[j - 1][e];
-#pragma unroll
-        for (int e = 0; e < CPL; ++e) win[0][e] = cur[e];
-        float ss = 0.f;
-#pragma unroll
-        for (int e = 0; e < CPL; ++e) {
-            u[e] = acc[e] * sigmoidf_(acc[e]);
-            ss = fmaf(u[e], u[e], ss);
-        }
-        if (normalise) {
-            const float inv = rsqrtf(warp_allsum(ss) + kL2Eps);
-#pragma unroll
-            for (int e = 0; e < CPL; ++e) u[e] *= inv;
-        }
-        store_bf16<CPL>(out + ((b * p.T + t) * C + ch), u);
+        for (int i = 0; i < 4; ++i) cur[i] = (FULL || i0 + i < n) ? lane_ring[(rslot + i) * 32] : zero;
+        prologue_token<LPR, 0, NORM>(ring, tap, cur[0], FULL || i0 < n, o);
+        prologue_token<LPR, 1, NORM>(ring, tap, cur[1], FULL || i0 + 1 < n, o + rs1);
+        prologue_token<LPR, 2, NORM>(ring, tap, cur[2], FULL || i0 + 2 < n, o + 2 * rs1);
+        prologue_token<LPR, 3, NORM>(ring, tap, cur[3], FULL || i0 + 3 < n, o + 3 * rs1);
+        o += 4 * rs1;
+        rslot = rslot + 4 == kRing ? 0 : rslot + 4;
     }
-    if (sout && t1 >= p.T && warp == 0) {
-        // the last K-1 inputs of the sequence, oldest first
-        for (int j = 0; j < K - 1; ++j) {
-            const int i = nr - (K - 1) + j;
-            *reinterpret_cast<typename RawOf<CPL>::type *>(sout + (b * (K - 1) + j) * C + ch) =
-                *reinterpret_cast<const typename RawOf<CPL>::type *>(rows + i * d + cl);
+    cp_async_wait<0>();
+}
+
+// One warp per item: a tile of kTile tokens of one group of adjacent heads of
+// one of q, k, v.  LPR = d/8 lanes cover a head (8 channels and one 16-byte
+// load per lane per token), so a warp covers 32/LPR heads, which lie next to
+// each other in memory: every token row of the group is one contiguous
+// 512-byte access.  The convolution window lives in registers as a ring of
+// four token rows indexed by token mod 4, so the taps never move data; the
+// next four input rows are loaded while the current four are computed.
+// Items are handed out in memory order (heads, then tiles, then batches) by
+// a grid-stride loop over a grid of two CTAs per SM.
+template <int LPR>
+__global__ void __launch_bounds__(kWarps * 32, 2) prologue_kernel(ProloguePlan p) {
+    constexpr int HPW = 32 / LPR;
+    const int lane = threadIdx.x & 31;
+    const int sub = lane / LPR;           // head within the group
+    const int c0 = (lane % LPR) * 8;      // first channel of this lane within its head
+    const int d = p.d, K = p.kconv;
+    const int64_t nwarps = static_cast<int64_t>(gridDim.x) * kWarps;
+    const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
+    extern __shared__ uint4 prologue_ring[];
+    // this lane's ring: row slot r at lane_ring[r * 32]
+    uint4 *lane_ring = prologue_ring + (threadIdx.x >> 5) * kRing * 32 + lane;
+
+#pragma unroll 1
+    for (int64_t item = static_cast<int64_t>(blockIdx.x) * kWarps + (threadIdx.x >> 5); item < p.items;
+         item += nwarps) {
+        const int grp = static_cast<int>(item % p.ngroups);
+        const int64_t rest = item / p.ngroups;
+        const int tile = static_cast<int>(rest % p.ntiles);
+        const int64_t b = rest / p.ntiles;
+        const int which = grp < p.gq ? 0 : (grp < 2 * p.gq ? 1 : 2);   // q, k, v
+        const int g = which == 0 ? grp : (which == 1 ? grp - p.gq : grp - 2 * p.gq);
+        const int H = which == 2 ? p.Hv : p.Hqk;
+        const int h = g * HPW + sub;
+        const bool on = h < H;   // lanes past the last head of a partial group stay idle
+        const __nv_bfloat16 *x =
+            static_cast<const __nv_bfloat16 *>(which == 0 ? p.io.xq : which == 1 ? p.io.xk : p.io.xv);
+        const float *w = which == 0 ? p.io.wq : which == 1 ? p.io.wk : p.io.wv;
+        const __nv_bfloat16 *sin = static_cast<const __nv_bfloat16 *>(
+            which == 0 ? p.io.state_q_in : which == 1 ? p.io.state_k_in : p.io.state_v_in);
+        __nv_bfloat16 *sout = static_cast<__nv_bfloat16 *>(
+            which == 0 ? p.io.state_q_out : which == 1 ? p.io.state_k_out : p.io.state_v_out);
+        __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(which == 0 ? p.io.q : which == 1 ? p.io.k : p.io.v);
+        const int64_t rowstride = static_cast<int64_t>(H) * d;          // elements between tokens
+        const int64_t col = static_cast<int64_t>(h) * d + c0;            // this lane's channels in a row
+        const int64_t ta = static_cast<int64_t>(tile) * kTile;
+        const int64_t tb = ta + kTile < p.T ? ta + kTile : p.T;
+        const __nv_bfloat16 *xb = x + b * p.T * rowstride + col;
+        __nv_bfloat16 *ob = out + b * p.T * rowstride + col;
+
+        // Input row of token t (t may lie before the sequence: the convolution
+        // state, else zeros).
+        auto row_at = [&](int64_t t) -> uint4 {
+            if (!on) return zero;
+            if (t >= 0) return __ldg(reinterpret_cast<const uint4 *>(xb + t * rowstride));
+            if (sin && t >= -(K - 1))
+                return *reinterpret_cast<const uint4 *>(sin + (b * (K - 1) + (K - 1 + t)) * rowstride + col);
+            return zero;
+        };
+
+        // Start streaming the tile's rows.  n: tokens of the tile this lane
+        // loads and stores (0 for an idle lane).
+        const int len = static_cast<int>(tb - ta);
+        const int n = on ? len : 0;
+        const int rs = static_cast<int>(rowstride);
+        const __nv_bfloat16 *xp = xb + ta * rowstride;
+        __nv_bfloat16 *op = ob + ta * rowstride;
+        prologue_start(lane_ring, xp, rs, n);
+
+        if (which == 2) {
+            // decay and write gates of this group's value heads over the tile
+            const float *A = p.io.A, *ba = p.io.b_alpha;
+            for (int idx = lane; idx < len * HPW; idx += 32) {
+                const int64_t t = ta + idx / HPW;
+                const int hh = g * HPW + idx % HPW;
+                if (hh < p.Hv) {
+                    const int64_t gi = (b * p.T + t) * p.Hv + hh;
+                    p.io.alpha[gi] = __expf(-__expf(A[hh]) * softplusf_(__ldg(p.io.a_raw + gi) + ba[hh]));
+                    p.io.beta[gi] = sigmoidf_(__ldg(p.io.b_raw + gi));
+                }
+            }
         }
-    }
-    if (which == 2 && t1 > t0 && tid < kTile) {
-        // decay and write gates of this value head over the tile
-        const int64_t t = t0 + tid;
-        if (t < t1) {
-            const float eA = __expf(p.io.A[h]), ba = p.io.b_alpha[h];
-            const int64_t gi = (b * p.T + t) * p.Hv + h;
-            p.io.alpha[gi] = __expf(-eA * softplusf_(__ldg(p.io.a_raw + gi) + ba));
-            p.io.beta[gi] = sigmoidf_(__ldg(p.io.b_raw + gi));
+
+        // tap[j][e]: the weight applied to the input j tokens back (zero beyond K)
+        float tap[kMaxConv][8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+#pragma unroll
+            for (int j = 0; j < kMaxConv; ++j)
+                tap[j][e] = (on && j < K) ? __ldg(w + (col + e) * K + (K - 1 - j)) : 0.f;
+
+        // ring[s]: the input row of the token t with (t - ta) mod 4 == s
+        float ring[4][8];
+        {
+            float f[8];
+#pragma unroll
+            for (int j = 1; j < kMaxConv; ++j) {   // tokens ta-3 .. ta-1 -> slots 1 .. 3
+                const uint4 r = j >= kMaxConv - (K - 1) ? row_at(ta - kMaxConv + j) : zero;
+                unpack8(r, f);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) ring[j][e] = f[e];
+            }
+        }
+
+        if (n == kTile) {
+            if (which < 2)
+                prologue_rows<LPR, true, true>(ring, tap, lane_ring, xp, op, rs, n, len);
+            else
+                prologue_rows<LPR, false, true>(ring, tap, lane_ring, xp, op, rs, n, len);
+        } else {
+            if (which < 2)
+                prologue_rows<LPR, true, false>(ring, tap, lane_ring, xp, op, rs, n, len);
+            else
+                prologue_rows<LPR, false, false>(ring, tap, lane_ring, xp, op, rs, n, len);
+        }
+
+        if (sout && tb >= p.T && on) {
+            // the last K-1 inputs of the sequence, oldest first
+            for (int j = 0; j < K - 1; ++j)
+                *reinterpret_cast<uint4 *>(sout + (b * (K - 1) + j) * rowstride + col) = row_at(p.T - (K - 1) + j);
         }
     }
 }
@@ -315,15 +408,22 @@ gdn_status check_layer_shape(const gdn_layer_shape *s) {
     return GDN_OK;
 }
 
-gdn_status device_ok() {
+// The current device's SM count, after checking that it is an sm_103 part.
+gdn_status num_sms(int *sms) {
     int dev = 0, major = 0, minor = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) {
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
         cudaGetLastError();
         return GDN_ERR_CUDA;
     }
     return (major == 10 && minor == 3) ? GDN_OK : GDN_ERR_UNSUPPORTED;
+}
+
+gdn_status device_ok() {
+    int sms = 0;
+    return num_sms(&sms);
 }
 
 }  // namespace
@@ -377,16 +477,31 @@ extern "C" gdn_status gdn_layer_prologue(const gdn_layer_shape *shape, const gdn
     p.d = s.d;
     p.kconv = s.kconv;
     p.ntiles = static_cast<int>(s.T == 0 ? 1 : (s.T + kTile - 1) / kTile);
+    const int hpw = 32 / (s.d / 8);
+    p.gq = (s.Hqk + hpw - 1) / hpw;
+    p.gv = (s.Hv + hpw - 1) / hpw;
+    p.ngroups = 2 * p.gq + p.gv;
+    p.items = s.B * p.ntiles * p.ngroups;
     p.io = a;
-    const int64_t ctas = s.B * (2 * s.Hqk + s.Hv) * p.ntiles;
-    if (ctas > 0x7fffffff) return GDN_ERR_INVALID_ARG;
-    const dim3 grid(static_cast<unsigned>(ctas));
-    const size_t smem = static_cast<size_t>(kHalo + kTile) * s.d * 2;
+    int sms = 0;
+    if (num_sms(&sms) != GDN_OK) return GDN_ERR_CUDA;
+    const int64_t want = (p.items + kWarps - 1) / kWarps;
+    const unsigned grid = static_cast<unsigned>(want < int64_t{sms} * 2 ? want : int64_t{sms} * 2);
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    static std::once_flag attr_once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(attr_once, [] {
+        attr_err = cudaFuncSetAttribute(prologue_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        static_cast<int>(kPrologueSmem));
+        if (attr_err == cudaSuccess)
+            attr_err = cudaFuncSetAttribute(prologue_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                            static_cast<int>(kPrologueSmem));
+    });
+    if (attr_err != cudaSuccess) return GDN_ERR_CUDA;
     if (s.d == 128)
-        prologue_kernel<4><<<grid, 128, smem, cs>>>(p);
+        prologue_kernel<16><<<grid, kWarps * 32, kPrologueSmem, cs>>>(p);
     else
-        prologue_kernel<2><<<grid, 128, smem, cs>>>(p);
+        prologue_kernel<8><<<grid, kWarps * 32, kPrologueSmem, cs>>>(p);
     const cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
