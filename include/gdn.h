@@ -232,14 +232,42 @@ gdn_status gdn_prefill_noalloc_status(void *stream);
  * lines of the recurrence are unchanged.  This is the per-channel ("diagonal")
  * gate of Kimi Delta Attention, which the reading notes name beside the delta
  * rule (section 2.1, "Why the delta rule matters").  With all channels equal
- * it is the scalar recurrence.  Both calls run the token-sequential kernel
- * (dtype bf16 or fp32, state in fp32 registers); they need no workspace, and
- * S_T may equal S0.  Layouts, ownership and errors otherwise as gdn_prefill
- * and gdn_decode_step.
+ * it is the scalar recurrence.  S_T may equal S0.  Layouts, ownership and
+ * errors otherwise as gdn_prefill and gdn_decode_step.
+ *
+ * Prefill paths.  bf16 with dk = dv = 128 runs the chunked tensor-core path:
+ * a per-chunk pre-pass forms each chunk's gated operands from per-channel
+ * cumulative log decays (keys and queries scaled per channel against a
+ * reference token per 16-token block, so that every exponent stays bounded;
+ * a block whose own decay passes e^80 in some channel takes an element-wise
+ * path), the lower-triangular inverse and the chunk's W, U~ and P, then a
+ * chain kernel runs the state over the chunks, split into segments with
+ * warm-up windows as in gdn_prefill (the window bound uses the largest
+ * channel's decay; a segment without a window restarts from token 0, which
+ * is exact).  Every other shape runs the token-sequential kernel (bf16 or
+ * fp32, state in fp32 registers), as does the decode step.
+ *
+ * gdn_prefill_cw allocates the chunked path's workspace itself, in stream
+ * order (cudaMallocAsync / cudaFreeAsync on `stream`); gdn_prefill_cw_ex
+ * takes it from the caller: ws of at least gdn_prefill_cw_workspace_bytes
+ * bytes, 256-byte aligned (a 256-byte status area, B*Hv*dk*dv fp32 for an
+ * in-place S_T, and 74,244 bytes per (batch, value head, 64-token chunk); NULL
+ * with 0 bytes for a token-sequential call).  options as for gdn_prefill_ex:
+ * segments, log_eps and max_warmup_chunks apply to the chunked path;
+ * algorithm GDN_ALGO_SEQUENTIAL forces the token-sequential kernel and
+ * GDN_ALGO_CHUNKED returns GDN_ERR_UNSUPPORTED for shapes the chunked path
+ * does not take; test_stall_chunk must be 0.
  */
 gdn_status gdn_prefill_cw(const gdn_shape *shape, const void *q, const void *k, const void *v,
                           const float *alpha, const float *beta, const float *S0, void *y, float *S_T,
                           void *stream);
+
+size_t gdn_prefill_cw_workspace_bytes(const gdn_shape *shape);
+
+gdn_status gdn_prefill_cw_ex(const gdn_shape *shape, const gdn_prefill_options *options,
+                             const void *q, const void *k, const void *v,
+                             const float *alpha, const float *beta, const float *S0,
+                             void *y, float *S_T, void *ws, size_t ws_bytes, void *stream);
 
 gdn_status gdn_decode_step_cw(const gdn_shape *shape, const void *q, const void *k, const void *v,
                               const float *alpha, const float *beta, float *S_inout, void *y, void *stream);

@@ -361,9 +361,113 @@ static gdn_status recurrence_cw(const gdn_shape *shape, bool decode, const void 
     return from_cuda(gdn::launch_recurrent(p, s.dk, s.dv, static_cast<gdn_dtype>(s.dtype), stream));
 }
 
+// Whether a channel-wise prefill of this shape takes the chunked tensor-core path.
+static bool cw_chunked(const gdn_shape &s, int algorithm) {
+    if (algorithm == GDN_ALGO_SEQUENTIAL) return false;
+    return s.dtype == GDN_BF16 && s.dk == 128 && s.dv == 128;
+}
+
+// Workspace of the chunked channel-wise prefill: status area, in-place
+// staging, then the per-chunk operand records and decay bounds.
+static size_t cw_layout(const gdn_shape &s, int64_t n_state, size_t *off_ops) {
+    *off_ops = round256(kStatusBytes + static_cast<size_t>(n_state) * sizeof(float));
+    return *off_ops + gdn::chunked_cw_ops_bytes(s.B, s.T, s.Hv);
+}
+
+size_t gdn_prefill_cw_workspace_bytes(const gdn_shape *shape) {
+    int64_t n_qk, n_v, n_gate, n_state;
+    if (check_shape(shape, &n_qk, &n_v, &n_gate, &n_state) != GDN_OK) return 0;
+    if (!cw_chunked(*shape, GDN_ALGO_AUTO)) return kStatusBytes;
+    size_t off = 0;
+    return cw_layout(*shape, n_state, &off);
+}
+
+gdn_status gdn_prefill_cw_ex(const gdn_shape *shape, const gdn_prefill_options *options, const void *q,
+                             const void *k, const void *v, const float *alpha, const float *beta, const float *S0,
+                             void *y, float *S_T, void *ws, size_t ws_bytes, void *stream_) {
+    int64_t n_qk, n_v, n_gate, n_state;
+    gdn_status st = check_shape(shape, &n_qk, &n_v, &n_gate, &n_state);
+    if (st != GDN_OK) return st;
+    const gdn_shape &s = *shape;
+    gdn_prefill_options opt{0, 0.f, 0, GDN_ALGO_AUTO, 0};
+    if (options) opt = *options;
+    if (opt.segments < 0 || opt.max_warmup_chunks < 0 || !(opt.log_eps <= 0.f)) return GDN_ERR_INVALID_ARG;
+    if (opt.algorithm < GDN_ALGO_AUTO || opt.algorithm > GDN_ALGO_SEQUENTIAL) return GDN_ERR_INVALID_ARG;
+    if (opt.test_stall_chunk != 0) return GDN_ERR_INVALID_ARG;
+    if (opt.algorithm == GDN_ALGO_CHUNKED && !cw_chunked(s, GDN_ALGO_CHUNKED)) return GDN_ERR_UNSUPPORTED;
+    if (!cw_chunked(s, opt.algorithm)) return recurrence_cw(shape, false, q, k, v, alpha, beta, S0, S_T, y, stream_);
+
+    const bool has_tokens = s.B * s.T > 0;
+    if (has_tokens && (!q || !k || !v || !alpha || !beta || !y)) return GDN_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(y, 16) || !aligned(S0, 16) ||
+        !aligned(S_T, 16) || !aligned(alpha, 16) || !aligned(beta, 4) || !aligned(ws, 256))
+        return GDN_ERR_ALIGNMENT;
+    const Range rq{q, static_cast<size_t>(n_qk) * 2}, rk{k, static_cast<size_t>(n_qk) * 2};
+    const Range rv{v, static_cast<size_t>(n_v) * 2}, ry{y, static_cast<size_t>(n_v) * 2};
+    const Range ra{alpha, static_cast<size_t>(n_gate) * s.dk * 4}, rb{beta, static_cast<size_t>(n_gate) * 4};
+    const Range rs0{S0, static_cast<size_t>(n_state) * 4}, rst{S_T, static_cast<size_t>(n_state) * 4};
+    const Range rws{ws, ws_bytes};
+    for (const Range &in : {rq, rk, rv, ra, rb, rs0, rst, rws})
+        if (overlap(ry, in)) return GDN_ERR_ALIASING;
+    for (const Range &in : {rq, rk, rv, ra, rb, rws})
+        if (overlap(rst, in)) return GDN_ERR_ALIASING;
+    for (const Range &in : {rq, rk, rv, ra, rb, rs0})
+        if (overlap(rws, in)) return GDN_ERR_ALIASING;
+    const bool in_place = S0 && S_T && S0 == S_T;
+    if (!in_place && overlap(rst, rs0)) return GDN_ERR_ALIASING;
+    size_t off_ops = 0;
+    const size_t need = cw_layout(s, n_state, &off_ops);
+    if (has_tokens && s.Hv > 0 && (!ws || ws_bytes < need)) return GDN_ERR_WORKSPACE;
+    int num_sms = 0;
+    st = check_device(&num_sms);
+    if (st != GDN_OK) return st;
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+    if (s.B * s.Hv == 0) return GDN_OK;
+    if (!has_tokens) {
+        if (S_T && !in_place) {
+            if (S0) return from_cuda(cudaMemcpyAsync(S_T, S0, rst.n, cudaMemcpyDeviceToDevice, stream));
+            return from_cuda(cudaMemsetAsync(S_T, 0, rst.n, stream));
+        }
+        return GDN_OK;
+    }
+    float *staging = reinterpret_cast<float *>(static_cast<char *>(ws) + kStatusBytes);
+    gdn::ChunkedCwParams p{};
+    p.B = s.B; p.T = s.T; p.Hqk = s.Hqk; p.Hv = s.Hv; p.group = s.Hv / s.Hqk; p.d = s.dk;
+    p.q = q; p.k = k; p.v = v; p.alpha = alpha; p.beta = beta; p.S0 = S0; p.y = y;
+    // segments of one head run on different CTAs: stage an in-place S_T
+    p.S_T = in_place ? staging : S_T;
+    p.segments = opt.segments;
+    p.log_eps = opt.log_eps < 0.f ? opt.log_eps : kDefaultLogEps;
+    p.max_warmup_chunks = opt.max_warmup_chunks > 0 ? opt.max_warmup_chunks : kDefaultMaxWarmupChunks;
+    p.ops = static_cast<uint8_t *>(ws) + off_ops;
+    st = from_cuda(gdn::launch_chunked_cw(p, stream, num_sms));
+    if (st != GDN_OK) return st;
+    if (in_place) return from_cuda(cudaMemcpyAsync(S_T, staging, rst.n, cudaMemcpyDeviceToDevice, stream));
+    return GDN_OK;
+}
+
 gdn_status gdn_prefill_cw(const gdn_shape *shape, const void *q, const void *k, const void *v, const float *alpha,
                           const float *beta, const float *S0, void *y, float *S_T, void *stream) {
-    return recurrence_cw(shape, false, q, k, v, alpha, beta, S0, S_T, y, stream);
+    int64_t n_qk, n_v, n_gate, n_state;
+    gdn_status st = check_shape(shape, &n_qk, &n_v, &n_gate, &n_state);
+    if (st != GDN_OK) return st;
+    if (!cw_chunked(*shape, GDN_ALGO_AUTO) || shape->B * shape->T * shape->Hv == 0)
+        return recurrence_cw(shape, false, q, k, v, alpha, beta, S0, S_T, y, stream);
+    // Every argument check first (they end at the missing workspace), then the
+    // chunked path's workspace, allocated and freed in stream order.
+    st = gdn_prefill_cw_ex(shape, nullptr, q, k, v, alpha, beta, S0, y, S_T, nullptr, 0, stream);
+    if (st != GDN_ERR_WORKSPACE) return st;
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    const size_t bytes = gdn_prefill_cw_workspace_bytes(shape);
+    void *ws = nullptr;
+    if (cudaMallocAsync(&ws, bytes, cs) != cudaSuccess) {
+        cudaGetLastError();
+        return GDN_ERR_CUDA;
+    }
+    st = gdn_prefill_cw_ex(shape, nullptr, q, k, v, alpha, beta, S0, y, S_T, ws, bytes, stream);
+    const cudaError_t fe = cudaFreeAsync(ws, cs);
+    if (st == GDN_OK && fe != cudaSuccess) st = GDN_ERR_CUDA;
+    return st;
 }
 
 gdn_status gdn_decode_step_cw(const gdn_shape *shape, const void *q, const void *k, const void *v,

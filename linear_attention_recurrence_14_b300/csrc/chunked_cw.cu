@@ -1,0 +1,878 @@
+// Chunked prefill with the channel-wise decay gate (bf16 q/k/v, d = 128):
+// S~ = diag(alpha_t) S with alpha_t in (0, 1]^{dk}, the other three lines of the
+// recurrence unchanged (Qwen3.8-Next reading notes, section 2.1, "Why the
+// delta rule matters": the per-channel decay of Kimi Delta Attention).
+//
+// Chunk algebra.  Over a chunk of C = 64 tokens let G[t][c] be the cumulative
+// sum of log alpha of channel c up to and including token t, and write
+// Qp = Q (.) e^G, Kp = K (.) e^G, Kl = K (.) e^{g_C - G} (g_C the last row of G).
+// Unrolling the transition form S_t = diag(alpha_t)(I - beta_t k_t k_t^T) S_{t-1}
+// + beta_t k_t v_t^T over the chunk gives, for the state S entering it:
+//     A_ts = beta_t sum_c k_tc k_sc e^{G_tc - G_sc}      (s < t),   T = (I + A)^{-1}
+//     W = T diag(beta) Kp,  U~ = T diag(beta) V,  U = U~ - W S
+//     P_ts = sum_c q_tc k_sc e^{G_tc - G_sc}              (s <= t)
+//     Y = Qp S + P U,       S_next = diag(e^{g_C}) S + Kl^T U.
+// With a scalar gate the factors e^{G_t - G_s} come out of the channel sums;
+// here they stay inside, so A and P are Gram products of per-channel scaled
+// keys and queries.  Every factor used is bounded by 1 except inside a
+// 16-token block: row block I uses the reference R_I = G at the token before
+// the block, so (t in block I, s <= t)
+//     e^{G_t - G_s} = e^{G_t - R_I} * e^{R_I - G_s},
+// the first factor <= 1 and the second <= 1 for s before the block and at most
+// the block's own decay for s inside it.  A block whose decay exceeds e^80 in
+// some channel (far beyond any gate of a trained layer) has its diagonal part
+// computed element by element instead, so the result holds for every gate.
+//
+// Two kernels.  cw_prepass_kernel, one CTA per (batch, value head, chunk),
+// computes everything that does not depend on the state and writes it to the
+// workspace: -W, U~, Qp, Kl and P in bf16, e^{g_C}, and a per-chunk bound on
+// the state's decay (the sum over tokens of max_c log alpha) for the warm-up
+// windows.  cw_chain_kernel, one CTA per (batch, value head, segment), runs the
+// state through the chunks: three products per chunk on the tensor cores
+// (warp-level bf16 MMAs, fp32 accumulation), the state in fp32 registers as
+// the accumulator of its own update, y written per chunk.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "gdn_internal.h"
+
+namespace gdn {
+namespace {
+
+constexpr int kC = 64;             // tokens per chunk
+constexpr int kD = 128;            // head dimension (dk = dv)
+constexpr float kMaxExp = 80.f;    // largest exponent taken through a bf16 operand
+
+// Chunk record in the workspace, per (batch, value head, chunk); tiles are
+// row-major bf16 [64][128] (P: [64][64]), rows 256 (128) bytes.
+constexpr uint32_t REC_WN = 0;          // -W
+constexpr uint32_t REC_UT = 16384;      // U~
+constexpr uint32_t REC_QP = 32768;      // Qp
+constexpr uint32_t REC_KL = 49152;      // Kl
+constexpr uint32_t REC_P = 65536;       // P (zero above the diagonal)
+constexpr uint32_t REC_GC = 73728;      // e^{g_C}, fp32 [128]
+constexpr uint32_t kRecBytes = 74240;
+static_assert(kRecBytes == kCwChunkBytes, "chunk record size");
+
+// ---------------------------------------------------------------- helpers
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// Byte offset of the 16-byte piece `ch` of row `row` in a tile of 256-byte
+// rows (16 pieces) or 128-byte rows (8 pieces), XOR-swizzled by the row so
+// that eight rows read at the same column fall in different banks.
+__device__ __forceinline__ uint32_t sw256(int row, int ch) { return row * 256 + ((ch ^ (row & 7)) << 4); }
+__device__ __forceinline__ uint32_t sw128(int row, int ch) { return row * 128 + ((ch ^ (row & 7)) << 4); }
+
+__device__ __forceinline__ void cp_async16(uint32_t saddr, const void *g) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(saddr), "l"(g) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+
+__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], uint32_t a) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(a));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t (&r)[4], uint32_t a) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(a));
+}
+
+// d (16 x 8 fp32) += a (16 x 16 bf16, row) * b (16 x 8 bf16, col).
+__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// d (16 x 8 fp32) += a (16 x 8 tf32, row) * b (8 x 8 tf32, col).
+__device__ __forceinline__ void mma_tf32(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+    const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t *>(&v);
+}
+__device__ __forceinline__ float2 unpack2(uint32_t w) {
+    return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+}
+
+// Lane addresses of ldmatrix x4 loads (16 x 16 pieces of bf16 tiles).
+//  A, row-major [m][k] storage: matrices (m 0-7, k 0-7), (m 8-15, k 0-7), (m 0-7, k 8-15), (m 8-15, k 8-15).
+__device__ __forceinline__ int a_row(int lane) { return (lane & 7) + 8 * ((lane >> 3) & 1); }
+__device__ __forceinline__ int a_ch(int lane) { return lane >> 4; }
+//  B from [n][k] storage (no transpose), two n-tiles: (n 0-7, k 0-7), (n 0-7, k 8-15), (n 8-15, k 0-7), (n 8-15, k 8-15).
+__device__ __forceinline__ int bn_row(int lane) { return (lane & 7) + 8 * (lane >> 4); }
+__device__ __forceinline__ int bn_ch(int lane) { return (lane >> 3) & 1; }
+//  B from [k][n] storage (transposed load), two n-tiles: (k 0-7, n 0-7), (k 8-15, n 0-7), (k 0-7, n 8-15), (k 8-15, n 8-15).
+__device__ __forceinline__ int bt_row(int lane) { return (lane & 7) + 8 * ((lane >> 3) & 1); }
+__device__ __forceinline__ int bt_ch(int lane) { return lane >> 4; }
+//  A from [k][m] storage (transposed load): (k 0-7, m 0-7), (k 0-7, m 8-15), (k 8-15, m 0-7), (k 8-15, m 8-15).
+__device__ __forceinline__ int at_row(int lane) { return (lane & 7) + 8 * (lane >> 4); }
+__device__ __forceinline__ int at_ch(int lane) { return (lane >> 3) & 1; }
+
+// ------------------------------------------------ lower-triangular inverse
+// T = (I + A)^{-1} of the chunk's 64 x 64 strictly lower A by 16 x 16 blocks:
+// the four diagonal blocks by forward substitution, then with the left factors
+// F_IK = T_II A_IK each off-diagonal block T_IJ = -sum_{K=J}^{I-1} F_IK T_KJ.
+// Matrices are block-packed: block (I, J), J <= I, at index I (I + 1) / 2 + J,
+// rows of kBS floats; A is column-major within a block, T row-major.
+constexpr int kBS = 24;
+constexpr int kBlk = 16 * kBS;
+constexpr int kBlkFloats = 10 * kBlk;
+__device__ __forceinline__ int blk(int I, int J) { return I * (I + 1) / 2 + J; }
+
+// Column `col` of the diagonal block b of T: t[r] = delta(r, col) - sum_{m<r} A[r][m] t[m].
+__device__ __forceinline__ void diag_solve(int b, int col, const float *At, float *Tm) {
+    const float *Ab = At + blk(b, b) * kBlk;
+    float t[16];
+#pragma unroll
+    for (int r = 0; r < 16; ++r) t[r] = (r == col) ? 1.f : 0.f;
+#pragma unroll
+    for (int m = 0; m < 15; ++m) {
+        const float tm = t[m];
+#pragma unroll
+        for (int r = m + 1; r < 16; ++r) t[r] = fmaf(-Ab[m * kBS + r], tm, t[r]);
+    }
+    float *Tb = Tm + blk(b, b) * kBlk + col;
+#pragma unroll
+    for (int r = 0; r < 16; ++r) Tb[r * kBS] = t[r];
+}
+
+// The six left factors as twelve 8-column tiles, three per warp (warps 0-3),
+// written in place of A_IK (a warp reads and writes only its own columns).
+struct FactorJob {
+    uint8_t I, K, nt;
+};
+__constant__ FactorJob kFactorJobs[4][3] = {
+    {{1, 0, 0}, {1, 0, 1}, {2, 0, 0}},
+    {{2, 1, 0}, {2, 1, 1}, {2, 0, 1}},
+    {{3, 2, 0}, {3, 2, 1}, {3, 1, 0}},
+    {{3, 0, 0}, {3, 0, 1}, {3, 1, 1}},
+};
+
+__device__ __forceinline__ void solve_factors(int w, float *At, const float *Tm, int lane) {
+    const int gq = lane >> 2, t4 = lane & 3;
+    float acc[3][2][4];
+    float *fb[3];
+    int col[3];
+#pragma unroll
+    for (int u = 0; u < 3; ++u) {
+        const FactorJob jb = kFactorJobs[w][u];
+        const float *Td = Tm + blk(jb.I, jb.I) * kBlk;
+        fb[u] = At + blk(jb.I, jb.K) * kBlk;
+        col[u] = 8 * jb.nt + gq;
+#pragma unroll
+        for (int ks = 0; ks < 2; ++ks) {
+            const int k0 = 8 * ks;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[u][ks][e] = 0.f;
+            mma_tf32(acc[u][ks], __float_as_uint(Td[gq * kBS + k0 + t4]), __float_as_uint(Td[(gq + 8) * kBS + k0 + t4]),
+                     __float_as_uint(Td[gq * kBS + k0 + t4 + 4]), __float_as_uint(Td[(gq + 8) * kBS + k0 + t4 + 4]),
+                     __float_as_uint(fb[u][col[u] * kBS + k0 + t4]), __float_as_uint(fb[u][col[u] * kBS + k0 + t4 + 4]));
+        }
+    }
+    __syncwarp();
+#pragma unroll
+    for (int u = 0; u < 3; ++u) {
+        float *f = fb[u] + (col[u] - gq + 2 * t4) * kBS + gq;
+        f[0] = acc[u][0][0] + acc[u][1][0];
+        f[kBS] = acc[u][0][1] + acc[u][1][1];
+        f[8] = acc[u][0][2] + acc[u][1][2];
+        f[kBS + 8] = acc[u][0][3] + acc[u][1][3];
+    }
+}
+
+// Off-diagonal blocks of block column J (NNT = 2: both 8-column tiles, NNT = 1:
+// tile nt0): T_IJ = -sum_{K=J}^{I-1} F_IK T_KJ for I = J+1..3 in order.
+template <int NNT>
+__device__ __forceinline__ void solve_column(int J, int nt0, const float *At, float *Tm, int lane) {
+    const int gq = lane >> 2, t4 = lane & 3;
+#pragma unroll 1
+    for (int I = J + 1; I < 4; ++I) {
+        float c[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+        float e[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll 1
+        for (int K = J; K < I; ++K) {
+            const float *Fb = At + blk(I, K) * kBlk;   // F[r][k] at k*kBS + r
+            const float *Bb = Tm + blk(K, J) * kBlk;   // T[k][n] at k*kBS + n
+#pragma unroll
+            for (int ks = 0; ks < 2; ++ks) {
+                const int k0 = 8 * ks;
+                const uint32_t a0 = __float_as_uint(Fb[(k0 + t4) * kBS + gq]);
+                const uint32_t a1 = __float_as_uint(Fb[(k0 + t4) * kBS + gq + 8]);
+                const uint32_t a2 = __float_as_uint(Fb[(k0 + t4 + 4) * kBS + gq]);
+                const uint32_t a3 = __float_as_uint(Fb[(k0 + t4 + 4) * kBS + gq + 8]);
+#pragma unroll
+                for (int nt = 0; nt < NNT; ++nt) {
+                    const uint32_t b0 = __float_as_uint(Bb[(k0 + t4) * kBS + 8 * (nt0 + nt) + gq]);
+                    const uint32_t b1 = __float_as_uint(Bb[(k0 + t4 + 4) * kBS + 8 * (nt0 + nt) + gq]);
+                    mma_tf32(ks ? e[nt] : c[nt], a0, a1, a2, a3, b0, b1);
+                }
+            }
+        }
+        float *Tb = Tm + blk(I, J) * kBlk;
+#pragma unroll
+        for (int nt = 0; nt < NNT; ++nt) {
+            const int cn = 8 * (nt0 + nt) + 2 * t4;
+#pragma unroll
+            for (int hr = 0; hr < 2; ++hr) {
+                const int r = gq + 8 * hr;
+                *reinterpret_cast<float2 *>(Tb + r * kBS + cn) =
+                    make_float2(-(c[nt][2 * hr] + e[nt][2 * hr]), -(c[nt][2 * hr + 1] + e[nt][2 * hr + 1]));
+            }
+        }
+        __syncwarp();
+    }
+}
+
+// ------------------------------------------------------------- parameters
+
+struct CwDev {
+    int64_t T;
+    int B, Hqk, Hv, group, nchunks;
+    int seg_chunks, max_warmup;
+    float log_eps;
+    const __nv_bfloat16 *q, *k, *v;
+    const float *alpha, *beta, *S0;
+    __nv_bfloat16 *y;
+    float *S_T;
+    uint8_t *rec;     // [B * Hv][nchunks][kRecBytes]
+    float *bound;     // [B * Hv][nchunks]
+};
+
+// Pre-pass shared memory (bytes).  After the A and P products the q/k tiles
+// hold A and T, the G tile holds T diag(beta) and the Kn tile holds V.
+constexpr uint32_t PP_G = 0;            // G, fp32 [64][128]    | later T2 bf16 [64][64]
+constexpr uint32_t PP_QT = 32768;       // q, then Qloc         | later A (fp32, block-packed)
+constexpr uint32_t PP_KT = 49152;       // k                    | later T (from PP_QT + 15360)
+constexpr uint32_t PP_KL = 65536;       // Kloc
+constexpr uint32_t PP_KN = 81920;       // Kn of the current row block | later V
+constexpr uint32_t PP_FIX = 98304;      // element-wise diagonal blocks [4][2][16][16] fp32
+constexpr uint32_t PP_BETA = 106496;    // beta [64]
+constexpr uint32_t PP_R = 106752;       // R_I [4][128]
+constexpr uint32_t PP_ER = 108800;      // e^{R_I} [4][128]
+constexpr uint32_t PP_GC = 110848;      // g_C [128]
+constexpr uint32_t PP_VIOL = 111360;    // [4] int: block exceeds e^kMaxExp in some channel
+constexpr uint32_t PP_WRED = 111376;    // [8] per-warp partial sums
+constexpr uint32_t kPrepassSmem = 111408;
+constexpr uint32_t PP_AT = PP_QT;
+constexpr uint32_t PP_TM = PP_QT + kBlkFloats * 4;
+constexpr uint32_t PP_T2 = PP_G;
+static_assert(PP_TM + kBlkFloats * 4 <= PP_KL, "A and T fit in the q/k tiles");
+
+__device__ __forceinline__ float tile_elem(const uint8_t *tile, int row, int col) {
+    const uint16_t h = *reinterpret_cast<const uint16_t *>(tile + sw256(row, col >> 3) + 2 * (col & 7));
+    return __uint_as_float(static_cast<uint32_t>(h) << 16);
+}
+
+__global__ void __launch_bounds__(256, 2) cw_prepass_kernel(const CwDev p) {
+    extern __shared__ __align__(128) uint8_t sm[];
+    const uint32_t sb = smem_u32(sm);
+    float *G = reinterpret_cast<float *>(sm + PP_G);
+    float *beta_s = reinterpret_cast<float *>(sm + PP_BETA);
+    float *R = reinterpret_cast<float *>(sm + PP_R);
+    float *eR = reinterpret_cast<float *>(sm + PP_ER);
+    float *gC = reinterpret_cast<float *>(sm + PP_GC);
+    int *viol = reinterpret_cast<int *>(sm + PP_VIOL);
+    float *wred = reinterpret_cast<float *>(sm + PP_WRED);
+    float *fix = reinterpret_cast<float *>(sm + PP_FIX);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int g = lane >> 2, t4 = lane & 3;
+    const int hv = static_cast<int>(blockIdx.x % static_cast<unsigned>(p.Hv));
+    const int64_t rest = blockIdx.x / static_cast<unsigned>(p.Hv);
+    const int c = static_cast<int>(rest % p.nchunks);
+    const int b = static_cast<int>(rest / p.nchunks);
+    const int hk = hv / p.group;
+    const int64_t t0 = static_cast<int64_t>(c) * kC;
+    const int nvalid = p.T - t0 < kC ? static_cast<int>(p.T - t0) : kC;
+    const int64_t pr = static_cast<int64_t>(b) * p.Hv + hv;
+    uint8_t *rec = p.rec + (pr * p.nchunks + c) * static_cast<int64_t>(kRecBytes);
+    const uint4 zero4 = make_uint4(0u, 0u, 0u, 0u);
+
+    // ---- loads: alpha (tokens past T as 1), q and k (as 0), beta (as 0)
+    for (int e = tid; e < kC * 32; e += 256) {
+        const int r = e >> 5, pc = e & 31;
+        float *dst = G + r * kD + pc * 4;
+        if (r < nvalid)
+            cp_async16(smem_u32(dst), p.alpha + ((static_cast<int64_t>(b) * p.T + t0 + r) * p.Hv + hv) * kD + pc * 4);
+        else
+            *reinterpret_cast<float4 *>(dst) = make_float4(1.f, 1.f, 1.f, 1.f);
+    }
+    for (int e = tid; e < kC * 16; e += 256) {
+        const int r = e >> 4, pc = e & 15;
+        const uint32_t off = sw256(r, pc);
+        if (r < nvalid) {
+            const int64_t gi = ((static_cast<int64_t>(b) * p.T + t0 + r) * p.Hqk + hk) * kD + pc * 8;
+            cp_async16(sb + PP_QT + off, p.q + gi);
+            cp_async16(sb + PP_KT + off, p.k + gi);
+        } else {
+            *reinterpret_cast<uint4 *>(sm + PP_QT + off) = zero4;
+            *reinterpret_cast<uint4 *>(sm + PP_KT + off) = zero4;
+        }
+    }
+    if (tid < kC) beta_s[tid] = tid < nvalid ? __ldg(p.beta + (static_cast<int64_t>(b) * p.T + t0 + tid) * p.Hv + hv) : 0.f;
+    if (tid < 4) viol[tid] = 0;
+    cp_async_commit();
+    cp_async_wait_all();
+    __syncthreads();
+
+    // ---- G = cumulative log alpha per channel; block references R_I = G before
+    // block I; e^{g_C} into the record; blocks whose own decay passes e^kMaxExp
+    if (tid < kD) {
+        const int ch = tid;
+        float run = 0.f;
+#pragma unroll 4
+        for (int t = 0; t < kC; ++t) {
+            if ((t & 15) == 0) R[(t >> 4) * kD + ch] = run;
+            run += logf(G[t * kD + ch]);
+            G[t * kD + ch] = run;
+        }
+        gC[ch] = run;
+        reinterpret_cast<float *>(rec + REC_GC)[ch] = __expf(run);
+#pragma unroll
+        for (int I = 0; I < 4; ++I) {
+            const float r = R[I * kD + ch];
+            eR[I * kD + ch] = __expf(r);
+            if (r - G[(16 * I + 15) * kD + ch] > kMaxExp) viol[I] = 1;
+        }
+    }
+    __syncthreads();
+
+    // ---- decay bound of the chunk: sum over tokens of max_c log alpha
+    {
+        float part = 0.f;
+#pragma unroll 1
+        for (int i = 0; i < 8; ++i) {
+            const int t = warp * 8 + i;
+            float m = -INFINITY;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int ch = lane + 32 * j;
+                m = fmaxf(m, G[t * kD + ch] - (t > 0 ? G[(t - 1) * kD + ch] : 0.f));
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+            part += m;
+        }
+        if (lane == 0) wred[warp] = part;
+    }
+    // ---- diagonal blocks past the bf16 range, element by element (t >= s in the block)
+#pragma unroll 1
+    for (int I = 0; I < 4; ++I) {
+        if (!viol[I]) continue;
+        const int t = 16 * I + (tid >> 4), s = 16 * I + (tid & 15);
+        float a = 0.f, pp = 0.f;
+        if (s <= t) {
+#pragma unroll 4
+            for (int ch = 0; ch < kD; ++ch) {
+                const float e = __expf(G[t * kD + ch] - G[s * kD + ch]);
+                const float ks = tile_elem(sm + PP_KT, s, ch) * e;
+                a = fmaf(tile_elem(sm + PP_KT, t, ch), ks, a);
+                pp = fmaf(tile_elem(sm + PP_QT, t, ch), ks, pp);
+            }
+        }
+        fix[(2 * I) * 256 + (tid >> 4) * 16 + (tid & 15)] = s < t ? a : 0.f;
+        fix[(2 * I + 1) * 256 + (tid >> 4) * 16 + (tid & 15)] = s <= t ? pp : 0.f;
+    }
+    __syncthreads();
+    if (tid == 0) {
+        float s = 0.f;
+        for (int w = 0; w < 8; ++w) s += wred[w];
+        p.bound[pr * p.nchunks + c] = s;
+    }
+
+    // ---- per-token operands: Qp, Kl to the record; Qloc (in place of q), Kloc
+    for (int e = tid; e < kC * 16; e += 256) {
+        const int t = e >> 4, pc = e & 15, I = t >> 4;
+        const uint32_t off = sw256(t, pc);
+        const uint4 qr = *reinterpret_cast<const uint4 *>(sm + PP_QT + off);
+        const uint4 kr = *reinterpret_cast<const uint4 *>(sm + PP_KT + off);
+        const uint32_t qw[4] = {qr.x, qr.y, qr.z, qr.w}, kw[4] = {kr.x, kr.y, kr.z, kr.w};
+        const float *gr = G + t * kD + pc * 8;
+        const float *rr = R + I * kD + pc * 8;
+        const float *gc = gC + pc * 8;
+        uint32_t oqp[4], okl[4], oql[4], okq[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const float2 qf = unpack2(qw[j]), kf = unpack2(kw[j]);
+            float e1[2], el[2], eo[2];
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const float gv = gr[2 * j + h];
+                e1[h] = __expf(gv);
+                el[h] = __expf(gc[2 * j + h] - gv);
+                eo[h] = __expf(gv - rr[2 * j + h]);
+            }
+            oqp[j] = pack2(qf.x * e1[0], qf.y * e1[1]);
+            okl[j] = pack2(kf.x * el[0], kf.y * el[1]);
+            oql[j] = pack2(qf.x * eo[0], qf.y * eo[1]);
+            okq[j] = pack2(kf.x * eo[0], kf.y * eo[1]);
+        }
+        *reinterpret_cast<uint4 *>(rec + REC_QP + t * 256 + pc * 16) = make_uint4(oqp[0], oqp[1], oqp[2], oqp[3]);
+        *reinterpret_cast<uint4 *>(rec + REC_KL + t * 256 + pc * 16) = make_uint4(okl[0], okl[1], okl[2], okl[3]);
+        *reinterpret_cast<uint4 *>(sm + PP_QT + off) = make_uint4(oql[0], oql[1], oql[2], oql[3]);
+        *reinterpret_cast<uint4 *>(sm + PP_KL + off) = make_uint4(okq[0], okq[1], okq[2], okq[3]);
+    }
+    __syncthreads();
+
+    // ---- A and P by row block I: Kn = K (.) e^{R_I - G} for the key rows s < 16(I+1),
+    // then the products with Kloc (A) and Qloc (P) of the block's 16 rows, one
+    // task per (product, pair of 8-column tiles).  Warp w keeps the A tile pair
+    // np = w of every block I >= w in registers until the q/k tiles are free.
+    float aacc[4][2][4];
+#pragma unroll
+    for (int I = 0; I < 4; ++I) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) aacc[I][e >> 2][e & 3] = 0.f;
+        const bool vI = viol[I] != 0;
+        for (int e = tid; e < 16 * (I + 1) * 16; e += 256) {
+            const int s = e >> 4, pc = e & 15;
+            uint4 out = zero4;
+            if (!(vI && s >= 16 * I)) {
+                const uint4 kr = *reinterpret_cast<const uint4 *>(sm + PP_KT + sw256(s, pc));
+                const uint32_t kw[4] = {kr.x, kr.y, kr.z, kr.w};
+                const float *gr = G + s * kD + pc * 8;
+                const float *rr = R + I * kD + pc * 8;
+                uint32_t o[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const float2 kf = unpack2(kw[j]);
+                    o[j] = pack2(kf.x * __expf(rr[2 * j] - gr[2 * j]), kf.y * __expf(rr[2 * j + 1] - gr[2 * j + 1]));
+                }
+                out = make_uint4(o[0], o[1], o[2], o[3]);
+            }
+            *reinterpret_cast<uint4 *>(sm + PP_KN + sw256(s, pc)) = out;
+        }
+        __syncthreads();
+        const int ntask = 2 * (I + 1);
+        if (warp < ntask) {
+            const bool is_a = warp <= I;
+            const int np = is_a ? warp : warp - (I + 1);
+            const uint32_t xa = sb + (is_a ? PP_KL : PP_QT);
+            float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks) {
+                uint32_t af[4], bf[4];
+                ldsm_x4(af, xa + sw256(16 * I + a_row(lane), 2 * ks + a_ch(lane)));
+                ldsm_x4(bf, sb + PP_KN + sw256(16 * np + bn_row(lane), 2 * ks + bn_ch(lane)));
+                mma16816(acc[0], af, bf[0], bf[1]);
+                mma16816(acc[1], af, bf[2], bf[3]);
+            }
+            if (is_a) {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) aacc[I][e >> 2][e & 3] = acc[e >> 2][e & 3];
+            } else {
+                // P rows t = 16I + g (+8), columns s = 16np + 8j + 2t4 (+1), s <= t
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+#pragma unroll
+                    for (int hr = 0; hr < 2; ++hr) {
+                        const int t = 16 * I + g + 8 * hr;
+                        const int s = 16 * np + 8 * j + 2 * t4;
+                        float v0 = acc[j][2 * hr], v1 = acc[j][2 * hr + 1];
+                        if (vI && np == I) {
+                            v0 = fix[(2 * I + 1) * 256 + (t & 15) * 16 + (s & 15)];
+                            v1 = fix[(2 * I + 1) * 256 + (t & 15) * 16 + ((s + 1) & 15)];
+                        }
+                        v0 = s <= t ? v0 : 0.f;
+                        v1 = s + 1 <= t ? v1 : 0.f;
+                        *reinterpret_cast<uint32_t *>(rec + REC_P + t * 128 + s * 2) = pack2(v0, v1);
+                    }
+                }
+            }
+        }
+        __syncthreads();
+    }
+    // P above the diagonal blocks: zeros
+    for (int e = tid; e < 64 * 32; e += 256) {
+        const int t = e >> 5, s = 2 * (e & 31);
+        if (s >= 16 * ((t >> 4) + 1)) *reinterpret_cast<uint32_t *>(rec + REC_P + t * 128 + s * 2) = 0u;
+    }
+
+    // ---- A into the block-packed solve layout (over the q/k tiles), V into the Kn tile
+    float *At = reinterpret_cast<float *>(sm + PP_AT);
+    float *Tm = reinterpret_cast<float *>(sm + PP_TM);
+#pragma unroll
+    for (int I = 0; I < 4; ++I) {
+        if (warp <= I) {
+            const bool vdiag = warp == I && viol[I] != 0;
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+#pragma unroll
+                for (int hr = 0; hr < 2; ++hr) {
+                    const int t = 16 * I + g + 8 * hr;
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const int s = 16 * warp + 8 * j + 2 * t4 + h;
+                        if (s < t) {
+                            const float a = vdiag ? fix[(2 * I) * 256 + (t & 15) * 16 + (s & 15)] : aacc[I][j][2 * hr + h];
+                            At[blk(I, warp) * kBlk + (s & 15) * kBS + (t & 15)] = beta_s[t] * a;
+                        }
+                    }
+                }
+            }
+        }
+    }
+    for (int e = tid; e < kC * 16; e += 256) {
+        const int r = e >> 4, pc = e & 15;
+        const uint32_t off = sw256(r, pc);
+        if (r < nvalid)
+            cp_async16(sb + PP_KN + off, p.v + ((static_cast<int64_t>(b) * p.T + t0 + r) * p.Hv + hv) * kD + pc * 8);
+        else
+            *reinterpret_cast<uint4 *>(sm + PP_KN + off) = zero4;
+    }
+    cp_async_commit();
+    __syncthreads();
+
+    // ---- T = (I + A)^{-1} (warps 0-3)
+    if (warp < 4 && lane < 16) diag_solve(warp, lane, At, Tm);
+    __syncthreads();
+    if (warp < 4) solve_factors(warp, At, Tm, lane);
+    __syncthreads();
+    if (warp == 0 || warp == 3)
+        solve_column<1>(0, warp == 3 ? 1 : 0, At, Tm, lane);
+    else if (warp < 3)
+        solve_column<2>(warp, 0, At, Tm, lane);
+    __syncthreads();
+
+    // ---- T2 = T diag(beta) in bf16 over the G tile (rows of 64 columns)
+    for (int e = tid; e < kC * 8; e += 256) {
+        const int t = e >> 3, pc = e & 7, I = t >> 4, J = pc >> 1;
+        uint4 out = zero4;
+        if (J <= I) {
+            const float *src = Tm + blk(I, J) * kBlk + (t & 15) * kBS + (pc & 1) * 8;
+            const float *bc = beta_s + pc * 8;
+            out = make_uint4(pack2(src[0] * bc[0], src[1] * bc[1]), pack2(src[2] * bc[2], src[3] * bc[3]),
+                             pack2(src[4] * bc[4], src[5] * bc[5]), pack2(src[6] * bc[6], src[7] * bc[7]));
+        }
+        *reinterpret_cast<uint4 *>(sm + PP_T2 + sw128(t, pc)) = out;
+    }
+    cp_async_wait_all();
+    __syncthreads();
+
+    // ---- W = sum_J (T2[:, J] Kloc[J]) (.) e^{R_J} (Kp = Kloc (.) e^{R_J} on block J)
+    // and U~ = T2 V: warp w takes rows 16 (w & 3) and columns 64 (w >> 2) .. + 63.
+    {
+        const int mt = warp & 3, nh = warp >> 2;
+        float aw[8][4], au[8][4];
+#pragma unroll
+        for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) aw[nt][e] = au[nt][e] = 0.f;
+#pragma unroll
+        for (int J = 0; J < 4; ++J) {
+            if (J > mt) break;   // T2 is zero above the diagonal blocks
+            uint32_t af[4];
+            ldsm_x4(af, sb + PP_T2 + sw128(16 * mt + a_row(lane), 2 * J + a_ch(lane)));
+#pragma unroll
+            for (int np = 0; np < 4; ++np) {
+                uint32_t bk[4], bv[4];
+                ldsm_x4_t(bk, sb + PP_KL + sw256(16 * J + bt_row(lane), 8 * nh + 2 * np + bt_ch(lane)));
+                ldsm_x4_t(bv, sb + PP_KN + sw256(16 * J + bt_row(lane), 8 * nh + 2 * np + bt_ch(lane)));
+                float tw[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+                mma16816(tw[0], af, bk[0], bk[1]);
+                mma16816(tw[1], af, bk[2], bk[3]);
+                mma16816(au[2 * np], af, bv[0], bv[1]);
+                mma16816(au[2 * np + 1], af, bv[2], bv[3]);
+#pragma unroll
+                for (int jj = 0; jj < 2; ++jj) {
+                    const int col = 64 * nh + 16 * np + 8 * jj + 2 * t4;
+                    const float e0 = eR[J * kD + col], e1 = eR[J * kD + col + 1];
+                    aw[2 * np + jj][0] = fmaf(tw[jj][0], e0, aw[2 * np + jj][0]);
+                    aw[2 * np + jj][1] = fmaf(tw[jj][1], e1, aw[2 * np + jj][1]);
+                    aw[2 * np + jj][2] = fmaf(tw[jj][2], e0, aw[2 * np + jj][2]);
+                    aw[2 * np + jj][3] = fmaf(tw[jj][3], e1, aw[2 * np + jj][3]);
+                }
+            }
+        }
+#pragma unroll
+        for (int nt = 0; nt < 8; ++nt) {
+            const int col = 64 * nh + 8 * nt + 2 * t4;
+#pragma unroll
+            for (int hr = 0; hr < 2; ++hr) {
+                const int t = 16 * mt + g + 8 * hr;
+                *reinterpret_cast<uint32_t *>(rec + REC_WN + t * 256 + col * 2) =
+                    pack2(-aw[nt][2 * hr], -aw[nt][2 * hr + 1]);
+                *reinterpret_cast<uint32_t *>(rec + REC_UT + t * 256 + col * 2) = pack2(au[nt][2 * hr], au[nt][2 * hr + 1]);
+            }
+        }
+    }
+}
+
+// Chain shared memory: two stages of a chunk record (tiles swizzled), the bf16
+// copy of the state [dk][dv] and the bf16 U [tokens][dv].
+constexpr uint32_t CH_SB = 2 * kRecBytes;
+constexpr uint32_t CH_UB = CH_SB + kD * kD * 2;
+constexpr uint32_t CH_MISC = CH_UB + kC * kD * 2;
+constexpr uint32_t kChainSmem = CH_MISC + 64;
+
+// State scan of one (batch, value head, segment).  Warp w holds state rows
+// dk = 16w .. 16w+15 (all 128 dv columns) as MMA accumulator fragments.  Per
+// chunk, with the state S entering it:
+//   A: the bf16 copy of S to shared memory;
+//   B: U = U~ + (-W) S and Y = Qp S (warp w: tokens 16 (w & 3), columns 64 (w >> 2));
+//   C: Y += P U, y stored; S = diag(e^{g_C}) S + Kl^T U into the fragments.
+// Chunk records stream in with asynchronous copies one chunk ahead.
+__global__ void __launch_bounds__(256, 1) cw_chain_kernel(const CwDev p) {
+    extern __shared__ __align__(128) uint8_t sm[];
+    const uint32_t sb = smem_u32(sm);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int g = lane >> 2, t4 = lane & 3;
+    const int pairs = p.B * p.Hv;
+    const int pr = static_cast<int>(blockIdx.x % static_cast<unsigned>(pairs));
+    const int seg = static_cast<int>(blockIdx.x / static_cast<unsigned>(pairs));
+    const int b = pr / p.Hv, hv = pr % p.Hv;
+    const int c_begin = seg * p.seg_chunks;
+    const int c_end = c_begin + p.seg_chunks < p.nchunks ? c_begin + p.seg_chunks : p.nchunks;
+    int *misc = reinterpret_cast<int *>(sm + CH_MISC);
+
+    // Warm-up window: walk back from the segment start until the decay bound
+    // reaches exp(log_eps) (start there from a zero state); at chunk 0 or past
+    // the window limit, start at chunk 0 from S0 (exact).
+    if (tid == 0) {
+        int cw = 0;
+        if (seg > 0) {
+            float acc = 0.f;
+            for (int m = 1;; ++m) {
+                const int cc = c_begin - m;
+                if (cc < 0 || m > p.max_warmup) break;
+                acc += p.bound[static_cast<int64_t>(pr) * p.nchunks + cc];
+                if (acc <= p.log_eps) {
+                    cw = cc;
+                    break;
+                }
+            }
+        }
+        misc[0] = cw;
+    }
+    __syncthreads();
+    const int c_w = misc[0];
+
+    float S[16][4];
+    {
+        const float *s0 = (c_w == 0 && p.S0) ? p.S0 + static_cast<int64_t>(pr) * kD * kD : nullptr;
+#pragma unroll
+        for (int nt = 0; nt < 16; ++nt) {
+            const int r = 16 * warp + g, col = 8 * nt + 2 * t4;
+            float2 lo = make_float2(0.f, 0.f), hi = make_float2(0.f, 0.f);
+            if (s0) {
+                lo = *reinterpret_cast<const float2 *>(s0 + r * kD + col);
+                hi = *reinterpret_cast<const float2 *>(s0 + (r + 8) * kD + col);
+            }
+            S[nt][0] = lo.x;
+            S[nt][1] = lo.y;
+            S[nt][2] = hi.x;
+            S[nt][3] = hi.y;
+        }
+    }
+
+    const uint8_t *recs = p.rec + static_cast<int64_t>(pr) * p.nchunks * kRecBytes;
+    auto load_chunk = [&](int cc, int stage) {
+        const uint8_t *src = recs + static_cast<int64_t>(cc) * kRecBytes;
+        const uint32_t dst = sb + stage * kRecBytes;
+        for (int e = tid; e < 4 * 1024 + 512 + 32; e += 256) {
+            if (e < 4096) {
+                const int tile = e >> 10, r = (e >> 4) & 63, pc = e & 15;
+                cp_async16(dst + tile * 16384 + sw256(r, pc), src + tile * 16384 + r * 256 + pc * 16);
+            } else if (e < 4608) {
+                const int e2 = e - 4096, r = e2 >> 3, pc = e2 & 7;
+                cp_async16(dst + REC_P + sw128(r, pc), src + REC_P + r * 128 + pc * 16);
+            } else {
+                const int e3 = e - 4608;
+                cp_async16(dst + REC_GC + e3 * 16, src + REC_GC + e3 * 16);
+            }
+        }
+        cp_async_commit();
+    };
+
+    const int mt = warp & 3, nh = warp >> 2;
+    if (c_w < c_end) load_chunk(c_w, 0);
+#pragma unroll 1
+    for (int cc = c_w; cc < c_end; ++cc) {
+        const int st = (cc - c_w) & 1;
+        const uint32_t stg = sb + st * kRecBytes;
+        const uint8_t *stp = sm + st * kRecBytes;
+        // A: bf16 copy of the state
+#pragma unroll
+        for (int nt = 0; nt < 16; ++nt) {
+            const int r = 16 * warp + g;
+            *reinterpret_cast<uint32_t *>(sm + CH_SB + sw256(r, nt) + 4 * t4) = pack2(S[nt][0], S[nt][1]);
+            *reinterpret_cast<uint32_t *>(sm + CH_SB + sw256(r + 8, nt) + 4 * t4) = pack2(S[nt][2], S[nt][3]);
+        }
+        cp_async_wait_all();
+        __syncthreads();
+        if (cc + 1 < c_end) load_chunk(cc + 1, st ^ 1);
+
+        // B: U = U~ + (-W) S, Y = Qp S
+        float u[8][4], ys[8][4];
+#pragma unroll
+        for (int nt = 0; nt < 8; ++nt) {
+#pragma unroll
+            for (int hr = 0; hr < 2; ++hr) {
+                const int t = 16 * mt + g + 8 * hr;
+                const float2 f = unpack2(*reinterpret_cast<const uint32_t *>(stp + REC_UT + sw256(t, 8 * nh + nt) + 4 * t4));
+                u[nt][2 * hr] = f.x;
+                u[nt][2 * hr + 1] = f.y;
+                ys[nt][2 * hr] = 0.f;
+                ys[nt][2 * hr + 1] = 0.f;
+            }
+        }
+#pragma unroll 2
+        for (int kk = 0; kk < 8; ++kk) {
+            uint32_t aw[4], aq[4];
+            ldsm_x4(aw, stg + REC_WN + sw256(16 * mt + a_row(lane), 2 * kk + a_ch(lane)));
+            ldsm_x4(aq, stg + REC_QP + sw256(16 * mt + a_row(lane), 2 * kk + a_ch(lane)));
+#pragma unroll
+            for (int np = 0; np < 4; ++np) {
+                uint32_t bs[4];
+                ldsm_x4_t(bs, sb + CH_SB + sw256(16 * kk + bt_row(lane), 8 * nh + 2 * np + bt_ch(lane)));
+                mma16816(u[2 * np], aw, bs[0], bs[1]);
+                mma16816(u[2 * np + 1], aw, bs[2], bs[3]);
+                mma16816(ys[2 * np], aq, bs[0], bs[1]);
+                mma16816(ys[2 * np + 1], aq, bs[2], bs[3]);
+            }
+        }
+#pragma unroll
+        for (int nt = 0; nt < 8; ++nt) {
+            const int t = 16 * mt + g;
+            *reinterpret_cast<uint32_t *>(sm + CH_UB + sw256(t, 8 * nh + nt) + 4 * t4) = pack2(u[nt][0], u[nt][1]);
+            *reinterpret_cast<uint32_t *>(sm + CH_UB + sw256(t + 8, 8 * nh + nt) + 4 * t4) = pack2(u[nt][2], u[nt][3]);
+        }
+        __syncthreads();
+
+        // C: Y += P U (P is zero above the diagonal blocks)
+#pragma unroll 1
+        for (int kk = 0; kk <= mt; ++kk) {
+            uint32_t ap[4];
+            ldsm_x4(ap, stg + REC_P + sw128(16 * mt + a_row(lane), 2 * kk + a_ch(lane)));
+#pragma unroll
+            for (int np = 0; np < 4; ++np) {
+                uint32_t bu[4];
+                ldsm_x4_t(bu, sb + CH_UB + sw256(16 * kk + bt_row(lane), 8 * nh + 2 * np + bt_ch(lane)));
+                mma16816(ys[2 * np], ap, bu[0], bu[1]);
+                mma16816(ys[2 * np + 1], ap, bu[2], bu[3]);
+            }
+        }
+        if (cc >= c_begin) {
+#pragma unroll
+            for (int hr = 0; hr < 2; ++hr) {
+                const int64_t t = static_cast<int64_t>(cc) * kC + 16 * mt + g + 8 * hr;
+                if (t < p.T) {
+                    __nv_bfloat16 *yr = p.y + ((static_cast<int64_t>(b) * p.T + t) * p.Hv + hv) * kD + 64 * nh + 2 * t4;
+#pragma unroll
+                    for (int nt = 0; nt < 8; ++nt)
+                        *reinterpret_cast<uint32_t *>(yr + 8 * nt) = pack2(ys[nt][2 * hr], ys[nt][2 * hr + 1]);
+                }
+            }
+        }
+        // S = diag(e^{g_C}) S + Kl^T U
+        {
+            const float *gce = reinterpret_cast<const float *>(stp + REC_GC);
+            const float f0 = gce[16 * warp + g], f1 = gce[16 * warp + g + 8];
+#pragma unroll
+            for (int nt = 0; nt < 16; ++nt) {
+                S[nt][0] *= f0;
+                S[nt][1] *= f0;
+                S[nt][2] *= f1;
+                S[nt][3] *= f1;
+            }
+        }
+#pragma unroll 1
+        for (int kk = 0; kk < 4; ++kk) {
+            uint32_t ak[4];
+            ldsm_x4_t(ak, stg + REC_KL + sw256(16 * kk + at_row(lane), 2 * warp + at_ch(lane)));
+#pragma unroll
+            for (int np = 0; np < 8; ++np) {
+                uint32_t bu[4];
+                ldsm_x4_t(bu, sb + CH_UB + sw256(16 * kk + bt_row(lane), 2 * np + bt_ch(lane)));
+                mma16816(S[2 * np], ak, bu[0], bu[1]);
+                mma16816(S[2 * np + 1], ak, bu[2], bu[3]);
+            }
+        }
+    }
+
+    if (c_end == p.nchunks && p.S_T) {
+        float *so = p.S_T + static_cast<int64_t>(pr) * kD * kD;
+#pragma unroll
+        for (int nt = 0; nt < 16; ++nt) {
+            const int r = 16 * warp + g, col = 8 * nt + 2 * t4;
+            *reinterpret_cast<float2 *>(so + r * kD + col) = make_float2(S[nt][0], S[nt][1]);
+            *reinterpret_cast<float2 *>(so + (r + 8) * kD + col) = make_float2(S[nt][2], S[nt][3]);
+        }
+    }
+}
+
+cudaError_t set_cw_attributes() {
+    static cudaError_t result = [] {
+        cudaError_t e = cudaFuncSetAttribute(cw_prepass_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(kPrepassSmem));
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(cw_chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     static_cast<int>(kChainSmem));
+        return e;
+    }();
+    return result;
+}
+
+}  // namespace
+
+size_t chunked_cw_ops_bytes(int64_t B, int64_t T, int Hv) {
+    const int64_t nchunks = (T + kC - 1) / kC;
+    return static_cast<size_t>(B) * Hv * nchunks * (kRecBytes + sizeof(float));
+}
+
+cudaError_t launch_chunked_cw(const ChunkedCwParams &p, cudaStream_t stream, int num_sms) {
+    if (p.d != kD) return cudaErrorInvalidValue;
+    const int64_t nchunks = (p.T + kC - 1) / kC;
+    const int64_t pairs = p.B * p.Hv;
+    if (nchunks <= 0 || pairs <= 0) return cudaSuccess;
+    if (nchunks > 0x7fffffffLL || pairs > 0x7fffffffLL || p.B * nchunks * p.Hv > 0x7fffffffLL)
+        return cudaErrorInvalidValue;
+    int P = plan_segments(pairs, nchunks, num_sms, p.segments);
+    const int64_t len = (nchunks + P - 1) / P;
+    P = static_cast<int>((nchunks + len - 1) / len);
+    if (pairs * P > 0x7fffffffLL) return cudaErrorInvalidValue;
+    cudaError_t e = set_cw_attributes();
+    if (e != cudaSuccess) return e;
+    CwDev dv{};
+    dv.T = p.T;
+    dv.B = static_cast<int>(p.B);
+    dv.Hqk = p.Hqk;
+    dv.Hv = p.Hv;
+    dv.group = p.group;
+    dv.nchunks = static_cast<int>(nchunks);
+    dv.seg_chunks = static_cast<int>(len);
+    dv.max_warmup = p.max_warmup_chunks;
+    dv.log_eps = p.log_eps;
+    dv.q = static_cast<const __nv_bfloat16 *>(p.q);
+    dv.k = static_cast<const __nv_bfloat16 *>(p.k);
+    dv.v = static_cast<const __nv_bfloat16 *>(p.v);
+    dv.alpha = p.alpha;
+    dv.beta = p.beta;
+    dv.S0 = p.S0;
+    dv.y = static_cast<__nv_bfloat16 *>(p.y);
+    dv.S_T = p.S_T;
+    dv.rec = p.ops;
+    dv.bound = reinterpret_cast<float *>(p.ops + static_cast<size_t>(pairs) * nchunks * kRecBytes);
+    cw_prepass_kernel<<<static_cast<unsigned>(p.B * nchunks * p.Hv), 256, kPrepassSmem, stream>>>(dv);
+    cw_chain_kernel<<<static_cast<unsigned>(pairs * P), 256, kChainSmem, stream>>>(dv);
+    return cudaGetLastError();
+}
+
+}  // namespace gdn

@@ -69,6 +69,28 @@ bool takes_exact_split(int64_t pairs, int64_t nchunks, int P, int d, size_t seg_
 // Chunked tensor-core prefill (bf16).  Builds the TMA descriptors and launches.
 cudaError_t launch_chunked(const ChunkedParams &p, cudaStream_t stream, int num_sms);
 
+// Chunked prefill with the channel-wise decay gate (bf16, d = 128): a
+// per-chunk pre-pass writes each chunk's state-independent operands into the
+// workspace (`ops`), then a chain kernel runs the state scan over them.
+struct ChunkedCwParams {
+    int64_t B, T;
+    int Hqk, Hv, group, d;
+    const void *q, *k, *v;
+    const float *alpha, *beta;   // alpha [B, T, Hv, d]
+    const float *S0;             // nullptr = zero state
+    void *y;
+    float *S_T;
+    int segments;
+    float log_eps;
+    int max_warmup_chunks;
+    uint8_t *ops;                // chunked_cw_ops_bytes(B, T, Hv) bytes, 16-byte aligned
+};
+
+// Bytes of one chunk's operand record in the workspace.
+constexpr size_t kCwChunkBytes = 74240;
+size_t chunked_cw_ops_bytes(int64_t B, int64_t T, int Hv);
+cudaError_t launch_chunked_cw(const ChunkedCwParams &p, cudaStream_t stream, int num_sms);
+
 // Tokens between two checkpoints of the backward pass (and its chunk length).
 constexpr int kBackwardCheckpointTokens = 8;
 

@@ -29,7 +29,8 @@ EXPORTS = ("gdn_status_string", "gdn_prefill_workspace_bytes", "gdn_prefill", "g
            "gdn_decode_step", "gdn_read_device_status", "gdn_device_supported", "gdn_abi_version",
            "gdn_prefill_noalloc", "gdn_layer_prologue", "gdn_layer_epilogue", "gdn_prefill_host_workspace_bytes",
            "gdn_prefill_host", "gdn_prefill_cw", "gdn_decode_step_cw", "gdn_backward_workspace_bytes",
-           "gdn_backward", "gdn_prefill_noalloc_status", "gdn_prefill_launches")
+           "gdn_backward", "gdn_prefill_noalloc_status", "gdn_prefill_launches",
+           "gdn_prefill_cw_workspace_bytes", "gdn_prefill_cw_ex")
 NOALLOC_SCRATCH_BYTES = 256 + 8 * 1024 * 1024
 
 
@@ -79,6 +80,11 @@ def lib() -> ctypes.CDLL:
             L.gdn_status_string.argtypes = [ctypes.c_int]
             L.gdn_prefill_workspace_bytes.restype = c_size
             L.gdn_prefill_workspace_bytes.argtypes = [sp]
+            L.gdn_prefill_cw_workspace_bytes.restype = c_size
+            L.gdn_prefill_cw_workspace_bytes.argtypes = [sp]
+            L.gdn_prefill_cw_ex.restype = ctypes.c_int
+            L.gdn_prefill_cw_ex.argtypes = [sp, ctypes.POINTER(GdnPrefillOptions), vp, vp, vp, fp, fp, fp, vp, fp, vp,
+                                            c_size, vp]
             L.gdn_prefill_launches.restype = ctypes.c_int
             L.gdn_prefill_launches.argtypes = [sp, ctypes.POINTER(GdnPrefillOptions)]
             L.gdn_prefill.restype = ctypes.c_int
@@ -324,18 +330,35 @@ def prefill_host(q, k, v, alpha, beta, S0=None, *, y=None, S_T=None, workspace=N
     return y, S_T
 
 
-def prefill_cw(q, k, v, alpha, beta, S0=None, *, y=None, S_T=None, stream=None):
-    """Run gdn_prefill_cw (channel-wise decay, alpha [B,T,Hv,dk] fp32); returns (y, S_T)."""
+def prefill_cw(q, k, v, alpha, beta, S0=None, *, y=None, S_T=None, workspace=None, algorithm=ALGO_AUTO, segments=0,
+               log_eps=0.0, max_warmup_chunks=0, stream=None):
+    """Run gdn_prefill_cw_ex (channel-wise decay, alpha [B,T,Hv,dk] fp32); returns (y, S_T).
+    bf16 with d = 128 takes the chunked tensor-core path, whose workspace is allocated here
+    (on the call's stream) unless given."""
     _require(dict(q=q, k=k, v=v, alpha=alpha, beta=beta, S0=S0, y=y, S_T=S_T))
     shape = shape_of(q, v)
     if y is None:
         y = torch.empty_like(v)
     if S_T is None:
         S_T = torch.empty((shape.B, shape.Hv, shape.dk, shape.dv), dtype=torch.float32, device=v.device)
-    rc = lib().gdn_prefill_cw(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(beta), _ptr(S0),
-                              _ptr(y), _ptr(S_T), _stream(stream))
-    _check(rc, "gdn_prefill_cw")
+    if workspace is None:
+        workspace = new_cw_workspace(shape, v.device)
+    opts = GdnPrefillOptions(segments, log_eps, max_warmup_chunks, algorithm, 0)
+    rc = lib().gdn_prefill_cw_ex(ctypes.byref(shape), ctypes.byref(opts), _ptr(q), _ptr(k), _ptr(v), _ptr(alpha),
+                                 _ptr(beta), _ptr(S0), _ptr(y), _ptr(S_T), _ptr(workspace), workspace.numel(),
+                                 _stream(stream))
+    _check(rc, "gdn_prefill_cw_ex")
     return y, S_T
+
+
+def cw_workspace_bytes(shape: GdnShape) -> int:
+    return int(lib().gdn_prefill_cw_workspace_bytes(ctypes.byref(shape)))
+
+
+def new_cw_workspace(shape: GdnShape, device) -> torch.Tensor:
+    """Workspace of gdn_prefill_cw_ex (uint8, 256-byte aligned by the allocator; every byte
+    the chunked path reads it writes first, so it is not cleared)."""
+    return torch.empty(max(cw_workspace_bytes(shape), 256), dtype=torch.uint8, device=device)
 
 
 def decode_step_cw(q, k, v, alpha, beta, S, *, y=None, stream=None):
