@@ -14,7 +14,8 @@ and the backward pass (gradients of the recurrence) on the training-shape
 workload (B=2, H=16, T=4096, d=128, bf16) under "backward".  The other
 prefill workloads are timed beside it: the training shape ("prefill_train"),
 the long-context prefill (B=1, H=16, T=2^20, "prefill_long") and the grouped
-shape with gates that barely decay ("prefill_weak_decay"), each with its
+shape with gates that barely decay ("prefill_weak_decay") and the grouped
+shape with the channel-wise decay gate ("prefill_channelwise"), each with its
 rooflines and an oracle sample.  The line ends with "summary", the headline
 number of every section.
 
@@ -62,11 +63,12 @@ def useful_flops_per_token_head(d: int, group: int, chunk: int = CHUNK) -> float
     return 2.0 * (3 * d * d + (chunk / 2) * (d + 2 * d) + (chunk / 2) * (2 * d) / group)
 
 
-def prefill_bytes(w: dict, esz: int = 2) -> int:
-    """Algorithmic HBM bytes of one prefill: q, k, v, y, alpha, beta, S0 and S_T once each."""
+def prefill_bytes(w: dict, esz: int = 2, channelwise: bool = False) -> int:
+    """Algorithmic HBM bytes of one prefill: q, k, v, y, alpha, beta, S0 and S_T once each
+    (alpha [B, T, Hv, d] with the channel-wise gate)."""
     B, T, Hqk, Hv, d = w["B"], w["T"], w["Hqk"], w["Hv"], w["d"]
     io = (2 * B * T * Hqk * d + 2 * B * T * Hv * d) * esz
-    gates = 2 * B * T * Hv * 4
+    gates = (d + 1 if channelwise else 2) * B * T * Hv * 4
     state = (2 if w.get("s0_std", 0) > 0 else 1) * B * Hv * d * d * 4
     return io + gates + state
 
@@ -203,14 +205,15 @@ def max_over_ranks(x: float, ws: int, device) -> float:
 
 
 # ----------------------------------------------------------------- oracle timing
-def time_oracle_prefill(w: dict, seed: int, target_s: float, device="cpu", label: str = PREFILL_WORKLOAD):
+def time_oracle_prefill(w: dict, seed: int, target_s: float, device="cpu", label: str = PREFILL_WORKLOAD,
+                        channelwise: bool = False):
     """Time the fp64 oracle on the first T_s tokens of the workload (all heads).
 
     Returns (tokens/s, sample description, threads).  T_s is grown until one
     run takes about target_s seconds (bounded by the workload's T).
     """
     import oracle
-    from linear_attention_recurrence_14_b300.inputs import make_prefill_inputs
+    from linear_attention_recurrence_14_b300.inputs import make_channelwise_alpha, make_prefill_inputs
 
     oracle.build()
     threads = os.cpu_count() or 1
@@ -218,6 +221,8 @@ def time_oracle_prefill(w: dict, seed: int, target_s: float, device="cpu", label
     while True:
         x = make_prefill_inputs(w["B"], Ts, w["Hqk"], w["Hv"], w["d"], w["dtype"], w["decay_scale"], w["s0_std"],
                                 seed=seed, device=device)
+        if channelwise:
+            x.alpha = make_channelwise_alpha(w["B"], Ts, w["Hv"], w["d"], w["decay_scale"], seed=seed, device=device)
         t0 = time.perf_counter()
         oracle.recurrence(x.q, x.k, x.v, x.alpha, x.beta, x.S0, threads=threads)
         dt = time.perf_counter() - t0
@@ -450,6 +455,8 @@ def run_ours(args, ws, rank, local):
     if not args.no_prefill_configs:
         for name, nlaunch in (("train", 20), ("weak", 5), ("long", 3)):
             prefills[name] = time_prefill_section(args, peaks, seed, dev, ws, local, name, nlaunch)
+        prefills["channelwise"] = time_prefill_section(args, peaks, seed, dev, ws, local, "grouped", 5,
+                                                       channelwise=True)
 
     # ------------------------------------------------------------- decode
     dec = dec_cw = None
@@ -488,7 +495,8 @@ def run_ours(args, ws, rank, local):
         "roofline": roofline, "clocks": clocks, "e2e": e2e, "cpu_baseline": cpu, "gpu_launches": gpu_launches,
         "check": check, "layer": layer, "backward": bwd,
         "prefill_train": prefills.get("train"), "prefill_long": prefills.get("long"),
-        "prefill_weak_decay": prefills.get("weak"), "decode": dec, "decode_channelwise": dec_cw,
+        "prefill_weak_decay": prefills.get("weak"), "prefill_channelwise": prefills.get("channelwise"),
+        "decode": dec, "decode_channelwise": dec_cw,
     }
     # Last, so that a reader of the line's tail sees every section: its headline numbers.
     line["summary"] = summarize(line)
@@ -496,14 +504,16 @@ def run_ours(args, ws, rank, local):
         print(json.dumps(line), flush=True)
 
 
-def time_prefill_section(args, peaks, seed, dev, ws, local, name: str, launches_timed: int = 10) -> dict:
+def time_prefill_section(args, peaks, seed, dev, ws, local, name: str, launches_timed: int = 10,
+                         channelwise: bool = False) -> dict:
     """gdn_prefill on another prefill workload (name in WORKLOADS): the median of `launches_timed`
     launches (CUDA events on the launching stream), its HBM and tensor-core rooflines, clocks, and
-    the oracle on a bounded prefix of the same workload."""
+    the oracle on a bounded prefix of the same workload.  channelwise: the same workload with the
+    channel-wise decay gate (alpha [B, T, Hv, d], same gate scale) through gdn_prefill_cw_ex."""
     import torch
 
     from linear_attention_recurrence_14_b300 import gdn
-    from linear_attention_recurrence_14_b300.inputs import WORKLOADS, make_prefill_inputs
+    from linear_attention_recurrence_14_b300.inputs import WORKLOADS, make_channelwise_alpha, make_prefill_inputs
 
     w = dict(WORKLOADS[name])
     x = make_prefill_inputs(w["B"], w["T"], w["Hqk"], w["Hv"], w["d"], w["dtype"], w["decay_scale"], w["s0_std"],
@@ -511,15 +521,23 @@ def time_prefill_section(args, peaks, seed, dev, ws, local, name: str, launches_
     shape = gdn.shape_of(x.q, x.v)
     y = torch.empty_like(x.v)
     S_T = torch.empty((w["B"], w["Hv"], w["d"], w["d"]), dtype=torch.float32, device=dev)
-    wsb = gdn.new_workspace(shape, dev)
+    if channelwise:
+        x.alpha = make_channelwise_alpha(w["B"], w["T"], w["Hv"], w["d"], w["decay_scale"], seed=seed, device=dev)
+        wsb = gdn.new_cw_workspace(shape, dev)
+        wstat = gdn.new_workspace(shape, dev)   # status word only: read for uniformity with the scalar path
 
-    def fn():
-        gdn.prefill(x.q, x.k, x.v, x.alpha, x.beta, x.S0, y=y, S_T=S_T, workspace=wsb)
+        def fn():
+            gdn.prefill_cw(x.q, x.k, x.v, x.alpha, x.beta, x.S0, y=y, S_T=S_T, workspace=wsb)
+    else:
+        wsb = wstat = gdn.new_workspace(shape, dev)
+
+        def fn():
+            gdn.prefill(x.q, x.k, x.v, x.alpha, x.beta, x.S0, y=y, S_T=S_T, workspace=wsb)
 
     for _ in range(max(3, args.warmup)):
         fn()
     torch.cuda.synchronize()
-    if gdn.read_device_status(wsb) != 0:
+    if gdn.read_device_status(wstat) != 0:
         raise SystemExit(f"device status error in the {name} prefill")
     stream = torch.cuda.current_stream()
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(launches_timed)]
@@ -530,18 +548,19 @@ def time_prefill_section(args, peaks, seed, dev, ws, local, name: str, launches_
             fn()
             b.record(stream)
         torch.cuda.synchronize()
-    if gdn.read_device_status(wsb) != 0:
+    if gdn.read_device_status(wstat) != 0:
         raise SystemExit(f"device status error in the {name} prefill")
     ms = max_over_ranks(statistics.median(a.elapsed_time(b) for a, b in evs), ws, dev)
-    nbytes = prefill_bytes(w)
-    flops = useful_flops_per_token_head(w["d"], w["Hv"] // w["Hqk"]) * w["B"] * w["T"] * w["Hv"]
+    nbytes = prefill_bytes(w, channelwise=channelwise)
+    # channel-wise: every value head forms its own gated keys, so no Gram product is shared
+    flops = useful_flops_per_token_head(w["d"], 1 if channelwise else w["Hv"] // w["Hqk"]) * w["B"] * w["T"] * w["Hv"]
     gbs = nbytes / (ms * 1e-3) / 1e9
     tf = flops / (ms * 1e-3) / 1e12
     out = {
         "workload": f"{name}: B={w['B']}, T={w['T']}, Hqk={w['Hqk']}, Hv={w['Hv']}, d={w['d']}, {w['dtype']} q/k/v, "
-                    f"gate scale {w['decay_scale']}, S0 std {w['s0_std']}",
+                    f"{'channel-wise ' if channelwise else ''}gate scale {w['decay_scale']}, S0 std {w['s0_std']}",
         "ms": ms, "tokens_per_s": w["B"] * w["T"] * ws / (ms * 1e-3),
-        "gpu_launches": gdn.prefill_launches(shape) * launches_timed,
+        "gpu_launches": (2 if channelwise else gdn.prefill_launches(shape)) * launches_timed,
         "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": gbs / peaks["hbm_gbs"], "traffic": None, "bytes_per_launch": nbytes,
                      "peak_source": peaks["source"],
@@ -551,11 +570,14 @@ def time_prefill_section(args, peaks, seed, dev, ws, local, name: str, launches_
         "l2": f"inputs {nbytes / 1e9:.2f} GB per launch" + (" (larger than L2, no flush)" if nbytes > 126e6 else
                                                             " (fit in L2: timed back to back)"),
     }
-    del x, y, S_T, wsb
+    if channelwise:
+        out["kernels"] = "cw_prepass_kernel (per chunk) + cw_chain_kernel (per head and segment); roofline over both"
+    del x, y, S_T, wsb, wstat
     torch.cuda.empty_cache()
     if local == 0 and not args.no_cpu_baseline:
         def oracle_rate():
-            v, sample, threads, _ = time_oracle_prefill(w, seed, args.oracle_seconds, label=name)
+            v, sample, threads, _ = time_oracle_prefill(w, seed, args.oracle_seconds, label=name,
+                                                        channelwise=channelwise)
             return {"value": v, "unit": "tokens/s", "cores": threads, "kind": "oracle", "sample": sample}
         out["cpu_baseline"] = _oracle_timed(oracle_rate, f"{name} oracle")
     return out
@@ -573,7 +595,8 @@ def summarize(line: dict) -> dict:
     out = {"grouped_ms": g(line, "roofline", "launch_ms"), "grouped_hbm": g(line, "roofline", "frac"),
            "grouped_tc": g(line, "roofline", "tensor", "frac"), "e2e_ms": g(line, "e2e", "ms_per_step"),
            "check_err": g(line, "check", "max_rel_err_y")}
-    for key, short in (("prefill_train", "train"), ("prefill_long", "long"), ("prefill_weak_decay", "weak")):
+    for key, short in (("prefill_train", "train"), ("prefill_long", "long"), ("prefill_weak_decay", "weak"),
+                       ("prefill_channelwise", "cw")):
         out[f"{short}_ms"] = g(line, key, "ms")
         out[f"{short}_hbm"] = g(line, key, "roofline", "frac")
     out["decode_steps_s"] = g(line, "decode", "value")
