@@ -340,6 +340,36 @@ gdn_status gdn_backward(const gdn_shape *shape,
                         float *dq, float *dk, float *dv, float *dlog_alpha, float *dbeta, float *dS0,
                         void *ws, size_t ws_bytes, void *stream);
 
+/*
+ * Chunked backward on the tensor cores: the same gradients, arguments,
+ * layouts and aliasing rules as gdn_backward, for bf16 q, k, v, dy with
+ * dk = dv = 128 (else GDN_ERR_UNSUPPORTED).  It runs the chunk algebra of the
+ * forward in reverse: a pre-pass forms every 64-token chunk's operands, a
+ * forward chain writes the state entering every chunk, a reverse chain carries
+ * dS (dU = P^T dY + Kl dS', dS = gamma_C dS' + Qp^T dY - W^T dU) and writes
+ * the state gradient leaving every chunk, and a per-chunk kernel forms dq, dk,
+ * dv, dbeta and dlog alpha from those (through dA = -T^T dT T^T of the chunk's
+ * lower-triangular inverse T = (I + A)^{-1}).  Products take bf16 operands
+ * with fp32 accumulation, so results carry bf16-level rounding (about 1e-2
+ * of the largest gradient), unlike gdn_backward's fp32 arithmetic; the state
+ * chains split long sequences into segments with warm-up windows, as the
+ * prefill does.  dq and dk are summed over the value heads of a group with
+ * atomic additions (deterministic for up to two value heads per key head).
+ * ws: device memory of gdn_backward_chunked_workspace_bytes(shape) bytes,
+ * 256-byte aligned, no initial contents needed (74,244 bytes of chunk
+ * operands plus two 64 KB states per (batch, value head, chunk), then
+ * B*Hv*dk*dv fp32 to stage dS0 when it is dS_T's buffer).  Returns 0 bytes for
+ * shapes the chunked path does not take.
+ */
+size_t gdn_backward_chunked_workspace_bytes(const gdn_shape *shape);
+
+gdn_status gdn_backward_chunked(const gdn_shape *shape,
+                                const void *q, const void *k, const void *v,
+                                const float *alpha, const float *beta, const float *S0,
+                                const void *dy, const float *dS_T,
+                                float *dq, float *dk, float *dv, float *dlog_alpha, float *dbeta, float *dS0,
+                                void *ws, size_t ws_bytes, void *stream);
+
 /* 1 if the current CUDA device can run these kernels (compute capability 10.3). */
 int gdn_device_supported(void);
 

@@ -493,18 +493,18 @@ size_t gdn_backward_workspace_bytes(const gdn_shape *shape) {
     return backward_workspace(shape, &bytes) == GDN_OK ? bytes : 0;
 }
 
-gdn_status gdn_backward(const gdn_shape *shape, const void *q, const void *k, const void *v, const float *alpha,
-                        const float *beta, const float *S0, const void *dy, const float *dS_T, float *dq, float *dk,
-                        float *dv, float *dlog_alpha, float *dbeta, float *dS0, void *ws, size_t ws_bytes,
-                        void *stream_) {
+// Argument checks shared by both backward entry points (need: workspace bytes
+// the chosen path requires).  Returns GDN_OK with *done set when nothing is
+// left to launch (empty problem handled), else GDN_OK with *done clear.
+static gdn_status backward_prologue(const gdn_shape *shape, const void *q, const void *k, const void *v,
+                                    const float *alpha, const float *beta, const float *S0, const void *dy,
+                                    const float *dS_T, float *dq, float *dk, float *dv, float *dlog_alpha,
+                                    float *dbeta, float *dS0, void *ws, size_t ws_bytes, size_t need, void *stream_,
+                                    int *num_sms, bool *done) {
     int64_t n_qk, n_v, n_gate, n_state;
     gdn_status st = check_shape(shape, &n_qk, &n_v, &n_gate, &n_state);
     if (st != GDN_OK) return st;
-    // Per-token offsets inside the kernel are 32-bit: bound the head count times the head dim.
-    if (static_cast<int64_t>(shape->Hv) * shape->dk > (int64_t(1) << 24)) return GDN_ERR_UNSUPPORTED;
-    size_t need = 0;
-    st = backward_workspace(shape, &need);
-    if (st != GDN_OK) return st;
+    *done = false;
     const gdn_shape &s = *shape;
     const bool has_tokens = s.B * s.T > 0;
     if (has_tokens && (!q || !k || !v || !alpha || !beta || !dy || !dq || !dk || !dv || !dlog_alpha || !dbeta))
@@ -537,19 +537,43 @@ gdn_status gdn_backward(const gdn_shape *shape, const void *q, const void *k, co
             if (overlap(outs[o], outs[o2])) return GDN_ERR_ALIASING;
     }
 
-    int num_sms = 0;
-    st = check_device(&num_sms);
+    st = check_device(num_sms);
     if (st != GDN_OK) return st;
     cudaStream_t stream = static_cast<cudaStream_t>(stream_);
-    if (s.B * s.Hv == 0) return GDN_OK;
+    if (s.B * s.Hv == 0) {
+        *done = true;
+        return GDN_OK;
+    }
     if (!has_tokens) {
         // No tokens: dS0 = dS_T; there is nothing else to return.
+        *done = true;
         if (dS0 && !ds_in_place) {
             if (dS_T) return from_cuda(cudaMemcpyAsync(dS0, dS_T, rds0.n, cudaMemcpyDeviceToDevice, stream));
             return from_cuda(cudaMemsetAsync(dS0, 0, rds0.n, stream));
         }
-        return GDN_OK;
     }
+    return GDN_OK;
+}
+
+gdn_status gdn_backward(const gdn_shape *shape, const void *q, const void *k, const void *v, const float *alpha,
+                        const float *beta, const float *S0, const void *dy, const float *dS_T, float *dq, float *dk,
+                        float *dv, float *dlog_alpha, float *dbeta, float *dS0, void *ws, size_t ws_bytes,
+                        void *stream_) {
+    int64_t n_qk, n_v, n_gate, n_state;
+    gdn_status st = check_shape(shape, &n_qk, &n_v, &n_gate, &n_state);
+    if (st != GDN_OK) return st;
+    // Per-token offsets inside the kernel are 32-bit: bound the head count times the head dim.
+    if (static_cast<int64_t>(shape->Hv) * shape->dk > (int64_t(1) << 24)) return GDN_ERR_UNSUPPORTED;
+    size_t need = 0;
+    st = backward_workspace(shape, &need);
+    if (st != GDN_OK) return st;
+    int num_sms = 0;
+    bool done = false;
+    st = backward_prologue(shape, q, k, v, alpha, beta, S0, dy, dS_T, dq, dk, dv, dlog_alpha, dbeta, dS0, ws,
+                           ws_bytes, need, stream_, &num_sms, &done);
+    if (st != GDN_OK || done) return st;
+    const gdn_shape &s = *shape;
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_);
 
     size_t o_dq = 0, o_dk = 0, o_b = 0, o_g = 0;
     gdn::backward_workspace_layout(s.B, s.T, s.Hv, s.dk, &o_dq, &o_dk, &o_b, &o_g);
@@ -564,6 +588,50 @@ gdn_status gdn_backward(const gdn_shape *shape, const void *q, const void *k, co
     p.part_dbeta = reinterpret_cast<float *>(w + o_b);
     p.part_dlog_alpha = reinterpret_cast<float *>(w + o_g);
     return from_cuda(gdn::launch_backward(p, s.dk, static_cast<gdn_dtype>(s.dtype), stream, num_sms));
+}
+
+// Chunked backward workspace: the chunk records, the states entering and the
+// state gradients leaving every chunk, then (for dS0 == dS_T) dS0's staging.
+size_t gdn_backward_chunked_workspace_bytes(const gdn_shape *shape) {
+    int64_t n_qk, n_v, n_gate, n_state;
+    if (check_shape(shape, &n_qk, &n_v, &n_gate, &n_state) != GDN_OK) return 0;
+    if (shape->dtype != GDN_BF16 || shape->dk != 128 || shape->dv != 128) return 0;
+    return round256(gdn::backward_chunked_workspace_bytes(shape->B, shape->T, shape->Hv)) +
+           static_cast<size_t>(n_state) * sizeof(float);
+}
+
+gdn_status gdn_backward_chunked(const gdn_shape *shape, const void *q, const void *k, const void *v,
+                                const float *alpha, const float *beta, const float *S0, const void *dy,
+                                const float *dS_T, float *dq, float *dk, float *dv, float *dlog_alpha, float *dbeta,
+                                float *dS0, void *ws, size_t ws_bytes, void *stream_) {
+    int64_t n_qk, n_v, n_gate, n_state;
+    gdn_status st = check_shape(shape, &n_qk, &n_v, &n_gate, &n_state);
+    if (st != GDN_OK) return st;
+    if (shape->dtype != GDN_BF16 || shape->dk != 128 || shape->dv != 128) return GDN_ERR_UNSUPPORTED;
+    const size_t need = gdn_backward_chunked_workspace_bytes(shape);
+    int num_sms = 0;
+    bool done = false;
+    st = backward_prologue(shape, q, k, v, alpha, beta, S0, dy, dS_T, dq, dk, dv, dlog_alpha, dbeta, dS0, ws,
+                           ws_bytes, need, stream_, &num_sms, &done);
+    if (st != GDN_OK || done) return st;
+    const gdn_shape &s = *shape;
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+    uint8_t *w = static_cast<uint8_t *>(ws);
+    const size_t off_stage = round256(gdn::backward_chunked_workspace_bytes(s.B, s.T, s.Hv));
+    // dS0 over dS_T: segments of one head run on different CTAs, so stage dS0
+    const bool ds_in_place = dS0 && dS0 == dS_T;
+    float *staging = reinterpret_cast<float *>(w + off_stage);
+    gdn::BackwardParams p{};
+    p.B = s.B; p.T = s.T; p.Hqk = s.Hqk; p.Hv = s.Hv; p.group = s.Hv / s.Hqk;
+    p.q = q; p.k = k; p.v = v; p.dy = dy; p.alpha = alpha; p.beta = beta; p.S0 = S0; p.dS_T = dS_T;
+    p.dq = dq; p.dk = dk; p.dv = dv; p.dlog_alpha = dlog_alpha; p.dbeta = dbeta;
+    p.dS0 = ds_in_place ? staging : dS0;
+    st = from_cuda(gdn::launch_backward_chunked(p, w, stream, num_sms));
+    if (st != GDN_OK) return st;
+    if (ds_in_place)
+        return from_cuda(cudaMemcpyAsync(dS0, staging, static_cast<size_t>(n_state) * sizeof(float),
+                                         cudaMemcpyDeviceToDevice, stream));
+    return GDN_OK;
 }
 
 gdn_status gdn_read_device_status(void *ws, void *stream_) {

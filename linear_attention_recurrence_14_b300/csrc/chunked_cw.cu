@@ -22,6 +22,8 @@
 // the block's own decay for s inside it.  A block whose decay exceeds e^80 in
 // some channel (far beyond any gate of a trained layer) has its diagonal part
 // computed element by element instead, so the result holds for every gate.
+// The pre-pass keeps G in base 2 (cumulative log2 alpha) and takes every
+// power with one ex2.
 //
 // Two kernels.  cw_prepass_kernel, one CTA per (batch, value head, chunk),
 // computes everything that does not depend on the state and writes it to the
@@ -37,13 +39,20 @@
 #include <cstdint>
 
 #include "gdn_internal.h"
+#include "warp_mma.cuh"
 
 namespace gdn {
 namespace {
 
+using namespace wm;
+
 constexpr int kC = 64;             // tokens per chunk
 constexpr int kD = 128;            // head dimension (dk = dv)
-constexpr float kMaxExp = 80.f;    // largest exponent taken through a bf16 operand
+// Exponents are kept in base 2 (G holds cumulative log2 alpha): the largest
+// power of two taken through a bf16 operand is 2^115 (about e^80).
+constexpr float kMaxExp2 = 115.f;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
 
 // Chunk record in the workspace, per (batch, value head, chunk); tiles are
 // row-major bf16 [64][128] (P: [64][64]), rows 256 (128) bytes.
@@ -55,191 +64,6 @@ constexpr uint32_t REC_P = 65536;       // P (zero above the diagonal)
 constexpr uint32_t REC_GC = 73728;      // e^{g_C}, fp32 [128]
 constexpr uint32_t kRecBytes = 74240;
 static_assert(kRecBytes == kCwChunkBytes, "chunk record size");
-
-// ---------------------------------------------------------------- helpers
-
-__device__ __forceinline__ uint32_t smem_u32(const void *p) {
-    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-// Byte offset of the 16-byte piece `ch` of row `row` in a tile of 256-byte
-// rows (16 pieces) or 128-byte rows (8 pieces), XOR-swizzled by the row so
-// that eight rows read at the same column fall in different banks.
-__device__ __forceinline__ uint32_t sw256(int row, int ch) { return row * 256 + ((ch ^ (row & 7)) << 4); }
-__device__ __forceinline__ uint32_t sw128(int row, int ch) { return row * 128 + ((ch ^ (row & 7)) << 4); }
-
-__device__ __forceinline__ void cp_async16(uint32_t saddr, const void *g) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(saddr), "l"(g) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
-
-__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], uint32_t a) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-                 : "r"(a));
-}
-__device__ __forceinline__ void ldsm_x4_t(uint32_t (&r)[4], uint32_t a) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-                 : "r"(a));
-}
-
-// d (16 x 8 fp32) += a (16 x 16 bf16, row) * b (16 x 8 bf16, col).
-__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
-        "{%0, %1, %2, %3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-
-// d (16 x 8 fp32) += a (16 x 8 tf32, row) * b (8 x 8 tf32, col).
-__device__ __forceinline__ void mma_tf32(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                         uint32_t b0, uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
-        "{%0, %1, %2, %3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
-__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
-    const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-    return *reinterpret_cast<const uint32_t *>(&v);
-}
-__device__ __forceinline__ float2 unpack2(uint32_t w) {
-    return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
-}
-
-// Lane addresses of ldmatrix x4 loads (16 x 16 pieces of bf16 tiles).
-//  A, row-major [m][k] storage: matrices (m 0-7, k 0-7), (m 8-15, k 0-7), (m 0-7, k 8-15), (m 8-15, k 8-15).
-__device__ __forceinline__ int a_row(int lane) { return (lane & 7) + 8 * ((lane >> 3) & 1); }
-__device__ __forceinline__ int a_ch(int lane) { return lane >> 4; }
-//  B from [n][k] storage (no transpose), two n-tiles: (n 0-7, k 0-7), (n 0-7, k 8-15), (n 8-15, k 0-7), (n 8-15, k 8-15).
-__device__ __forceinline__ int bn_row(int lane) { return (lane & 7) + 8 * (lane >> 4); }
-__device__ __forceinline__ int bn_ch(int lane) { return (lane >> 3) & 1; }
-//  B from [k][n] storage (transposed load), two n-tiles: (k 0-7, n 0-7), (k 8-15, n 0-7), (k 0-7, n 8-15), (k 8-15, n 8-15).
-__device__ __forceinline__ int bt_row(int lane) { return (lane & 7) + 8 * ((lane >> 3) & 1); }
-__device__ __forceinline__ int bt_ch(int lane) { return lane >> 4; }
-//  A from [k][m] storage (transposed load): (k 0-7, m 0-7), (k 0-7, m 8-15), (k 8-15, m 0-7), (k 8-15, m 8-15).
-__device__ __forceinline__ int at_row(int lane) { return (lane & 7) + 8 * (lane >> 4); }
-__device__ __forceinline__ int at_ch(int lane) { return (lane >> 3) & 1; }
-
-// ------------------------------------------------ lower-triangular inverse
-// T = (I + A)^{-1} of the chunk's 64 x 64 strictly lower A by 16 x 16 blocks:
-// the four diagonal blocks by forward substitution, then with the left factors
-// F_IK = T_II A_IK each off-diagonal block T_IJ = -sum_{K=J}^{I-1} F_IK T_KJ.
-// Matrices are block-packed: block (I, J), J <= I, at index I (I + 1) / 2 + J,
-// rows of kBS floats; A is column-major within a block, T row-major.
-constexpr int kBS = 24;
-constexpr int kBlk = 16 * kBS;
-constexpr int kBlkFloats = 10 * kBlk;
-__device__ __forceinline__ int blk(int I, int J) { return I * (I + 1) / 2 + J; }
-
-// Column `col` of the diagonal block b of T: t[r] = delta(r, col) - sum_{m<r} A[r][m] t[m].
-__device__ __forceinline__ void diag_solve(int b, int col, const float *At, float *Tm) {
-    const float *Ab = At + blk(b, b) * kBlk;
-    float t[16];
-#pragma unroll
-    for (int r = 0; r < 16; ++r) t[r] = (r == col) ? 1.f : 0.f;
-#pragma unroll
-    for (int m = 0; m < 15; ++m) {
-        const float tm = t[m];
-#pragma unroll
-        for (int r = m + 1; r < 16; ++r) t[r] = fmaf(-Ab[m * kBS + r], tm, t[r]);
-    }
-    float *Tb = Tm + blk(b, b) * kBlk + col;
-#pragma unroll
-    for (int r = 0; r < 16; ++r) Tb[r * kBS] = t[r];
-}
-
-// The six left factors as twelve 8-column tiles, three per warp (warps 0-3),
-// written in place of A_IK (a warp reads and writes only its own columns).
-struct FactorJob {
-    uint8_t I, K, nt;
-};
-__constant__ FactorJob kFactorJobs[4][3] = {
-    {{1, 0, 0}, {1, 0, 1}, {2, 0, 0}},
-    {{2, 1, 0}, {2, 1, 1}, {2, 0, 1}},
-    {{3, 2, 0}, {3, 2, 1}, {3, 1, 0}},
-    {{3, 0, 0}, {3, 0, 1}, {3, 1, 1}},
-};
-
-__device__ __forceinline__ void solve_factors(int w, float *At, const float *Tm, int lane) {
-    const int gq = lane >> 2, t4 = lane & 3;
-    float acc[3][2][4];
-    float *fb[3];
-    int col[3];
-#pragma unroll
-    for (int u = 0; u < 3; ++u) {
-        const FactorJob jb = kFactorJobs[w][u];
-        const float *Td = Tm + blk(jb.I, jb.I) * kBlk;
-        fb[u] = At + blk(jb.I, jb.K) * kBlk;
-        col[u] = 8 * jb.nt + gq;
-#pragma unroll
-        for (int ks = 0; ks < 2; ++ks) {
-            const int k0 = 8 * ks;
-#pragma unroll
-            for (int e = 0; e < 4; ++e) acc[u][ks][e] = 0.f;
-            mma_tf32(acc[u][ks], __float_as_uint(Td[gq * kBS + k0 + t4]), __float_as_uint(Td[(gq + 8) * kBS + k0 + t4]),
-                     __float_as_uint(Td[gq * kBS + k0 + t4 + 4]), __float_as_uint(Td[(gq + 8) * kBS + k0 + t4 + 4]),
-                     __float_as_uint(fb[u][col[u] * kBS + k0 + t4]), __float_as_uint(fb[u][col[u] * kBS + k0 + t4 + 4]));
-        }
-    }
-    __syncwarp();
-#pragma unroll
-    for (int u = 0; u < 3; ++u) {
-        float *f = fb[u] + (col[u] - gq + 2 * t4) * kBS + gq;
-        f[0] = acc[u][0][0] + acc[u][1][0];
-        f[kBS] = acc[u][0][1] + acc[u][1][1];
-        f[8] = acc[u][0][2] + acc[u][1][2];
-        f[kBS + 8] = acc[u][0][3] + acc[u][1][3];
-    }
-}
-
-// Off-diagonal blocks of block column J (NNT = 2: both 8-column tiles, NNT = 1:
-// tile nt0): T_IJ = -sum_{K=J}^{I-1} F_IK T_KJ for I = J+1..3 in order.
-template <int NNT>
-__device__ __forceinline__ void solve_column(int J, int nt0, const float *At, float *Tm, int lane) {
-    const int gq = lane >> 2, t4 = lane & 3;
-#pragma unroll 1
-    for (int I = J + 1; I < 4; ++I) {
-        float c[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-        float e[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-#pragma unroll 1
-        for (int K = J; K < I; ++K) {
-            const float *Fb = At + blk(I, K) * kBlk;   // F[r][k] at k*kBS + r
-            const float *Bb = Tm + blk(K, J) * kBlk;   // T[k][n] at k*kBS + n
-#pragma unroll
-            for (int ks = 0; ks < 2; ++ks) {
-                const int k0 = 8 * ks;
-                const uint32_t a0 = __float_as_uint(Fb[(k0 + t4) * kBS + gq]);
-                const uint32_t a1 = __float_as_uint(Fb[(k0 + t4) * kBS + gq + 8]);
-                const uint32_t a2 = __float_as_uint(Fb[(k0 + t4 + 4) * kBS + gq]);
-                const uint32_t a3 = __float_as_uint(Fb[(k0 + t4 + 4) * kBS + gq + 8]);
-#pragma unroll
-                for (int nt = 0; nt < NNT; ++nt) {
-                    const uint32_t b0 = __float_as_uint(Bb[(k0 + t4) * kBS + 8 * (nt0 + nt) + gq]);
-                    const uint32_t b1 = __float_as_uint(Bb[(k0 + t4 + 4) * kBS + 8 * (nt0 + nt) + gq]);
-                    mma_tf32(ks ? e[nt] : c[nt], a0, a1, a2, a3, b0, b1);
-                }
-            }
-        }
-        float *Tb = Tm + blk(I, J) * kBlk;
-#pragma unroll
-        for (int nt = 0; nt < NNT; ++nt) {
-            const int cn = 8 * (nt0 + nt) + 2 * t4;
-#pragma unroll
-            for (int hr = 0; hr < 2; ++hr) {
-                const int r = gq + 8 * hr;
-                *reinterpret_cast<float2 *>(Tb + r * kBS + cn) =
-                    make_float2(-(c[nt][2 * hr] + e[nt][2 * hr]), -(c[nt][2 * hr + 1] + e[nt][2 * hr + 1]));
-            }
-        }
-        __syncwarp();
-    }
-}
 
 // ------------------------------------------------------------- parameters
 
@@ -254,6 +78,8 @@ struct CwDev {
     float *S_T;
     uint8_t *rec;     // [B * Hv][nchunks][kRecBytes]
     float *bound;     // [B * Hv][nchunks]
+    int scalar_alpha; // alpha is [B, T, Hv], the same decay for every channel
+    float *state_out; // nullptr, or the state entering every chunk [B * Hv][nchunks][d][d] fp32
 };
 
 // Pre-pass shared memory (bytes).  After the A and P products the q/k tiles
@@ -309,10 +135,12 @@ __global__ void __launch_bounds__(256, 2) cw_prepass_kernel(const CwDev p) {
     for (int e = tid; e < kC * 32; e += 256) {
         const int r = e >> 5, pc = e & 31;
         float *dst = G + r * kD + pc * 4;
-        if (r < nvalid)
+        if (r < nvalid && !p.scalar_alpha) {
             cp_async16(smem_u32(dst), p.alpha + ((static_cast<int64_t>(b) * p.T + t0 + r) * p.Hv + hv) * kD + pc * 4);
-        else
-            *reinterpret_cast<float4 *>(dst) = make_float4(1.f, 1.f, 1.f, 1.f);
+        } else {
+            const float a = r < nvalid ? __ldg(p.alpha + (static_cast<int64_t>(b) * p.T + t0 + r) * p.Hv + hv) : 1.f;
+            *reinterpret_cast<float4 *>(dst) = make_float4(a, a, a, a);
+        }
     }
     for (int e = tid; e < kC * 16; e += 256) {
         const int r = e >> 4, pc = e & 15;
@@ -332,29 +160,42 @@ __global__ void __launch_bounds__(256, 2) cw_prepass_kernel(const CwDev p) {
     cp_async_wait_all();
     __syncthreads();
 
-    // ---- G = cumulative log alpha per channel; block references R_I = G before
-    // block I; e^{g_C} into the record; blocks whose own decay passes e^kMaxExp
-    if (tid < kD) {
-        const int ch = tid;
+    // ---- G = cumulative log2 alpha per channel (two halves of 32 tokens, then
+    // the second half offset by the first); block references R_I = G before
+    // block I; e^{g_C} into the record; blocks whose own decay passes 2^kMaxExp2
+    {
+        const int ch = tid & (kD - 1), h = tid >> 7;
         float run = 0.f;
-#pragma unroll 4
-        for (int t = 0; t < kC; ++t) {
-            if ((t & 15) == 0) R[(t >> 4) * kD + ch] = run;
-            run += logf(G[t * kD + ch]);
+#pragma unroll 8
+        for (int t = 32 * h; t < 32 * h + 32; ++t) {
+            run += logf(G[t * kD + ch]) * kLog2e;
             G[t * kD + ch] = run;
         }
-        gC[ch] = run;
-        reinterpret_cast<float *>(rec + REC_GC)[ch] = __expf(run);
+    }
+    __syncthreads();
+    {
+        const int ch = tid & (kD - 1), h = tid >> 7;
+        const float off = G[31 * kD + ch];
+#pragma unroll 8
+        for (int t = 32 + 16 * h; t < 48 + 16 * h; ++t) G[t * kD + ch] += off;
+    }
+    __syncthreads();
+    if (tid < kD) {
+        const int ch = tid;
+        const float gc = G[63 * kD + ch];
+        gC[ch] = gc;
+        reinterpret_cast<float *>(rec + REC_GC)[ch] = exp2_ftz(gc);
 #pragma unroll
         for (int I = 0; I < 4; ++I) {
-            const float r = R[I * kD + ch];
-            eR[I * kD + ch] = __expf(r);
-            if (r - G[(16 * I + 15) * kD + ch] > kMaxExp) viol[I] = 1;
+            const float r = I == 0 ? 0.f : G[(16 * I - 1) * kD + ch];
+            R[I * kD + ch] = r;
+            eR[I * kD + ch] = exp2_ftz(r);
+            if (r - G[(16 * I + 15) * kD + ch] > kMaxExp2) viol[I] = 1;
         }
     }
     __syncthreads();
 
-    // ---- decay bound of the chunk: sum over tokens of max_c log alpha
+    // ---- decay bound of the chunk: sum over tokens of max_c log alpha (natural log)
     {
         float part = 0.f;
 #pragma unroll 1
@@ -381,7 +222,7 @@ __global__ void __launch_bounds__(256, 2) cw_prepass_kernel(const CwDev p) {
         if (s <= t) {
 #pragma unroll 4
             for (int ch = 0; ch < kD; ++ch) {
-                const float e = __expf(G[t * kD + ch] - G[s * kD + ch]);
+                const float e = exp2_ftz(G[t * kD + ch] - G[s * kD + ch]);
                 const float ks = tile_elem(sm + PP_KT, s, ch) * e;
                 a = fmaf(tile_elem(sm + PP_KT, t, ch), ks, a);
                 pp = fmaf(tile_elem(sm + PP_QT, t, ch), ks, pp);
@@ -394,7 +235,7 @@ __global__ void __launch_bounds__(256, 2) cw_prepass_kernel(const CwDev p) {
     if (tid == 0) {
         float s = 0.f;
         for (int w = 0; w < 8; ++w) s += wred[w];
-        p.bound[pr * p.nchunks + c] = s;
+        p.bound[pr * p.nchunks + c] = s * kLn2;
     }
 
     // ---- per-token operands: Qp, Kl to the record; Qloc (in place of q), Kloc
@@ -404,9 +245,13 @@ __global__ void __launch_bounds__(256, 2) cw_prepass_kernel(const CwDev p) {
         const uint4 qr = *reinterpret_cast<const uint4 *>(sm + PP_QT + off);
         const uint4 kr = *reinterpret_cast<const uint4 *>(sm + PP_KT + off);
         const uint32_t qw[4] = {qr.x, qr.y, qr.z, qr.w}, kw[4] = {kr.x, kr.y, kr.z, kr.w};
-        const float *gr = G + t * kD + pc * 8;
-        const float *rr = R + I * kD + pc * 8;
-        const float *gc = gC + pc * 8;
+        float gr[8], rr[8], gc[8];
+        *reinterpret_cast<float4 *>(gr) = *reinterpret_cast<const float4 *>(G + t * kD + pc * 8);
+        *reinterpret_cast<float4 *>(gr + 4) = *reinterpret_cast<const float4 *>(G + t * kD + pc * 8 + 4);
+        *reinterpret_cast<float4 *>(rr) = *reinterpret_cast<const float4 *>(R + I * kD + pc * 8);
+        *reinterpret_cast<float4 *>(rr + 4) = *reinterpret_cast<const float4 *>(R + I * kD + pc * 8 + 4);
+        *reinterpret_cast<float4 *>(gc) = *reinterpret_cast<const float4 *>(gC + pc * 8);
+        *reinterpret_cast<float4 *>(gc + 4) = *reinterpret_cast<const float4 *>(gC + pc * 8 + 4);
         uint32_t oqp[4], okl[4], oql[4], okq[4];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
@@ -415,9 +260,9 @@ __global__ void __launch_bounds__(256, 2) cw_prepass_kernel(const CwDev p) {
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 const float gv = gr[2 * j + h];
-                e1[h] = __expf(gv);
-                el[h] = __expf(gc[2 * j + h] - gv);
-                eo[h] = __expf(gv - rr[2 * j + h]);
+                e1[h] = exp2_ftz(gv);
+                el[h] = exp2_ftz(gc[2 * j + h] - gv);
+                eo[h] = exp2_ftz(gv - rr[2 * j + h]);
             }
             oqp[j] = pack2(qf.x * e1[0], qf.y * e1[1]);
             okl[j] = pack2(kf.x * el[0], kf.y * el[1]);
@@ -447,13 +292,16 @@ __global__ void __launch_bounds__(256, 2) cw_prepass_kernel(const CwDev p) {
             if (!(vI && s >= 16 * I)) {
                 const uint4 kr = *reinterpret_cast<const uint4 *>(sm + PP_KT + sw256(s, pc));
                 const uint32_t kw[4] = {kr.x, kr.y, kr.z, kr.w};
-                const float *gr = G + s * kD + pc * 8;
-                const float *rr = R + I * kD + pc * 8;
+                float gr[8], rr[8];
+                *reinterpret_cast<float4 *>(gr) = *reinterpret_cast<const float4 *>(G + s * kD + pc * 8);
+                *reinterpret_cast<float4 *>(gr + 4) = *reinterpret_cast<const float4 *>(G + s * kD + pc * 8 + 4);
+                *reinterpret_cast<float4 *>(rr) = *reinterpret_cast<const float4 *>(R + I * kD + pc * 8);
+                *reinterpret_cast<float4 *>(rr + 4) = *reinterpret_cast<const float4 *>(R + I * kD + pc * 8 + 4);
                 uint32_t o[4];
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
                     const float2 kf = unpack2(kw[j]);
-                    o[j] = pack2(kf.x * __expf(rr[2 * j] - gr[2 * j]), kf.y * __expf(rr[2 * j + 1] - gr[2 * j + 1]));
+                    o[j] = pack2(kf.x * exp2_ftz(rr[2 * j] - gr[2 * j]), kf.y * exp2_ftz(rr[2 * j + 1] - gr[2 * j + 1]));
                 }
                 out = make_uint4(o[0], o[1], o[2], o[3]);
             }
@@ -708,6 +556,15 @@ __global__ void __launch_bounds__(256, 1) cw_chain_kernel(const CwDev p) {
         const int st = (cc - c_w) & 1;
         const uint32_t stg = sb + st * kRecBytes;
         const uint8_t *stp = sm + st * kRecBytes;
+        if (p.state_out && cc >= c_begin) {
+            float *so = p.state_out + (static_cast<int64_t>(pr) * p.nchunks + cc) * kD * kD;
+#pragma unroll
+            for (int nt = 0; nt < 16; ++nt) {
+                const int r = 16 * warp + g, col = 8 * nt + 2 * t4;
+                *reinterpret_cast<float2 *>(so + r * kD + col) = make_float2(S[nt][0], S[nt][1]);
+                *reinterpret_cast<float2 *>(so + (r + 8) * kD + col) = make_float2(S[nt][2], S[nt][3]);
+            }
+        }
         // A: bf16 copy of the state
 #pragma unroll
         for (int nt = 0; nt < 16; ++nt) {
@@ -769,7 +626,7 @@ __global__ void __launch_bounds__(256, 1) cw_chain_kernel(const CwDev p) {
                 mma16816(ys[2 * np + 1], ap, bu[2], bu[3]);
             }
         }
-        if (cc >= c_begin) {
+        if (cc >= c_begin && p.y) {
 #pragma unroll
             for (int hr = 0; hr < 2; ++hr) {
                 const int64_t t = static_cast<int64_t>(cc) * kC + 16 * mt + g + 8 * hr;
@@ -870,6 +727,8 @@ cudaError_t launch_chunked_cw(const ChunkedCwParams &p, cudaStream_t stream, int
     dv.S_T = p.S_T;
     dv.rec = p.ops;
     dv.bound = reinterpret_cast<float *>(p.ops + static_cast<size_t>(pairs) * nchunks * kRecBytes);
+    dv.scalar_alpha = p.scalar_alpha ? 1 : 0;
+    dv.state_out = p.state_out;
     cw_prepass_kernel<<<static_cast<unsigned>(p.B * nchunks * p.Hv), 256, kPrepassSmem, stream>>>(dv);
     cw_chain_kernel<<<static_cast<unsigned>(pairs * P), 256, kChainSmem, stream>>>(dv);
     return cudaGetLastError();

@@ -84,7 +84,15 @@ struct ChunkedCwParams {
     float log_eps;
     int max_warmup_chunks;
     uint8_t *ops;                // chunked_cw_ops_bytes(B, T, Hv) bytes, 16-byte aligned
+    bool scalar_alpha;           // alpha is [B, T, Hv] (one decay for every channel)
+    float *state_out;            // nullptr, or the state entering every chunk [B * Hv][nchunks][d][d]
 };
+
+// The per-chunk operand record the chunked pre-pass writes (bytes): -W, U~,
+// Qp and Kl as bf16 [64][128], P as bf16 [64][64], e^{g_C} as fp32 [128].
+namespace rec {
+constexpr uint32_t kWn = 0, kUt = 16384, kQp = 32768, kKl = 49152, kP = 65536, kGc = 73728, kBytes = 74240;
+}
 
 // Bytes of one chunk's operand record in the workspace.
 constexpr size_t kCwChunkBytes = 74240;
@@ -113,6 +121,12 @@ struct BackwardParams {
 // its partial-sum regions (the checkpoints start at offset 0).
 size_t backward_workspace_layout(int64_t B, int64_t T, int Hv, int d, size_t *off_part_dq, size_t *off_part_dk,
                                  size_t *off_part_b, size_t *off_part_g);
+
+// Chunked tensor-core backward (bf16, d = 128): workspace bytes and launch
+// (pre-pass, forward chain with the entering states, reverse chain, per-chunk
+// gradients).  ws: 256-byte aligned, backward_chunked_workspace_bytes bytes.
+size_t backward_chunked_workspace_bytes(int64_t B, int64_t T, int Hv);
+cudaError_t launch_backward_chunked(const BackwardParams &p, uint8_t *ws, cudaStream_t stream, int num_sms);
 
 // Backward of the recurrence: the per-slab kernel, then the reduction of its partial sums.
 cudaError_t launch_backward(const BackwardParams &p, int d, gdn_dtype dtype, cudaStream_t stream, int num_sms);

@@ -30,7 +30,8 @@ EXPORTS = ("gdn_status_string", "gdn_prefill_workspace_bytes", "gdn_prefill", "g
            "gdn_prefill_noalloc", "gdn_layer_prologue", "gdn_layer_epilogue", "gdn_prefill_host_workspace_bytes",
            "gdn_prefill_host", "gdn_prefill_cw", "gdn_decode_step_cw", "gdn_backward_workspace_bytes",
            "gdn_backward", "gdn_prefill_noalloc_status", "gdn_prefill_launches",
-           "gdn_prefill_cw_workspace_bytes", "gdn_prefill_cw_ex")
+           "gdn_prefill_cw_workspace_bytes", "gdn_prefill_cw_ex", "gdn_backward_chunked_workspace_bytes",
+           "gdn_backward_chunked")
 NOALLOC_SCRATCH_BYTES = 256 + 8 * 1024 * 1024
 
 
@@ -116,6 +117,10 @@ def lib() -> ctypes.CDLL:
             L.gdn_backward_workspace_bytes.argtypes = [sp]
             L.gdn_backward.restype = ctypes.c_int
             L.gdn_backward.argtypes = [sp, vp, vp, vp, fp, fp, fp, vp, fp, fp, fp, fp, fp, fp, fp, vp, c_size, vp]
+            L.gdn_backward_chunked_workspace_bytes.restype = c_size
+            L.gdn_backward_chunked_workspace_bytes.argtypes = [sp]
+            L.gdn_backward_chunked.restype = ctypes.c_int
+            L.gdn_backward_chunked.argtypes = L.gdn_backward.argtypes
             L.gdn_device_supported.restype = ctypes.c_int
             L.gdn_abi_version.restype = ctypes.c_int
             _lib = L
@@ -373,22 +378,26 @@ def decode_step_cw(q, k, v, alpha, beta, S, *, y=None, stream=None):
     return y
 
 
-def backward_workspace_bytes(shape: GdnShape) -> int:
-    return int(lib().gdn_backward_workspace_bytes(ctypes.byref(shape)))
+def backward_workspace_bytes(shape: GdnShape, chunked: bool = False) -> int:
+    fn = lib().gdn_backward_chunked_workspace_bytes if chunked else lib().gdn_backward_workspace_bytes
+    return int(fn(ctypes.byref(shape)))
 
 
-def new_backward_workspace(shape: GdnShape, device) -> torch.Tensor:
-    """A workspace of the size gdn_backward needs (uint8; its contents need no initialisation)."""
-    return torch.empty(max(backward_workspace_bytes(shape), 256), dtype=torch.uint8, device=device)
+def new_backward_workspace(shape: GdnShape, device, chunked: bool = False) -> torch.Tensor:
+    """A workspace of the size gdn_backward (or gdn_backward_chunked) needs (uint8; no initialisation needed)."""
+    return torch.empty(max(backward_workspace_bytes(shape, chunked), 256), dtype=torch.uint8, device=device)
 
 
-def backward(q, k, v, alpha, beta, S0, dy, dS_T=None, *, dS0=True, out=None, workspace=None, stream=None):
-    """Run gdn_backward; returns a dict with dq, dk [B,T,Hqk,d], dv [B,T,Hv,d], dlog_alpha, dbeta [B,T,Hv]
-    (fp32) and dS0 [B,Hv,d,d] (fp32; None when dS0=False).
+def backward(q, k, v, alpha, beta, S0, dy, dS_T=None, *, dS0=True, out=None, workspace=None, stream=None,
+             algorithm=ALGO_SEQUENTIAL):
+    """Run gdn_backward (algorithm ALGO_SEQUENTIAL: fp32, token by token) or gdn_backward_chunked
+    (ALGO_CHUNKED: tensor cores, bf16 with d = 128); returns a dict with dq, dk [B,T,Hqk,d],
+    dv [B,T,Hv,d], dlog_alpha, dbeta [B,T,Hv] (fp32) and dS0 [B,Hv,d,d] (fp32; None when dS0=False).
 
     dlog_alpha is alpha * dL/dalpha.  dy has the dtype of q, k, v; dS_T (fp32) may be None (zero).
     out: optional dict of preallocated outputs with the same keys.
     """
+    chunked = algorithm == ALGO_CHUNKED
     _require(dict(q=q, k=k, v=v, alpha=alpha, beta=beta, S0=S0, dy=dy, dS_T=dS_T, workspace=workspace))
     if dy.dtype != q.dtype:
         raise TypeError(f"dy is {dy.dtype}, expected {q.dtype}")
@@ -409,12 +418,13 @@ def backward(q, k, v, alpha, beta, S0, dy, dS_T=None, *, dS0=True, out=None, wor
     _require(o)
     own_ws = workspace is None
     if own_ws:
-        workspace = new_backward_workspace(shape, dev)
-    rc = lib().gdn_backward(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(beta), _ptr(S0),
-                            _ptr(dy), _ptr(dS_T), _ptr(o["dq"]), _ptr(o["dk"]), _ptr(o["dv"]), _ptr(o["dlog_alpha"]),
-                            _ptr(o["dbeta"]), _ptr(o["dS0"]), _ptr(workspace),
-                            workspace.numel() * workspace.element_size(), _stream(stream))
-    _check(rc, "gdn_backward")
+        workspace = new_backward_workspace(shape, dev, chunked=chunked)
+    fn = lib().gdn_backward_chunked if chunked else lib().gdn_backward
+    rc = fn(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(beta), _ptr(S0),
+            _ptr(dy), _ptr(dS_T), _ptr(o["dq"]), _ptr(o["dk"]), _ptr(o["dv"]), _ptr(o["dlog_alpha"]),
+            _ptr(o["dbeta"]), _ptr(o["dS0"]), _ptr(workspace),
+            workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(rc, "gdn_backward_chunked" if chunked else "gdn_backward")
     if own_ws and stream is not None:
         workspace.record_stream(stream)
     return o

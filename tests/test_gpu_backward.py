@@ -105,3 +105,64 @@ def test_backward_training_shape_sampled_heads():
         got = {n: sl(out[n]) for n in ("dq", "dk", "dv", "dlog_alpha", "dbeta")}
         got["dS0"] = out["dS0"][b:b + 1, heads]
         _check(got, ref)
+
+
+# ----------------------------------------------------------------------------
+# The chunked backward on the tensor cores (bf16, d = 128): bf16 operands with
+# fp32 accumulation, so the bf16 tolerance of the forward (2e-2) applies.
+CHUNKED_TOL = 2e-2
+
+
+def _check_chunked(out, ref, names=("dq", "dk", "dv", "dlog_alpha", "dbeta", "dS0")):
+    for n in names:
+        assert rel_err(out[n], ref[n]) <= CHUNKED_TOL, (n, rel_err(out[n], ref[n]))
+
+
+@pytest.mark.parametrize("B,T,Hqk,Hv,s0,ds,decay", [
+    (1, 64, 1, 1, 0.02, 1.0, 0.1),       # one whole chunk
+    (1, 37, 1, 2, 0.05, 1.0, 0.1),       # grouped heads, shorter than a chunk
+    (2, 200, 2, 4, 0.0, 1.0, 0.1),       # several chunks, ragged tail, no initial state
+    (1, 150, 1, 1, 0.02, 0.0, 0.5),      # strong decay, no state gradient
+    (1, 1, 1, 2, 0.05, 1.0, 0.1),        # a single token
+])
+def test_backward_chunked_matches_oracle(B, T, Hqk, Hv, s0, ds, decay):
+    x = make_prefill_inputs(B, T, Hqk, Hv, 128, "bf16", decay_scale=decay, s0_std=s0, seed=T + 91, device="cuda")
+    g = make_backward_grads(B, T, Hv, 128, "bf16", ds_std=ds, seed=T + 91, device="cuda")
+    out = gdn.backward(x.q, x.k, x.v, x.alpha, x.beta, x.S0, g.dy, g.dS_T, algorithm=gdn.ALGO_CHUNKED)
+    torch.cuda.synchronize()
+    _check_chunked(out, _reference(x, g))
+
+
+def test_backward_chunked_segments_and_in_place_state_gradient():
+    # 2000 tokens over 2 heads: the state chains split into segments with warm-up windows.
+    x = make_prefill_inputs(1, 2000, 1, 2, 128, "bf16", decay_scale=0.1, s0_std=0.02, seed=93, device="cuda")
+    g = make_backward_grads(1, 2000, 2, 128, "bf16", ds_std=1.0, seed=93, device="cuda")
+    ref = _reference(x, g)
+    dST = g.dS_T.clone()
+    out = gdn.backward(x.q, x.k, x.v, x.alpha, x.beta, x.S0, g.dy, dST, out={"dS0": dST},
+                       algorithm=gdn.ALGO_CHUNKED)
+    torch.cuda.synchronize()
+    _check_chunked(out, ref)
+    # agrees with the fp32 token-sequential backward
+    seq = gdn.backward(x.q, x.k, x.v, x.alpha, x.beta, x.S0, g.dy, g.dS_T)
+    torch.cuda.synchronize()
+    for n in ("dq", "dk", "dv", "dlog_alpha", "dbeta"):
+        assert rel_err(out[n], seq[n].double().cpu().numpy()) <= CHUNKED_TOL, n
+
+
+def test_backward_chunked_training_shape_sampled_heads():
+    # B=2, H=16, T=4096, d=128, bf16: eight (batch, head) pairs including the last head.
+    x = workload_inputs("train", seed=0, device="cuda")
+    g = make_backward_grads(2, 4096, 16, 128, "bf16", ds_std=1.0, seed=0, device="cuda")
+    out = gdn.backward(x.q, x.k, x.v, x.alpha, x.beta, x.S0, g.dy, g.dS_T, algorithm=gdn.ALGO_CHUNKED)
+    torch.cuda.synchronize()
+    for n in ("dq", "dk", "dv", "dlog_alpha", "dbeta", "dS0"):
+        assert torch.isfinite(out[n]).all(), n
+    for b, heads in ((0, [0, 5, 10, 15]), (1, [2, 7, 12, 15])):
+        sl = lambda t: t[b:b + 1, :, heads].contiguous()  # noqa: E731
+        ref = obw.recurrence_grad(sl(x.q), sl(x.k), sl(x.v), sl(x.alpha), sl(x.beta), None, sl(g.dy),
+                                  g.dS_T[b:b + 1, heads])
+        ref["dlog_alpha"] = sl(x.alpha).double().cpu().numpy() * ref["dalpha"]
+        got = {n: sl(out[n]) for n in ("dq", "dk", "dv", "dlog_alpha", "dbeta")}
+        got["dS0"] = out["dS0"][b:b + 1, heads]
+        _check_chunked(got, ref)
