@@ -11,7 +11,8 @@ and reports it under "decode", and the layer steps around the recurrence
 (fused prologue: short convolution, SiLU, L2Norm, gates; fused epilogue:
 sigmoid gate times zero-centred RMSNorm) on the prefill shape under "layer",
 and the backward pass (gradients of the recurrence) on the training-shape
-workload (B=2, H=16, T=4096, d=128, bf16) under "backward".  The other
+workload (B=2, H=16, T=4096, d=128, bf16) under "backward": the chunked
+tensor-core path, with the fp32 token-sequential path beside it.  The other
 prefill workloads are timed beside it: the training shape ("prefill_train"),
 the long-context prefill (B=1, H=16, T=2^20, "prefill_long") and the grouped
 shape with gates that barely decay ("prefill_weak_decay") and the grouped
@@ -606,7 +607,8 @@ def summarize(line: dict) -> dict:
     out["prologue_hbm"] = g(line, "layer", "prologue", "roofline", "frac")
     out["epilogue_hbm"] = g(line, "layer", "epilogue", "roofline", "frac")
     out["backward_ms"] = g(line, "backward", "ms")
-    out["backward_alu"] = g(line, "backward", "roofline", "frac")
+    out["backward_tc"] = g(line, "backward", "roofline", "frac")
+    out["backward_fp32_ms"] = g(line, "backward", "sequential_fp32", "ms")
     return {k: v for k, v in out.items() if v is not None}
 
 
@@ -736,9 +738,32 @@ def fp32_alu_peak_tflops(sm_mhz: float, sms: int = 148) -> float:
     return sms * 128 * 2 * sm_mhz * 1e6 / 1e12
 
 
+def backward_chunked_flops_per_chunk(d: int = 128, chunk: int = 64) -> float:
+    """Tensor-core FLOPs of the chunked backward per (chunk, value head), products as executed
+    (block-triangular operands skip their zero blocks): the pre-pass, the forward chain (no y),
+    the reverse chain and the per-chunk gradient kernel."""
+    C, blocks = chunk, chunk // 16
+    tri = sum(range(1, blocks + 1)) / blocks ** 2        # fraction of 16 x 16 blocks on or below the diagonal
+    full_cd = C * d * d            # a 64 x d x d product
+    cc_d = C * C * d               # a 64 x 64 x d product
+    prepass = 2 * cc_d * tri + 2 * C * C * d * tri       # A and P by row block; W and U~ from block-lower T
+    fwd_chain = 2 * full_cd                              # U = U~ - W S, S' = gamma S + Kl^T U
+    rev_chain = cc_d * tri + 3 * full_cd                 # P^T dY, Kl dS', Qp^T dY, W^T dU
+    grad = (2 * cc_d                                     # K K^T, Q K^T
+            + 2 * cc_d * tri + full_cd                   # W, U~; W S
+            + full_cd + cc_d * tri                       # K dS'; P^T dY
+            + 3 * full_cd + cc_d                         # U dS'^T, dY S^T, Q S; dY U^T
+            + 2 * cc_d * tri + full_cd                   # dQK K, dQK^T Q; dU S^T
+            + 2 * cc_d * tri + 2 * cc_d                  # T^T dU, T^T dW; dW K^T, dU V^T
+            + C * C * C * tri + C * C * C                # T^T dT; X T^T
+            + 2 * cc_d * tri)                            # (dKK + dKK^T) K
+    return 2.0 * (prepass + fwd_chain + rev_chain + grad)
+
+
 def time_backward(args, peaks, seed, dev, ws, local):
-    """gdn_backward on the training-shape workload (B=2, H=16, T=4096, d=128, bf16 inputs, dy ~ N(0,1),
-    dS_T ~ N(0,1)); median of 10 calls, each the per-slab kernel plus its reduction."""
+    """gdn_backward_chunked (tensor cores) and gdn_backward (fp32, token by token) on the
+    training-shape workload (B=2, H=16, T=4096, d=128, bf16 inputs, dy ~ N(0,1), dS_T ~ N(0,1));
+    median of 10 calls each."""
     import torch
 
     from linear_attention_recurrence_14_b300 import gdn
@@ -749,44 +774,66 @@ def time_backward(args, peaks, seed, dev, ws, local):
     Hv = x.v.shape[2]
     g = make_backward_grads(B, T, Hv, d, "bf16", ds_std=1.0, seed=seed, device=dev)
     shape = gdn.shape_of(x.q, x.v)
-    wsb = gdn.new_backward_workspace(shape, dev)
-    out = gdn.backward(x.q, x.k, x.v, x.alpha, x.beta, x.S0, g.dy, g.dS_T, workspace=wsb)
     stream = torch.cuda.current_stream()
-
-    def fn():
-        gdn.backward(x.q, x.k, x.v, x.alpha, x.beta, x.S0, g.dy, g.dS_T, out=out, workspace=wsb)
-
-    for _ in range(max(3, args.warmup)):
-        fn()
-    torch.cuda.synchronize()
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(10)]
-    barrier(ws)
-    with ClockSampler(local) as clk:
-        for a, b in evs:
-            a.record(stream)
-            fn()
-            b.record(stream)
-        torch.cuda.synchronize()
-    ms = max_over_ranks(statistics.median(a.elapsed_time(b) for a, b in evs), ws, dev)
-    clocks = clk.summary()
-    flops = backward_flops_per_token_head(d) * B * T * Hv
-    tflops = flops / (ms * 1e-3) / 1e12
-    mhz = clocks.get("sm_max_mhz") or 2032
-    peak = fp32_alu_peak_tflops(mhz)
     # algorithmic HBM bytes: inputs (q, k, v, dy bf16; alpha, beta fp32), outputs (dq, dk, dv fp32,
     # dlog_alpha, dbeta fp32), dS_T in and dS0 out
     nbytes = (2 * B * T * Hqk * d * 2 + 2 * B * T * Hv * d * 2 + 2 * B * T * Hv * 4
               + 2 * B * T * Hqk * d * 4 + B * T * Hv * d * 4 + 2 * B * T * Hv * 4 + 2 * B * Hv * d * d * 4)
+
+    def timed(algorithm):
+        chunked = algorithm == gdn.ALGO_CHUNKED
+        wsb = gdn.new_backward_workspace(shape, dev, chunked=chunked)
+        out = gdn.backward(x.q, x.k, x.v, x.alpha, x.beta, x.S0, g.dy, g.dS_T, workspace=wsb, algorithm=algorithm)
+
+        def fn():
+            gdn.backward(x.q, x.k, x.v, x.alpha, x.beta, x.S0, g.dy, g.dS_T, out=out, workspace=wsb,
+                         algorithm=algorithm)
+
+        for _ in range(max(3, args.warmup)):
+            fn()
+        torch.cuda.synchronize()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(10)]
+        barrier(ws)
+        with ClockSampler(local) as clk:
+            for a, b in evs:
+                a.record(stream)
+                fn()
+                b.record(stream)
+            torch.cuda.synchronize()
+        ms = max_over_ranks(statistics.median(a.elapsed_time(b) for a, b in evs), ws, dev)
+        del wsb, out
+        torch.cuda.empty_cache()
+        return ms, clk.summary()
+
+    hbm = lambda ms: {"bytes_per_call": nbytes, "achieved_gbs": nbytes / (ms * 1e-3) / 1e9,  # noqa: E731
+                      "frac": nbytes / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"]}
+    # chunked, tensor cores: against the bf16 tensor peak
+    ms, clocks = timed(gdn.ALGO_CHUNKED)
+    nchunks = (T + 63) // 64
+    flops = backward_chunked_flops_per_chunk(d) * B * nchunks * Hv
+    tf = flops / (ms * 1e-3) / 1e12
+    # fp32 token-sequential: against the fp32 FMA peak
+    ms_s, clocks_s = timed(gdn.ALGO_SEQUENTIAL)
+    flops_s = backward_flops_per_token_head(d) * B * T * Hv
+    tf_s = flops_s / (ms_s * 1e-3) / 1e12
+    peak_s = fp32_alu_peak_tflops(clocks_s.get("sm_max_mhz") or 2032)
     return {"ms": ms, "tokens_per_s": B * T * ws / (ms * 1e-3),
-            "roofline": {"bound": "alu", "achieved": tflops, "peak": peak, "unit": "TFLOP/s", "frac": tflops / peak,
-                         "traffic": None, "flops_per_call": flops,
-                         "peak_source": "fp32 FMA: 148 SMs x 128 lanes x 2 FLOPs at the sampled max SM clock",
-                         "hbm": {"bytes_per_call": nbytes, "achieved_gbs": nbytes / (ms * 1e-3) / 1e9,
-                                 "frac": nbytes / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"]}},
-            "gpu_launches": gdn.backward_launches(shape),
+            "path": "gdn_backward_chunked: pre-pass, forward chain, reverse chain, per-chunk gradients "
+                    "(warp-level bf16 MMAs, fp32 accumulation)",
+            "roofline": {"bound": "tensor", "achieved": tf, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                         "frac": tf / peaks["bf16_tflops"], "traffic": None, "flops_per_call": flops,
+                         "flops_convention": "MMA products as executed, zero blocks of triangular operands skipped",
+                         "peak_source": peaks["source"], "hbm": hbm(ms)},
+            "gpu_launches": 4 * 10,
+            "sequential_fp32": {"ms": ms_s, "tokens_per_s": B * T * ws / (ms_s * 1e-3),
+                                "roofline": {"bound": "alu", "achieved": tf_s, "peak": peak_s, "unit": "TFLOP/s",
+                                             "frac": tf_s / peak_s, "flops_per_call": flops_s,
+                                             "peak_source": "fp32 FMA: 148 SMs x 128 lanes x 2 FLOPs at the "
+                                                            "sampled max SM clock", "hbm": hbm(ms_s)},
+                                "gpu_launches": gdn.backward_launches(shape) * 10, "clocks": clocks_s},
             "config": "training-shape backward: B=2, H=16, T=4096, d=128, bf16 q/k/v/dy, fp32 gates, state and "
                       "gradients; median of 10 calls",
-            "l2": "inputs and workspace larger than L2 (1.3 GB), no flush", "clocks": clocks,
+            "l2": "inputs and workspace larger than L2, no flush", "clocks": clocks,
             "cpu_baseline": _oracle_timed(lambda: time_oracle_backward(x, g, seed, args.oracle_seconds),
                                           "backward oracle") if local == 0 and not args.no_cpu_baseline else None}
 

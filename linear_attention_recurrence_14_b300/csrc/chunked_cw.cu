@@ -477,6 +477,8 @@ constexpr uint32_t kChainSmem = CH_MISC + 64;
 //   B: U = U~ + (-W) S and Y = Qp S (warp w: tokens 16 (w & 3), columns 64 (w >> 2));
 //   C: Y += P U, y stored; S = diag(e^{g_C}) S + Kl^T U into the fragments.
 // Chunk records stream in with asynchronous copies one chunk ahead.
+// WITH_Y = false (no y requested, only states): the Y products are skipped.
+template <bool WITH_Y>
 __global__ void __launch_bounds__(256, 1) cw_chain_kernel(const CwDev p) {
     extern __shared__ __align__(128) uint8_t sm[];
     const uint32_t sb = smem_u32(sm);
@@ -592,17 +594,19 @@ __global__ void __launch_bounds__(256, 1) cw_chain_kernel(const CwDev p) {
         }
 #pragma unroll 2
         for (int kk = 0; kk < 8; ++kk) {
-            uint32_t aw[4], aq[4];
+            uint32_t aw[4], aq[4] = {0u, 0u, 0u, 0u};
             ldsm_x4(aw, stg + REC_WN + sw256(16 * mt + a_row(lane), 2 * kk + a_ch(lane)));
-            ldsm_x4(aq, stg + REC_QP + sw256(16 * mt + a_row(lane), 2 * kk + a_ch(lane)));
+            if constexpr (WITH_Y) ldsm_x4(aq, stg + REC_QP + sw256(16 * mt + a_row(lane), 2 * kk + a_ch(lane)));
 #pragma unroll
             for (int np = 0; np < 4; ++np) {
                 uint32_t bs[4];
                 ldsm_x4_t(bs, sb + CH_SB + sw256(16 * kk + bt_row(lane), 8 * nh + 2 * np + bt_ch(lane)));
                 mma16816(u[2 * np], aw, bs[0], bs[1]);
                 mma16816(u[2 * np + 1], aw, bs[2], bs[3]);
-                mma16816(ys[2 * np], aq, bs[0], bs[1]);
-                mma16816(ys[2 * np + 1], aq, bs[2], bs[3]);
+                if constexpr (WITH_Y) {
+                    mma16816(ys[2 * np], aq, bs[0], bs[1]);
+                    mma16816(ys[2 * np + 1], aq, bs[2], bs[3]);
+                }
             }
         }
 #pragma unroll
@@ -615,7 +619,7 @@ __global__ void __launch_bounds__(256, 1) cw_chain_kernel(const CwDev p) {
 
         // C: Y += P U (P is zero above the diagonal blocks)
 #pragma unroll 1
-        for (int kk = 0; kk <= mt; ++kk) {
+        for (int kk = 0; WITH_Y && kk <= mt; ++kk) {
             uint32_t ap[4];
             ldsm_x4(ap, stg + REC_P + sw128(16 * mt + a_row(lane), 2 * kk + a_ch(lane)));
 #pragma unroll
@@ -626,7 +630,7 @@ __global__ void __launch_bounds__(256, 1) cw_chain_kernel(const CwDev p) {
                 mma16816(ys[2 * np + 1], ap, bu[2], bu[3]);
             }
         }
-        if (cc >= c_begin && p.y) {
+        if (WITH_Y && cc >= c_begin) {
 #pragma unroll
             for (int hr = 0; hr < 2; ++hr) {
                 const int64_t t = static_cast<int64_t>(cc) * kC + 16 * mt + g + 8 * hr;
@@ -680,7 +684,10 @@ cudaError_t set_cw_attributes() {
         cudaError_t e = cudaFuncSetAttribute(cw_prepass_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              static_cast<int>(kPrepassSmem));
         if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(cw_chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+            e = cudaFuncSetAttribute(cw_chain_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     static_cast<int>(kChainSmem));
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(cw_chain_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      static_cast<int>(kChainSmem));
         return e;
     }();
@@ -730,7 +737,10 @@ cudaError_t launch_chunked_cw(const ChunkedCwParams &p, cudaStream_t stream, int
     dv.scalar_alpha = p.scalar_alpha ? 1 : 0;
     dv.state_out = p.state_out;
     cw_prepass_kernel<<<static_cast<unsigned>(p.B * nchunks * p.Hv), 256, kPrepassSmem, stream>>>(dv);
-    cw_chain_kernel<<<static_cast<unsigned>(pairs * P), 256, kChainSmem, stream>>>(dv);
+    if (p.y)
+        cw_chain_kernel<true><<<static_cast<unsigned>(pairs * P), 256, kChainSmem, stream>>>(dv);
+    else
+        cw_chain_kernel<false><<<static_cast<unsigned>(pairs * P), 256, kChainSmem, stream>>>(dv);
     return cudaGetLastError();
 }
 
