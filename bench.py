@@ -595,6 +595,7 @@ def summarize(line: dict) -> dict:
         return float(f"{d:.4g}") if isinstance(d, (int, float)) else d
     out = {"grouped_ms": g(line, "roofline", "launch_ms"), "grouped_hbm": g(line, "roofline", "frac"),
            "grouped_tc": g(line, "roofline", "tensor", "frac"), "e2e_ms": g(line, "e2e", "ms_per_step"),
+           "e2e_of_link_floor": g(line, "e2e", "link", "frac_of_floor"),
            "check_err": g(line, "check", "max_rel_err_y")}
     for key, short in (("prefill_train", "train"), ("prefill_long", "long"), ("prefill_weak_decay", "weak"),
                        ("prefill_channelwise", "cw")):
@@ -661,8 +662,41 @@ def time_e2e(args, x, shape, w, dev, ws):
     torch.cuda.synchronize()
     ms = max_over_ranks(e0.elapsed_time(e1), ws, dev)
     value = w["B"] * w["T"] * ws * steps / (ms * 1e-3)
+    link = measure_link(dev, h2d, d2h)
+    floor_ms = max(h2d / (link["h2d_gbs"] * 1e9), d2h / (link["d2h_gbs"] * 1e9)) * 1e3
+    link.update({"floor_ms_per_step": floor_ms, "frac_of_floor": floor_ms / (ms / steps),
+                 "floor": "the step's copies at the measured link rates, the two directions overlapped"})
     return {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "steps": steps, "ms_per_step": ms / steps, "api": "gdn_prefill_host (pinned host buffers)"}
+            "steps": steps, "ms_per_step": ms / steps, "api": "gdn_prefill_host (pinned host buffers)",
+            "link": link}
+
+
+def measure_link(dev, h2d: int, d2h: int) -> dict:
+    """Host link rates: one pinned host -> device copy of h2d bytes and one device -> host copy of
+    d2h bytes, each timed alone with CUDA events (best of 3)."""
+    import torch
+
+    a = torch.empty(h2d, dtype=torch.uint8).pin_memory()
+    b = torch.empty(h2d, dtype=torch.uint8, device=dev)
+    c = torch.empty(d2h, dtype=torch.uint8, device=dev)
+    e = torch.empty(d2h, dtype=torch.uint8).pin_memory()
+
+    def best(fn, n):
+        t = []
+        for _ in range(3):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            torch.cuda.synchronize()
+            t.append(e0.elapsed_time(e1))
+        return n / (min(t) * 1e-3) / 1e9
+
+    out = {"h2d_gbs": best(lambda: b.copy_(a, non_blocking=True), h2d),
+           "d2h_gbs": best(lambda: e.copy_(c, non_blocking=True), d2h)}
+    del a, b, c, e
+    torch.cuda.empty_cache()
+    return out
 
 
 def layer_bytes(B, T, Hqk, Hv, d, kconv=4) -> tuple[int, int]:

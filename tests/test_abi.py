@@ -252,3 +252,66 @@ def test_backward_workspace_and_arguments(L):
     assert call(dS0=at["S0"]) == E["GDN_ERR_ALIASING"]
     # dS0 may be the very buffer of dS_T: past the host checks (no GPU here, so a CUDA/device status)
     assert call(dS0=at["dS_T"]) not in (E["GDN_ERR_ALIASING"], E["GDN_ERR_INVALID_ARG"], E["GDN_ERR_ALIGNMENT"])
+
+
+def test_chunked_backward_workspace_and_arguments(L):
+    E = {v: k for k, v in gdn.STATUS_NAMES.items()}
+    r = lambda n: (n + 255) // 256 * 256  # noqa: E731
+    # chunk records (74,240 bytes) and decay bounds (4 bytes) per (head, chunk); then the entering
+    # states and the state gradients (64 KB each per (head, chunk)); then dS0's staging
+    for B, T, Hv in [(2, 1000, 4), (1, 64, 2), (1, 65, 1)]:
+        s = shape(B=B, T=T, Hqk=1, Hv=Hv, d=128)
+        n = B * Hv * ((T + 63) // 64)
+        want = r(r(n * 74244) + 2 * n * 128 * 128 * 4) + B * Hv * 128 * 128 * 4
+        assert L.gdn_backward_chunked_workspace_bytes(ctypes.byref(s)) == want
+    assert L.gdn_backward_chunked_workspace_bytes(ctypes.byref(shape(d=64))) == 0
+    assert L.gdn_backward_chunked_workspace_bytes(ctypes.byref(shape(dtype=gdn.GDN_F32))) == 0
+    s = shape(B=1, T=64, Hqk=2, Hv=4, d=128)
+    n = L.gdn_backward_chunked_workspace_bytes(ctypes.byref(s))
+    vp = lambda x: None if x is None else ctypes.c_void_p(x)  # noqa: E731
+    names = ("q", "k", "v", "alpha", "beta", "S0", "dy", "dS_T", "dq", "dk", "dv", "dlog_alpha", "dbeta", "dS0")
+    at = {k_: BASE + i * 64 * MB for i, k_ in enumerate(names)}
+
+    def call(shp=s, ws=BASE + 16 * 64 * MB, ws_bytes=n, **over):
+        a = {**at, **over}
+        return L.gdn_backward_chunked(ctypes.byref(shp), *(vp(a[k_]) for k_ in names), vp(ws), ws_bytes, None)
+    assert call(shp=shape(dtype=gdn.GDN_F32)) == E["GDN_ERR_UNSUPPORTED"]
+    assert call(shp=shape(d=64)) == E["GDN_ERR_UNSUPPORTED"]
+    assert call(shp=shape(Hqk=3, Hv=4)) == E["GDN_ERR_INVALID_ARG"]
+    assert call(dy=None) == E["GDN_ERR_INVALID_ARG"]
+    assert call(ws=None) == E["GDN_ERR_WORKSPACE"]
+    assert call(ws_bytes=n - 1) == E["GDN_ERR_WORKSPACE"]
+    assert call(dq=at["q"]) == E["GDN_ERR_ALIASING"]
+    assert call(dv=at["dv"] + 4) == E["GDN_ERR_ALIGNMENT"]
+
+
+def test_channelwise_chunked_workspace_and_arguments(L):
+    E = {v: k for k, v in gdn.STATUS_NAMES.items()}
+    r = lambda n: (n + 255) // 256 * 256  # noqa: E731
+    for B, T, Hv in [(2, 1000, 4), (1, 1, 2)]:
+        s = shape(B=B, T=T, Hqk=2, Hv=Hv, d=128)
+        want = r(256 + B * Hv * 128 * 128 * 4) + B * Hv * ((T + 63) // 64) * 74244
+        assert L.gdn_prefill_cw_workspace_bytes(ctypes.byref(s)) == want
+    # shapes the token-sequential kernel takes need only the status area
+    assert L.gdn_prefill_cw_workspace_bytes(ctypes.byref(shape(d=64))) == 256
+    assert L.gdn_prefill_cw_workspace_bytes(ctypes.byref(shape(dtype=gdn.GDN_F32))) == 256
+    s = shape(B=1, T=200, Hqk=2, Hv=4, d=128)
+    n = L.gdn_prefill_cw_workspace_bytes(ctypes.byref(s))
+    vp = lambda x: None if x is None else ctypes.c_void_p(x)  # noqa: E731
+    names = ("q", "k", "v", "alpha", "beta", "S0", "y", "S_T")
+    at = {k_: BASE + i * 64 * MB for i, k_ in enumerate(names)}
+
+    def call(shp=s, opts=None, ws=BASE + 16 * 64 * MB, ws_bytes=n, **over):
+        a = {**at, **over}
+        return L.gdn_prefill_cw_ex(ctypes.byref(shp), None if opts is None else ctypes.byref(opts),
+                                   *(vp(a[k_]) for k_ in names), vp(ws), ws_bytes, None)
+    chunked = gdn.GdnPrefillOptions(0, 0.0, 0, gdn.ALGO_CHUNKED, 0)
+    assert call(shp=shape(d=64), opts=chunked) == E["GDN_ERR_UNSUPPORTED"]
+    assert call(opts=gdn.GdnPrefillOptions(-1, 0.0, 0, 0, 0)) == E["GDN_ERR_INVALID_ARG"]
+    assert call(opts=gdn.GdnPrefillOptions(0, 0.0, 0, 0, 3)) == E["GDN_ERR_INVALID_ARG"]   # no stall hook here
+    assert call(ws=None) == E["GDN_ERR_WORKSPACE"]
+    assert call(ws_bytes=n - 1) == E["GDN_ERR_WORKSPACE"]
+    assert call(ws=BASE + 16 * 64 * MB + 16) == E["GDN_ERR_ALIGNMENT"]
+    assert call(alpha=at["alpha"] + 4) == E["GDN_ERR_ALIGNMENT"]   # 16-byte rows of the channel gate
+    assert call(y=at["q"]) == E["GDN_ERR_ALIASING"]
+    assert call(ws=at["y"]) == E["GDN_ERR_ALIASING"]
