@@ -252,62 +252,90 @@ __global__ void __launch_bounds__(256, 2) cw_prepass_kernel(const CwDev p) {
         *reinterpret_cast<float4 *>(rr + 4) = *reinterpret_cast<const float4 *>(R + I * kD + pc * 8 + 4);
         *reinterpret_cast<float4 *>(gc) = *reinterpret_cast<const float4 *>(gC + pc * 8);
         *reinterpret_cast<float4 *>(gc + 4) = *reinterpret_cast<const float4 *>(gC + pc * 8 + 4);
-        uint32_t oqp[4], okl[4], oql[4], okq[4];
+        // end of this token's block: R_{I+1} (g_C for the last block)
+        float re[8];
+        const float *rn = I < 3 ? R + (I + 1) * kD + pc * 8 : gC + pc * 8;
+        *reinterpret_cast<float4 *>(re) = *reinterpret_cast<const float4 *>(rn);
+        *reinterpret_cast<float4 *>(re + 4) = *reinterpret_cast<const float4 *>(rn + 4);
+        uint32_t oqp[4], okl[4], oql[4], okq[4], okn[4];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
             const float2 qf = unpack2(qw[j]), kf = unpack2(kw[j]);
-            float e1[2], el[2], eo[2];
+            float e1[2], el[2], eo[2], en[2];
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 const float gv = gr[2 * j + h];
                 e1[h] = exp2_ftz(gv);
                 el[h] = exp2_ftz(gc[2 * j + h] - gv);
                 eo[h] = exp2_ftz(gv - rr[2 * j + h]);
+                en[h] = exp2_ftz(re[2 * j + h] - gv);   // <= 1: the block's end is no later than the token
             }
             oqp[j] = pack2(qf.x * e1[0], qf.y * e1[1]);
             okl[j] = pack2(kf.x * el[0], kf.y * el[1]);
             oql[j] = pack2(qf.x * eo[0], qf.y * eo[1]);
             okq[j] = pack2(kf.x * eo[0], kf.y * eo[1]);
+            okn[j] = pack2(kf.x * en[0], kf.y * en[1]);
         }
         *reinterpret_cast<uint4 *>(rec + REC_QP + t * 256 + pc * 16) = make_uint4(oqp[0], oqp[1], oqp[2], oqp[3]);
         *reinterpret_cast<uint4 *>(rec + REC_KL + t * 256 + pc * 16) = make_uint4(okl[0], okl[1], okl[2], okl[3]);
         *reinterpret_cast<uint4 *>(sm + PP_QT + off) = make_uint4(oql[0], oql[1], oql[2], oql[3]);
         *reinterpret_cast<uint4 *>(sm + PP_KL + off) = make_uint4(okq[0], okq[1], okq[2], okq[3]);
+        *reinterpret_cast<uint4 *>(sm + PP_KT + off) = make_uint4(okn[0], okn[1], okn[2], okn[3]);
     }
     __syncthreads();
 
-    // ---- A and P by row block I: Kn = K (.) e^{R_I - G} for the key rows s < 16(I+1),
-    // then the products with Kloc (A) and Qloc (P) of the block's 16 rows, one
-    // task per (product, pair of 8-column tiles).  Warp w keeps the A tile pair
-    // np = w of every block I >= w in registers until the q/k tiles are free.
+    // ---- A and P by row block I with Kn_I = K (.) 2^{R_I - G} on the key rows s < 16(I+1).
+    // The raw k tile now holds Knend = K (.) 2^{R_{J+1} - G} (J the block of s, bounded by 1), so
+    // Kn_I = Knend (.) 2^{R_I - R_{J+1}}: the factor is at most 1 before block I and the block's
+    // own decay inside it (rows of a block past 2^kMaxExp2 left zero for the element-wise path).
+    // All four Kn_I are built at once (into the G tile and the Kn tile); then each warp runs its
+    // product tasks of every row block without further barriers, one task per (product, pair of
+    // 8-column tiles).  Warp w keeps the A tile pair np = w of every block I >= w in registers
+    // until the q/k tiles are free.
+    auto kn_base = [](int I) -> uint32_t {   // rows 0..16(I+1)-1 of Kn_I
+        return I == 3 ? PP_KN : PP_G + static_cast<uint32_t>(I * (I + 1) / 2) * 16u * 256u;
+    };
+    // the factors 2^{R_I - R_{J+1}} for the ten (I, J <= I) pairs, per channel, in the G tile's
+    // last 8 KB (the Kn_I use its first 24 KB)
+    float *fac = reinterpret_cast<float *>(sm + PP_G + 24576);
+    for (int e = tid; e < 10 * kD; e += 256) {
+        const int pair = e >> 7, ch = e & (kD - 1);
+        const int I = pair < 1 ? 0 : (pair < 3 ? 1 : (pair < 6 ? 2 : 3));
+        const int J = pair - I * (I + 1) / 2;
+        const float rj = J < 3 ? R[(J + 1) * kD + ch] : gC[ch];
+        fac[e] = exp2_ftz(R[I * kD + ch] - rj);
+    }
+    __syncthreads();
+    for (int e = tid; e < 160 * 16; e += 256) {   // 16 + 32 + 48 + 64 rows
+        const int row = e >> 4, pc = e & 15;
+        const int I = row < 16 ? 0 : (row < 48 ? 1 : (row < 96 ? 2 : 3));
+        const int s = row - 16 * (I * (I + 1) / 2);
+        const int J = s >> 4;
+        uint4 out = zero4;
+        if (!(J == I && viol[I] != 0)) {
+            const uint4 kr = *reinterpret_cast<const uint4 *>(sm + PP_KT + sw256(s, pc));
+            const uint32_t kw[4] = {kr.x, kr.y, kr.z, kr.w};
+            float f[8];
+            const float *fp = fac + (I * (I + 1) / 2 + J) * kD + pc * 8;
+            *reinterpret_cast<float4 *>(f) = *reinterpret_cast<const float4 *>(fp);
+            *reinterpret_cast<float4 *>(f + 4) = *reinterpret_cast<const float4 *>(fp + 4);
+            uint32_t o[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const float2 kf = unpack2(kw[j]);
+                o[j] = pack2(kf.x * f[2 * j], kf.y * f[2 * j + 1]);
+            }
+            out = make_uint4(o[0], o[1], o[2], o[3]);
+        }
+        *reinterpret_cast<uint4 *>(sm + kn_base(I) + sw256(s, pc)) = out;
+    }
+    __syncthreads();
     float aacc[4][2][4];
 #pragma unroll
     for (int I = 0; I < 4; ++I) {
 #pragma unroll
         for (int e = 0; e < 8; ++e) aacc[I][e >> 2][e & 3] = 0.f;
         const bool vI = viol[I] != 0;
-        for (int e = tid; e < 16 * (I + 1) * 16; e += 256) {
-            const int s = e >> 4, pc = e & 15;
-            uint4 out = zero4;
-            if (!(vI && s >= 16 * I)) {
-                const uint4 kr = *reinterpret_cast<const uint4 *>(sm + PP_KT + sw256(s, pc));
-                const uint32_t kw[4] = {kr.x, kr.y, kr.z, kr.w};
-                float gr[8], rr[8];
-                *reinterpret_cast<float4 *>(gr) = *reinterpret_cast<const float4 *>(G + s * kD + pc * 8);
-                *reinterpret_cast<float4 *>(gr + 4) = *reinterpret_cast<const float4 *>(G + s * kD + pc * 8 + 4);
-                *reinterpret_cast<float4 *>(rr) = *reinterpret_cast<const float4 *>(R + I * kD + pc * 8);
-                *reinterpret_cast<float4 *>(rr + 4) = *reinterpret_cast<const float4 *>(R + I * kD + pc * 8 + 4);
-                uint32_t o[4];
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const float2 kf = unpack2(kw[j]);
-                    o[j] = pack2(kf.x * exp2_ftz(rr[2 * j] - gr[2 * j]), kf.y * exp2_ftz(rr[2 * j + 1] - gr[2 * j + 1]));
-                }
-                out = make_uint4(o[0], o[1], o[2], o[3]);
-            }
-            *reinterpret_cast<uint4 *>(sm + PP_KN + sw256(s, pc)) = out;
-        }
-        __syncthreads();
         const int ntask = 2 * (I + 1);
         if (warp < ntask) {
             const bool is_a = warp <= I;
@@ -318,7 +346,7 @@ __global__ void __launch_bounds__(256, 2) cw_prepass_kernel(const CwDev p) {
             for (int ks = 0; ks < 8; ++ks) {
                 uint32_t af[4], bf[4];
                 ldsm_x4(af, xa + sw256(16 * I + a_row(lane), 2 * ks + a_ch(lane)));
-                ldsm_x4(bf, sb + PP_KN + sw256(16 * np + bn_row(lane), 2 * ks + bn_ch(lane)));
+                ldsm_x4(bf, sb + kn_base(I) + sw256(16 * np + bn_row(lane), 2 * ks + bn_ch(lane)));
                 mma16816(acc[0], af, bf[0], bf[1]);
                 mma16816(acc[1], af, bf[2], bf[3]);
             }
@@ -345,8 +373,8 @@ __global__ void __launch_bounds__(256, 2) cw_prepass_kernel(const CwDev p) {
                 }
             }
         }
-        __syncthreads();
     }
+    __syncthreads();
     // P above the diagonal blocks: zeros
     for (int e = tid; e < 64 * 32; e += 256) {
         const int t = e >> 5, s = 2 * (e & 31);
