@@ -357,7 +357,7 @@ gdn_status gdn_backward(const gdn_shape *shape,
  * atomic additions (deterministic for up to two value heads per key head).
  * ws: device memory of gdn_backward_chunked_workspace_bytes(shape) bytes,
  * 256-byte aligned, no initial contents needed (74,244 bytes of chunk
- * operands plus two 64 KB states per (batch, value head, chunk), then
+ * operands plus two 32 KB bf16 states per (batch, value head, chunk), then
  * B*Hv*dk*dv fp32 to stage dS0 when it is dS_T's buffer).  Returns 0 bytes for
  * shapes the chunked path does not take.
  */

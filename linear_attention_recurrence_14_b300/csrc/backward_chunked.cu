@@ -45,8 +45,8 @@ struct BwDev {
     const float *dS_T;        // nullptr = zero
     const uint8_t *rec;       // chunk records [B * Hv][nchunks][rec::kBytes]
     const float *bound;       // per-chunk decay bounds [B * Hv][nchunks]
-    const float *state;       // state entering every chunk [B * Hv][nchunks][d][d]
-    float *dstate;            // gradient of the state leaving every chunk, same layout
+    const __nv_bfloat16 *state;   // state entering every chunk [B * Hv][nchunks][d][d] (bf16, the products' operand)
+    __nv_bfloat16 *dstate;        // gradient of the state leaving every chunk, same layout
     float *dS0;               // nullptr = not returned
     float *dq, *dk;           // [B, T, Hqk, d] (summed over the value heads of a group)
     float *dv;                // [B, T, Hv, d]
@@ -156,12 +156,12 @@ __global__ void __launch_bounds__(256, 1) bw_reverse_chain_kernel(const BwDev p)
         const uint32_t stg = sb + st * RC_STAGE;
         const uint8_t *stp = sm + st * RC_STAGE;
         if (cc < c_end) {
-            float *so = p.dstate + (static_cast<int64_t>(pr) * p.nchunks + cc) * kD * kD;
+            __nv_bfloat16 *so = p.dstate + (static_cast<int64_t>(pr) * p.nchunks + cc) * kD * kD;
 #pragma unroll
             for (int nt = 0; nt < 16; ++nt) {
                 const int r = 16 * warp + g, col = 8 * nt + 2 * t4;
-                *reinterpret_cast<float2 *>(so + r * kD + col) = make_float2(S[nt][0], S[nt][1]);
-                *reinterpret_cast<float2 *>(so + (r + 8) * kD + col) = make_float2(S[nt][2], S[nt][3]);
+                *reinterpret_cast<uint32_t *>(so + r * kD + col) = pack2(S[nt][0], S[nt][1]);
+                *reinterpret_cast<uint32_t *>(so + (r + 8) * kD + col) = pack2(S[nt][2], S[nt][3]);
             }
         }
         // A: bf16 copy of dS'
@@ -340,28 +340,17 @@ __global__ void __launch_bounds__(256, 1) bw_chunk_grad_kernel(const BwDev p) {
             *reinterpret_cast<uint4 *>(sm + BG_DY + off) = zero4;
         }
     }
-    cp_async_commit();
-    float sds = 0.f;   // sum of S (.) dS'
     {
-        const float *Sg = p.state + (pr * p.nchunks + c) * kD * kD;
-        const float *Dg = p.dstate + (pr * p.nchunks + c) * kD * kD;
-        for (int e = tid; e < kD * 16; e += 256) {   // 128 rows x 16 pieces of 8 floats
+        // the entering state and the leaving state gradient, bf16 [dk][dv] rows, into their tiles
+        const __nv_bfloat16 *Sg = p.state + (pr * p.nchunks + c) * kD * kD;
+        const __nv_bfloat16 *Dg = p.dstate + (pr * p.nchunks + c) * kD * kD;
+        for (int e = tid; e < kD * 16; e += 256) {   // 128 rows x 16 pieces of 8
             const int r = e >> 4, pc = e & 15;
-            const float4 s0 = *reinterpret_cast<const float4 *>(Sg + r * kD + pc * 8);
-            const float4 s1 = *reinterpret_cast<const float4 *>(Sg + r * kD + pc * 8 + 4);
-            const float4 d0 = *reinterpret_cast<const float4 *>(Dg + r * kD + pc * 8);
-            const float4 d1 = *reinterpret_cast<const float4 *>(Dg + r * kD + pc * 8 + 4);
-            sds += s0.x * d0.x + s0.y * d0.y + s0.z * d0.z + s0.w * d0.w + s1.x * d1.x + s1.y * d1.y + s1.z * d1.z +
-                   s1.w * d1.w;
-            *reinterpret_cast<uint4 *>(sm + BG_S + sw256(r, pc)) =
-                make_uint4(pack2(s0.x, s0.y), pack2(s0.z, s0.w), pack2(s1.x, s1.y), pack2(s1.z, s1.w));
-            *reinterpret_cast<uint4 *>(sm + BG_DS + sw256(r, pc)) =
-                make_uint4(pack2(d0.x, d0.y), pack2(d0.z, d0.w), pack2(d1.x, d1.y), pack2(d1.z, d1.w));
+            cp_async16(sb + BG_S + sw256(r, pc), Sg + r * kD + pc * 8);
+            cp_async16(sb + BG_DS + sw256(r, pc), Dg + r * kD + pc * 8);
         }
     }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) sds += __shfl_xor_sync(0xffffffffu, sds, o);
-    if (lane == 0) fs[SM_RED + warp] = sds;
+    cp_async_commit();
     // gates: g = inclusive cumsum of log alpha (tokens past T: alpha = 1, beta = 0)
     if (tid < kC) {
         const int64_t gi = (static_cast<int64_t>(b) * p.T + t0 + tid) * p.Hv + hv;
@@ -378,6 +367,24 @@ __global__ void __launch_bounds__(256, 1) bw_chunk_grad_kernel(const BwDev p) {
     }
     cp_async_wait_all();
     __syncthreads();
+    {
+        // sum of S (.) dS' over the bf16 tiles (the same values the products use)
+        float sds = 0.f;
+        for (int e = tid; e < kD * 16; e += 256) {
+            const int r = e >> 4, pc = e & 15;
+            const uint4 a = *reinterpret_cast<const uint4 *>(sm + BG_S + sw256(r, pc));
+            const uint4 d = *reinterpret_cast<const uint4 *>(sm + BG_DS + sw256(r, pc));
+            const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, dw[4] = {d.x, d.y, d.z, d.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const float2 x = unpack2(aw[j]), y = unpack2(dw[j]);
+                sds = fmaf(x.x, y.x, fmaf(x.y, y.y, sds));
+            }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) sds += __shfl_xor_sync(0xffffffffu, sds, o);
+        if (lane == 0) fs[SM_RED + warp] = sds;
+    }
     if (tid < kC) {
         const float gv = fs[SM_G + tid] + (tid >= 32 ? fs[SM_WS] : 0.f);
         const float glast = fs[SM_WS] + fs[SM_WS + 1];
@@ -1004,14 +1011,14 @@ cudaError_t set_bw_attributes() {
 }  // namespace
 
 // Workspace: the chunk records and decay bounds, then (256-byte aligned) the
-// states entering and the state gradients leaving every chunk.
+// states entering and the state gradients leaving every chunk (bf16).
 static size_t states_offset(int64_t B, int64_t T, int Hv) {
     return (chunked_cw_ops_bytes(B, T, Hv) + 255) / 256 * 256;
 }
 
 size_t backward_chunked_workspace_bytes(int64_t B, int64_t T, int Hv) {
     const int64_t nchunks = (T + kC - 1) / kC;
-    const size_t states = static_cast<size_t>(B) * Hv * nchunks * kD * kD * sizeof(float);
+    const size_t states = static_cast<size_t>(B) * Hv * nchunks * kD * kD * sizeof(__nv_bfloat16);
     return states_offset(B, T, Hv) + 2 * states;
 }
 
@@ -1023,9 +1030,9 @@ cudaError_t launch_backward_chunked(const BackwardParams &p, uint8_t *ws, cudaSt
     cudaError_t e = set_bw_attributes();
     if (e != cudaSuccess) return e;
     const size_t ops = states_offset(p.B, p.T, p.Hv);
-    const size_t states = static_cast<size_t>(pairs) * nchunks * kD * kD * sizeof(float);
-    float *state = reinterpret_cast<float *>(ws + ops);
-    float *dstate = reinterpret_cast<float *>(ws + ops + states);
+    const size_t states = static_cast<size_t>(pairs) * nchunks * kD * kD * sizeof(__nv_bfloat16);
+    __nv_bfloat16 *state = reinterpret_cast<__nv_bfloat16 *>(ws + ops);
+    __nv_bfloat16 *dstate = reinterpret_cast<__nv_bfloat16 *>(ws + ops + states);
 
     // forward: chunk records and the state entering every chunk
     ChunkedCwParams f{};

@@ -79,7 +79,7 @@ struct CwDev {
     uint8_t *rec;     // [B * Hv][nchunks][kRecBytes]
     float *bound;     // [B * Hv][nchunks]
     int scalar_alpha; // alpha is [B, T, Hv], the same decay for every channel
-    float *state_out; // nullptr, or the state entering every chunk [B * Hv][nchunks][d][d] fp32
+    __nv_bfloat16 *state_out; // nullptr, or the state entering every chunk [B * Hv][nchunks][d][d] bf16
 };
 
 // Pre-pass shared memory (bytes).  After the A and P products the q/k tiles
@@ -587,12 +587,12 @@ __global__ void __launch_bounds__(256, 1) cw_chain_kernel(const CwDev p) {
         const uint32_t stg = sb + st * kRecBytes;
         const uint8_t *stp = sm + st * kRecBytes;
         if (p.state_out && cc >= c_begin) {
-            float *so = p.state_out + (static_cast<int64_t>(pr) * p.nchunks + cc) * kD * kD;
+            __nv_bfloat16 *so = p.state_out + (static_cast<int64_t>(pr) * p.nchunks + cc) * kD * kD;
 #pragma unroll
             for (int nt = 0; nt < 16; ++nt) {
                 const int r = 16 * warp + g, col = 8 * nt + 2 * t4;
-                *reinterpret_cast<float2 *>(so + r * kD + col) = make_float2(S[nt][0], S[nt][1]);
-                *reinterpret_cast<float2 *>(so + (r + 8) * kD + col) = make_float2(S[nt][2], S[nt][3]);
+                *reinterpret_cast<uint32_t *>(so + r * kD + col) = pack2(S[nt][0], S[nt][1]);
+                *reinterpret_cast<uint32_t *>(so + (r + 8) * kD + col) = pack2(S[nt][2], S[nt][3]);
             }
         }
         // A: bf16 copy of the state
@@ -763,7 +763,7 @@ cudaError_t launch_chunked_cw(const ChunkedCwParams &p, cudaStream_t stream, int
     dv.rec = p.ops;
     dv.bound = reinterpret_cast<float *>(p.ops + static_cast<size_t>(pairs) * nchunks * kRecBytes);
     dv.scalar_alpha = p.scalar_alpha ? 1 : 0;
-    dv.state_out = p.state_out;
+    dv.state_out = static_cast<__nv_bfloat16 *>(p.state_out);
     cw_prepass_kernel<<<static_cast<unsigned>(p.B * nchunks * p.Hv), 256, kPrepassSmem, stream>>>(dv);
     if (p.y)
         cw_chain_kernel<true><<<static_cast<unsigned>(pairs * P), 256, kChainSmem, stream>>>(dv);

@@ -85,7 +85,7 @@ struct ChunkedCwParams {
     int max_warmup_chunks;
     uint8_t *ops;                // chunked_cw_ops_bytes(B, T, Hv) bytes, 16-byte aligned
     bool scalar_alpha;           // alpha is [B, T, Hv] (one decay for every channel)
-    float *state_out;            // nullptr, or the state entering every chunk [B * Hv][nchunks][d][d]
+    void *state_out;             // nullptr, or the state entering every chunk [B * Hv][nchunks][d][d] bf16
 };
 
 // The per-chunk operand record the chunked pre-pass writes (bytes): -W, U~,

@@ -258,11 +258,11 @@ def test_chunked_backward_workspace_and_arguments(L):
     E = {v: k for k, v in gdn.STATUS_NAMES.items()}
     r = lambda n: (n + 255) // 256 * 256  # noqa: E731
     # chunk records (74,240 bytes) and decay bounds (4 bytes) per (head, chunk); then the entering
-    # states and the state gradients (64 KB each per (head, chunk)); then dS0's staging
+    # states and the state gradients (bf16, 32 KB each per (head, chunk)); then dS0's staging
     for B, T, Hv in [(2, 1000, 4), (1, 64, 2), (1, 65, 1)]:
         s = shape(B=B, T=T, Hqk=1, Hv=Hv, d=128)
         n = B * Hv * ((T + 63) // 64)
-        want = r(r(n * 74244) + 2 * n * 128 * 128 * 4) + B * Hv * 128 * 128 * 4
+        want = r(r(n * 74244) + 2 * n * 128 * 128 * 2) + B * Hv * 128 * 128 * 4
         assert L.gdn_backward_chunked_workspace_bytes(ctypes.byref(s)) == want
     assert L.gdn_backward_chunked_workspace_bytes(ctypes.byref(shape(d=64))) == 0
     assert L.gdn_backward_chunked_workspace_bytes(ctypes.byref(shape(dtype=gdn.GDN_F32))) == 0
