@@ -346,13 +346,17 @@ def prefill_cw(q, k, v, alpha, beta, S0=None, *, y=None, S_T=None, workspace=Non
         y = torch.empty_like(v)
     if S_T is None:
         S_T = torch.empty((shape.B, shape.Hv, shape.dk, shape.dv), dtype=torch.float32, device=v.device)
-    if workspace is None:
+    own_ws = workspace is None
+    if own_ws:
         workspace = new_cw_workspace(shape, v.device)
     opts = GdnPrefillOptions(segments, log_eps, max_warmup_chunks, algorithm, 0)
     rc = lib().gdn_prefill_cw_ex(ctypes.byref(shape), ctypes.byref(opts), _ptr(q), _ptr(k), _ptr(v), _ptr(alpha),
                                  _ptr(beta), _ptr(S0), _ptr(y), _ptr(S_T), _ptr(workspace), workspace.numel(),
                                  _stream(stream))
     _check(rc, "gdn_prefill_cw_ex")
+    if own_ws and stream is not None:
+        # allocated on the current stream but used on `stream`: keep it from being reused too early
+        workspace.record_stream(stream)
     return y, S_T
 
 
