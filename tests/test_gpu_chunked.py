@@ -235,3 +235,15 @@ def test_short_sequence_restarts_instead_of_splitting():
     x = make_prefill_inputs(1, 64 * 40 + 5, 2, 4, 128, "bf16", decay_scale=0.0, s0_std=0.02, seed=67, device="cuda")
     y, S_T = _chunked(x, segments=5)
     _oracle_check(x, y, S_T)
+
+
+def test_prefill_launch_counts():
+    # gdn_prefill_launches: 4 kernels when the exact split is taken (long bf16 sequences over several
+    # segments with a full workspace), else 1; 0 for an empty problem.
+    big = gdn.GdnShape(1, 64 * 1024, 16, 32, 128, 128, gdn.GDN_BF16)   # the grouped shape
+    assert gdn.prefill_launches(big) == 4
+    assert gdn.prefill_launches(big, segments=1) == 1                  # one segment: nothing to split
+    assert gdn.prefill_launches(big, algorithm=gdn.ALGO_SEQUENTIAL) == 1
+    train = gdn.GdnShape(2, 4096, 16, 16, 128, 128, gdn.GDN_BF16)     # 64 chunks: restarts, no split
+    assert gdn.prefill_launches(train) == 1
+    assert gdn.prefill_launches(gdn.GdnShape(1, 0, 1, 2, 128, 128, gdn.GDN_BF16)) == 0
