@@ -124,6 +124,7 @@ def _check_chunked(out, ref, names=("dq", "dk", "dv", "dlog_alpha", "dbeta", "dS
     (2, 200, 2, 4, 0.0, 1.0, 0.1),       # several chunks, ragged tail, no initial state
     (1, 150, 1, 1, 0.02, 0.0, 0.5),      # strong decay, no state gradient
     (1, 1, 1, 2, 0.05, 1.0, 0.1),        # a single token
+    (2, 333, 1, 4, 0.02, 1.0, 0.1),      # four value heads per key head (dq, dk summed by atomics)
 ])
 def test_backward_chunked_matches_oracle(B, T, Hqk, Hv, s0, ds, decay):
     x = make_prefill_inputs(B, T, Hqk, Hv, 128, "bf16", decay_scale=decay, s0_std=s0, seed=T + 91, device="cuda")

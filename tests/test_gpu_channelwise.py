@@ -78,6 +78,7 @@ def _cw_chunked(x, a, **kw):
     (2, 777, 1, 2, 0.02, 3, 0.1),     # segments with warm-up windows
     (1, 1500, 2, 2, 0.05, 7, 0.5),    # strong decay: short windows
     (1, 640, 1, 2, 0.02, 4, 0.0),     # alpha = 1: no window, segments restart from token 0
+    (1, 500, 1, 4, 0.02, 2, 0.1),     # four value heads per key head
 ])
 def test_prefill_cw_chunked_matches_oracle(B, T, Hqk, Hv, s0, segments, decay):
     x = make_prefill_inputs(B, T, Hqk, Hv, 128, "bf16", s0_std=s0, seed=T + 7, device="cuda")
