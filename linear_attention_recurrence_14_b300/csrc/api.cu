@@ -367,10 +367,25 @@ static bool cw_chunked(const gdn_shape &s, int algorithm) {
     return s.dtype == GDN_BF16 && s.dk == 128 && s.dv == 128;
 }
 
+// Segment count for which the exact split's maps are reserved: about two
+// waves of a GPU with up to kExactSplitSmBound SMs (at most the chunk count).
+static int64_t split_segments(const gdn_shape &s) {
+    return gdn::exact_split_segments(s.B * s.Hv, (s.T + 63) / 64);
+}
+
 // Workspace of the chunked channel-wise prefill: status area, in-place
-// staging, then the per-chunk operand records and decay bounds.
-static size_t cw_layout(const gdn_shape &s, int64_t n_state, size_t *off_ops) {
-    *off_ops = round256(kStatusBytes + static_cast<size_t>(n_state) * sizeof(float));
+// staging, the exact split's flags and segment maps, then the per-chunk
+// operand records and decay bounds.
+static size_t cw_layout(const gdn_shape &s, int64_t n_state, size_t *off_ops, size_t *off_flag = nullptr,
+                        size_t *off_seg = nullptr, size_t *seg_bytes = nullptr) {
+    const size_t base = round256(kStatusBytes + static_cast<size_t>(n_state) * sizeof(float));
+    const int64_t segs = split_segments(s), pairs = s.B * s.Hv;
+    const size_t flags = round256(static_cast<size_t>(pairs) * segs * sizeof(int));
+    const size_t maps = static_cast<size_t>(pairs) * segs * 3 * s.dk * s.dv * sizeof(float);
+    if (off_flag) *off_flag = base;
+    if (off_seg) *off_seg = base + flags;
+    if (seg_bytes) *seg_bytes = maps;
+    *off_ops = base + flags + round256(maps);
     return *off_ops + gdn::chunked_cw_ops_bytes(s.B, s.T, s.Hv);
 }
 
@@ -440,6 +455,15 @@ gdn_status gdn_prefill_cw_ex(const gdn_shape *shape, const gdn_prefill_options *
     p.log_eps = opt.log_eps < 0.f ? opt.log_eps : kDefaultLogEps;
     p.max_warmup_chunks = opt.max_warmup_chunks > 0 ? opt.max_warmup_chunks : kDefaultMaxWarmupChunks;
     p.ops = static_cast<uint8_t *>(ws) + off_ops;
+    {
+        size_t off_flag = 0, off_seg = 0, seg_bytes = 0;
+        cw_layout(s, n_state, &off_ops, &off_flag, &off_seg, &seg_bytes);
+        if (seg_bytes > 0) {
+            p.exact_flag = reinterpret_cast<int *>(static_cast<char *>(ws) + off_flag);
+            p.seg_state = reinterpret_cast<float *>(static_cast<char *>(ws) + off_seg);
+            p.seg_state_bytes = seg_bytes;
+        }
+    }
     st = from_cuda(gdn::launch_chunked_cw(p, stream, num_sms));
     if (st != GDN_OK) return st;
     if (in_place) return from_cuda(cudaMemcpyAsync(S_T, staging, rst.n, cudaMemcpyDeviceToDevice, stream));

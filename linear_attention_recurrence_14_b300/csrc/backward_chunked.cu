@@ -51,7 +51,48 @@ struct BwDev {
     float *dq, *dk;           // [B, T, Hqk, d] (summed over the value heads of a group)
     float *dv;                // [B, T, Hv, d]
     float *dlog_alpha, *dbeta;   // [B, T, Hv]
+    // Exact sequence split of the reverse chain (heads whose segments reach no
+    // window): pass 1 runs the transitions (kind 0: from dS = 0 with dY, or
+    // from dS_T for the last segment; kind 1: from the identity with dY
+    // zero), pass 0 the output pass.  Segment s's maps are stored at index
+    // nseg - 1 - s, so that the forward combine chains them from the last
+    // segment down: seg_state [pairs][nseg][3][d][d].
+    int nseg, pass;
+    const int *exact_flag;
+    float *seg_state;
 };
+
+// Reverse-chain plan: flag[pair][nseg - 1 - s] = 1 when segment s < nseg - 1
+// reaches neither a window of later chunks nor the sequence's end within the
+// limit.  One thread per (pair, segment).
+__global__ void bw_plan_kernel(const BwDev p, int *flag) {
+    const int pairs = p.B * p.Hv;
+    const int idx = static_cast<int>(blockIdx.x * blockDim.x + threadIdx.x);
+    if (idx >= pairs * (p.nseg - 1)) return;
+    const int pr = idx % pairs, seg = idx / pairs;   // seg = 0 .. nseg - 2
+    const int c_end = (seg + 1) * p.seg_chunks;
+    float acc = 0.f;
+    int v = 1;
+    for (int m = 0; m < p.max_warmup; ++m) {
+        const int cc = c_end + m;
+        if (cc >= p.nchunks) {
+            v = 0;
+            break;
+        }
+        acc += p.bound[static_cast<int64_t>(pr) * p.nchunks + cc];
+        if (acc <= p.log_eps) {
+            v = 0;
+            break;
+        }
+    }
+    flag[static_cast<int64_t>(pr) * p.nseg + (p.nseg - 1 - seg)] = v;
+}
+
+__device__ __forceinline__ bool bw_head_split(const int *flag, int pr, int nseg) {
+    int any = 0;
+    for (int sg = 1; sg < nseg; ++sg) any |= flag[static_cast<int64_t>(pr) * nseg + sg];
+    return any != 0;
+}
 
 // ------------------------------------------------------------ reverse chain
 // Stage: a chunk record, then the chunk's dY tile (swizzled [64][128] bf16).
@@ -76,16 +117,25 @@ __global__ void __launch_bounds__(256, 1) bw_reverse_chain_kernel(const BwDev p)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int g = lane >> 2, t4 = lane & 3;
     const int pairs = p.B * p.Hv;
-    const int pr = static_cast<int>(blockIdx.x % static_cast<unsigned>(pairs));
-    const int seg = static_cast<int>(blockIdx.x / static_cast<unsigned>(pairs));
+    const unsigned per_pass = static_cast<unsigned>(pairs * p.nseg);
+    const int bx = static_cast<int>(blockIdx.x % per_pass);
+    const int kind = p.pass == 1 ? static_cast<int>(blockIdx.x / per_pass) : -1;
+    const int pr = bx % pairs;
+    const int seg = bx / pairs;
     const int b = pr / p.Hv, hv = pr % p.Hv;
     const int c_begin = seg * p.seg_chunks;
     const int c_end = c_begin + p.seg_chunks < p.nchunks ? c_begin + p.seg_chunks : p.nchunks;
     int *misc = reinterpret_cast<int *>(sm + RC_MISC);
+    const int sp = p.nseg - 1 - seg;   // where this segment's maps are stored
+    const bool split = p.exact_flag != nullptr && bw_head_split(p.exact_flag, pr, p.nseg);
+    if (p.pass == 1 && (!split || seg == 0 || (kind == 1 && seg == p.nseg - 1))) return;
 
     if (tid == 0) {
         int cs = p.nchunks - 1;   // exact start
-        if (c_end < p.nchunks) {
+        if (p.pass == 1 || split) {
+            cs = -1 - (c_end - 1);   // the segment's own last chunk (encoded as a windowed start)
+            if (c_end == p.nchunks && kind != 1) cs = p.nchunks - 1;   // the last segment from dS_T
+        } else if (c_end < p.nchunks) {
             float acc = 0.f;
             for (int m = 0;; ++m) {
                 const int cc = c_end + m;
@@ -105,7 +155,15 @@ __global__ void __launch_bounds__(256, 1) bw_reverse_chain_kernel(const BwDev p)
 
     float S[16][4];   // dS
     {
-        const float *s0 = (exact && p.dS_T) ? p.dS_T + static_cast<int64_t>(pr) * kD * kD : nullptr;
+        // dS_T for an exact start; the combined gradient for a split head's other segments
+        // (output pass); the identity for a kind-1 transition; else zero
+        const float *s0 = nullptr;
+        if (kind == 1)
+            s0 = nullptr;
+        else if (exact)
+            s0 = p.dS_T ? p.dS_T + static_cast<int64_t>(pr) * kD * kD : nullptr;
+        else if (p.pass == 0 && split)
+            s0 = p.seg_state + ((static_cast<int64_t>(pr) * p.nseg + sp) * 3 + 2) * kD * kD;
 #pragma unroll
         for (int nt = 0; nt < 16; ++nt) {
             const int r = 16 * warp + g, col = 8 * nt + 2 * t4;
@@ -113,6 +171,9 @@ __global__ void __launch_bounds__(256, 1) bw_reverse_chain_kernel(const BwDev p)
             if (s0) {
                 lo = *reinterpret_cast<const float2 *>(s0 + r * kD + col);
                 hi = *reinterpret_cast<const float2 *>(s0 + (r + 8) * kD + col);
+            } else if (kind == 1) {
+                lo = make_float2(r == col ? 1.f : 0.f, r == col + 1 ? 1.f : 0.f);
+                hi = make_float2(r + 8 == col ? 1.f : 0.f, r + 8 == col + 1 ? 1.f : 0.f);
             }
             S[nt][0] = lo.x;
             S[nt][1] = lo.y;
@@ -155,7 +216,7 @@ __global__ void __launch_bounds__(256, 1) bw_reverse_chain_kernel(const BwDev p)
         const int st = (c_start - cc) & 1;
         const uint32_t stg = sb + st * RC_STAGE;
         const uint8_t *stp = sm + st * RC_STAGE;
-        if (cc < c_end) {
+        if (cc < c_end && p.pass == 0) {
             __nv_bfloat16 *so = p.dstate + (static_cast<int64_t>(pr) * p.nchunks + cc) * kD * kD;
 #pragma unroll
             for (int nt = 0; nt < 16; ++nt) {
@@ -182,7 +243,7 @@ __global__ void __launch_bounds__(256, 1) bw_reverse_chain_kernel(const BwDev p)
 #pragma unroll
             for (int e = 0; e < 4; ++e) du[nt][e] = 0.f;
 #pragma unroll 1
-        for (int kk = mt; kk < 4; ++kk) {   // P^T[t][s] is zero for s below the row block
+        for (int kk = mt; kk < 4 && kind != 1; ++kk) {   // P^T[t][s] is zero for s below the row block
             uint32_t ap[4];
             ldsm_x4_t(ap, stg + rec::kP + sw128(16 * kk + at_row(lane), 2 * mt + at_ch(lane)));
 #pragma unroll
@@ -235,16 +296,23 @@ __global__ void __launch_bounds__(256, 1) bw_reverse_chain_kernel(const BwDev p)
                 uint32_t by[4], bu[4];
                 ldsm_x4_t(by, stg + RC_DY + sw256(16 * kk + bt_row(lane), 2 * np + bt_ch(lane)));
                 ldsm_x4_t(bu, sb + RC_UB + sw256(16 * kk + bt_row(lane), 2 * np + bt_ch(lane)));
-                mma16816(S[2 * np], aq, by[0], by[1]);
-                mma16816(S[2 * np + 1], aq, by[2], by[3]);
+                if (kind != 1) {   // dY zero on a kind-1 transition
+                    mma16816(S[2 * np], aq, by[0], by[1]);
+                    mma16816(S[2 * np + 1], aq, by[2], by[3]);
+                }
                 mma16816(S[2 * np], aw, bu[0], bu[1]);
                 mma16816(S[2 * np + 1], aw, bu[2], bu[3]);
             }
         }
     }
 
-    if (c_begin == 0 && p.dS0) {
-        float *so = p.dS0 + static_cast<int64_t>(pr) * kD * kD;
+    float *s_end = nullptr;   // where this run's final gradient goes
+    if (p.pass == 1)
+        s_end = p.seg_state + ((static_cast<int64_t>(pr) * p.nseg + sp) * 3 + kind) * kD * kD;
+    else if (c_begin == 0 && p.dS0)
+        s_end = p.dS0 + static_cast<int64_t>(pr) * kD * kD;
+    if (s_end) {
+        float *so = s_end;
 #pragma unroll
         for (int nt = 0; nt < 16; ++nt) {
             const int r = 16 * warp + g, col = 8 * nt + 2 * t4;
@@ -1016,10 +1084,24 @@ static size_t states_offset(int64_t B, int64_t T, int Hv) {
     return (chunked_cw_ops_bytes(B, T, Hv) + 255) / 256 * 256;
 }
 
-size_t backward_chunked_workspace_bytes(int64_t B, int64_t T, int Hv) {
+// After the states: the exact split's flags and segment maps (used by the
+// forward chain, then by the reverse chain, in stream order).
+static size_t split_offset(int64_t B, int64_t T, int Hv) {
     const int64_t nchunks = (T + kC - 1) / kC;
     const size_t states = static_cast<size_t>(B) * Hv * nchunks * kD * kD * sizeof(__nv_bfloat16);
-    return states_offset(B, T, Hv) + 2 * states;
+    return (states_offset(B, T, Hv) + 2 * states + 255) / 256 * 256;
+}
+
+static void split_sizes(int64_t B, int64_t T, int Hv, size_t *flag_bytes, size_t *map_bytes) {
+    const int64_t pairs = B * Hv, segs = exact_split_segments(pairs, (T + kC - 1) / kC);
+    *flag_bytes = (static_cast<size_t>(pairs) * segs * sizeof(int) + 255) / 256 * 256;
+    *map_bytes = static_cast<size_t>(pairs) * segs * 3 * kD * kD * sizeof(float);
+}
+
+size_t backward_chunked_workspace_bytes(int64_t B, int64_t T, int Hv) {
+    size_t fb = 0, mb = 0;
+    split_sizes(B, T, Hv, &fb, &mb);
+    return split_offset(B, T, Hv) + fb + mb;
 }
 
 cudaError_t launch_backward_chunked(const BackwardParams &p, uint8_t *ws, cudaStream_t stream, int num_sms) {
@@ -1041,6 +1123,15 @@ cudaError_t launch_backward_chunked(const BackwardParams &p, uint8_t *ws, cudaSt
     f.y = nullptr; f.S_T = nullptr;
     f.segments = 0; f.log_eps = -13.862943611198906f; f.max_warmup_chunks = 64;
     f.ops = ws; f.scalar_alpha = true; f.state_out = state;
+    size_t flag_bytes = 0, map_bytes = 0;
+    split_sizes(p.B, p.T, p.Hv, &flag_bytes, &map_bytes);
+    int *flags = reinterpret_cast<int *>(ws + split_offset(p.B, p.T, p.Hv));
+    float *maps = reinterpret_cast<float *>(ws + split_offset(p.B, p.T, p.Hv) + flag_bytes);
+    if (map_bytes > 0) {
+        f.exact_flag = flags;
+        f.seg_state = maps;
+        f.seg_state_bytes = map_bytes;
+    }
     e = launch_chunked_cw(f, stream, num_sms);
     if (e != cudaSuccess) return e;
 
@@ -1074,6 +1165,22 @@ cudaError_t launch_backward_chunked(const BackwardParams &p, uint8_t *ws, cudaSt
     dv.dv = p.dv;
     dv.dlog_alpha = p.dlog_alpha;
     dv.dbeta = p.dbeta;
+    dv.nseg = P;
+    dv.pass = 0;
+    dv.exact_flag = nullptr;
+    dv.seg_state = nullptr;
+    if (map_bytes > 0 && takes_exact_split(pairs, nchunks, P, kD, map_bytes)) {
+        // the reverse chain's exact split: plan, transitions, combine (maps stored in reverse
+        // segment order, so the forward combine applies), then the output pass
+        dv.exact_flag = flags;
+        dv.seg_state = maps;
+        const int nplan = static_cast<int>(pairs * (P - 1));
+        bw_plan_kernel<<<static_cast<unsigned>((nplan + 127) / 128), 128, 0, stream>>>(dv, flags);
+        dv.pass = 1;
+        bw_reverse_chain_kernel<<<static_cast<unsigned>(2 * pairs * P), 256, kRevSmem, stream>>>(dv);
+        if ((e = launch_segment_combine(flags, maps, pairs, P, kD, stream)) != cudaSuccess) return e;
+        dv.pass = 0;
+    }
     bw_reverse_chain_kernel<<<static_cast<unsigned>(pairs * P), 256, kRevSmem, stream>>>(dv);
     if (p.group > 1) {   // dq, dk accumulate over the value heads of a group
         const size_t nqk = static_cast<size_t>(p.B) * p.T * p.Hqk * kD * sizeof(float);

@@ -80,7 +80,47 @@ struct CwDev {
     float *bound;     // [B * Hv][nchunks]
     int scalar_alpha; // alpha is [B, T, Hv], the same decay for every channel
     __nv_bfloat16 *state_out; // nullptr, or the state entering every chunk [B * Hv][nchunks][d][d] bf16
+    // Exact sequence split (chain): nseg segments per head; pass 1 runs the
+    // transitions of the heads with a flag set (kind 0: from the zero state,
+    // or S0 for segment 0, with the values; kind 1: from the identity with
+    // the values zero), pass 0 the output pass, where those heads start every
+    // segment from the state the combine wrote.  seg_state: [pairs][nseg][3][d][d].
+    int nseg, pass;
+    const int *exact_flag;
+    float *seg_state;
 };
+
+// Segments (of every head) whose preceding chunks reach no window within the
+// limit: flag[pair][seg] = 1 (one thread per (pair, segment >= 1)).  Walking
+// back to chunk 0 within the limit needs no split (that start is exact).
+__global__ void cw_plan_kernel(const CwDev p, int *flag) {
+    const int pairs = p.B * p.Hv;
+    const int idx = static_cast<int>(blockIdx.x * blockDim.x + threadIdx.x);
+    if (idx >= pairs * (p.nseg - 1)) return;
+    const int pr = idx % pairs, seg = 1 + idx / pairs;
+    const int c_begin = seg * p.seg_chunks;
+    float acc = 0.f;
+    int v = 1;
+    for (int m = 1; m <= p.max_warmup; ++m) {
+        const int cc = c_begin - m;
+        if (cc < 0) {
+            v = 0;
+            break;
+        }
+        acc += p.bound[static_cast<int64_t>(pr) * p.nchunks + cc];
+        if (acc <= p.log_eps) {
+            v = 0;
+            break;
+        }
+    }
+    flag[static_cast<int64_t>(pr) * p.nseg + seg] = v;
+}
+
+__device__ __forceinline__ bool cw_head_split(const int *flag, int pr, int nseg) {
+    int any = 0;
+    for (int sg = 1; sg < nseg; ++sg) any |= flag[static_cast<int64_t>(pr) * nseg + sg];
+    return any != 0;
+}
 
 // Pre-pass shared memory (bytes).  After the A and P products the q/k tiles
 // hold A and T, the G tile holds T diag(beta) and the Kn tile holds V.
@@ -513,19 +553,28 @@ __global__ void __launch_bounds__(256, 1) cw_chain_kernel(const CwDev p) {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int g = lane >> 2, t4 = lane & 3;
     const int pairs = p.B * p.Hv;
-    const int pr = static_cast<int>(blockIdx.x % static_cast<unsigned>(pairs));
-    const int seg = static_cast<int>(blockIdx.x / static_cast<unsigned>(pairs));
+    const unsigned per_pass = static_cast<unsigned>(pairs * p.nseg);
+    const int bx = static_cast<int>(blockIdx.x % per_pass);
+    const int kind = p.pass == 1 ? static_cast<int>(blockIdx.x / per_pass) : -1;
+    const int pr = bx % pairs;
+    const int seg = bx / pairs;
     const int b = pr / p.Hv, hv = pr % p.Hv;
     const int c_begin = seg * p.seg_chunks;
     const int c_end = c_begin + p.seg_chunks < p.nchunks ? c_begin + p.seg_chunks : p.nchunks;
     int *misc = reinterpret_cast<int *>(sm + CH_MISC);
+    const bool exact = p.exact_flag != nullptr && cw_head_split(p.exact_flag, pr, p.nseg);
+    // transition pass: heads that need the split, segments whose maps are used
+    if (p.pass == 1 && (!exact || seg == p.nseg - 1 || (kind == 1 && seg == 0))) return;
 
     // Warm-up window: walk back from the segment start until the decay bound
     // reaches exp(log_eps) (start there from a zero state); at chunk 0 or past
-    // the window limit, start at chunk 0 from S0 (exact).
+    // the window limit, start at chunk 0 from S0 (exact).  The transition pass
+    // and the heads that take the split start every segment at its first chunk.
     if (tid == 0) {
         int cw = 0;
-        if (seg > 0) {
+        if (p.pass == 1 || exact) {
+            cw = c_begin;
+        } else if (seg > 0) {
             float acc = 0.f;
             for (int m = 1;; ++m) {
                 const int cc = c_begin - m;
@@ -544,7 +593,15 @@ __global__ void __launch_bounds__(256, 1) cw_chain_kernel(const CwDev p) {
 
     float S[16][4];
     {
-        const float *s0 = (c_w == 0 && p.S0) ? p.S0 + static_cast<int64_t>(pr) * kD * kD : nullptr;
+        // the starting state: S0 at chunk 0, a combined entering state for a split head,
+        // the identity for a kind-1 transition, else zero
+        const float *s0 = nullptr;
+        if (kind == 1)
+            s0 = nullptr;
+        else if (c_w == 0)
+            s0 = p.S0 ? p.S0 + static_cast<int64_t>(pr) * kD * kD : nullptr;
+        else if (p.pass == 0 && exact)
+            s0 = p.seg_state + ((static_cast<int64_t>(pr) * p.nseg + seg) * 3 + 2) * kD * kD;
 #pragma unroll
         for (int nt = 0; nt < 16; ++nt) {
             const int r = 16 * warp + g, col = 8 * nt + 2 * t4;
@@ -552,6 +609,9 @@ __global__ void __launch_bounds__(256, 1) cw_chain_kernel(const CwDev p) {
             if (s0) {
                 lo = *reinterpret_cast<const float2 *>(s0 + r * kD + col);
                 hi = *reinterpret_cast<const float2 *>(s0 + (r + 8) * kD + col);
+            } else if (kind == 1) {
+                lo = make_float2(r == col ? 1.f : 0.f, r == col + 1 ? 1.f : 0.f);
+                hi = make_float2(r + 8 == col ? 1.f : 0.f, r + 8 == col + 1 ? 1.f : 0.f);
             }
             S[nt][0] = lo.x;
             S[nt][1] = lo.y;
@@ -586,7 +646,7 @@ __global__ void __launch_bounds__(256, 1) cw_chain_kernel(const CwDev p) {
         const int st = (cc - c_w) & 1;
         const uint32_t stg = sb + st * kRecBytes;
         const uint8_t *stp = sm + st * kRecBytes;
-        if (p.state_out && cc >= c_begin) {
+        if (p.state_out && p.pass == 0 && cc >= c_begin) {
             __nv_bfloat16 *so = p.state_out + (static_cast<int64_t>(pr) * p.nchunks + cc) * kD * kD;
 #pragma unroll
             for (int nt = 0; nt < 16; ++nt) {
@@ -613,7 +673,8 @@ __global__ void __launch_bounds__(256, 1) cw_chain_kernel(const CwDev p) {
 #pragma unroll
             for (int hr = 0; hr < 2; ++hr) {
                 const int t = 16 * mt + g + 8 * hr;
-                const float2 f = unpack2(*reinterpret_cast<const uint32_t *>(stp + REC_UT + sw256(t, 8 * nh + nt) + 4 * t4));
+                const float2 f = kind == 1 ? make_float2(0.f, 0.f)   // values zero: U~ = 0
+                    : unpack2(*reinterpret_cast<const uint32_t *>(stp + REC_UT + sw256(t, 8 * nh + nt) + 4 * t4));
                 u[nt][2 * hr] = f.x;
                 u[nt][2 * hr + 1] = f.y;
                 ys[nt][2 * hr] = 0.f;
@@ -696,8 +757,13 @@ __global__ void __launch_bounds__(256, 1) cw_chain_kernel(const CwDev p) {
         }
     }
 
-    if (c_end == p.nchunks && p.S_T) {
-        float *so = p.S_T + static_cast<int64_t>(pr) * kD * kD;
+    float *s_end = nullptr;   // where this run's final state goes
+    if (p.pass == 1)
+        s_end = p.seg_state + ((static_cast<int64_t>(pr) * p.nseg + seg) * 3 + kind) * kD * kD;
+    else if (c_end == p.nchunks)
+        s_end = p.S_T;
+    if (s_end) {
+        float *so = p.pass == 1 ? s_end : s_end + static_cast<int64_t>(pr) * kD * kD;
 #pragma unroll
         for (int nt = 0; nt < 16; ++nt) {
             const int r = 16 * warp + g, col = 8 * nt + 2 * t4;
@@ -764,7 +830,24 @@ cudaError_t launch_chunked_cw(const ChunkedCwParams &p, cudaStream_t stream, int
     dv.bound = reinterpret_cast<float *>(p.ops + static_cast<size_t>(pairs) * nchunks * kRecBytes);
     dv.scalar_alpha = p.scalar_alpha ? 1 : 0;
     dv.state_out = static_cast<__nv_bfloat16 *>(p.state_out);
+    dv.nseg = P;
+    dv.pass = 0;
+    dv.exact_flag = nullptr;
+    dv.seg_state = nullptr;
     cw_prepass_kernel<<<static_cast<unsigned>(p.B * nchunks * p.Hv), 256, kPrepassSmem, stream>>>(dv);
+    // Exact sequence split for the heads whose segments reach no window (as the
+    // scalar prefill does): plan, transition runs, combine, then the output pass.
+    if (p.exact_flag && p.seg_state && takes_exact_split(pairs, nchunks, P, kD, p.seg_state_bytes)) {
+        dv.exact_flag = p.exact_flag;
+        dv.seg_state = p.seg_state;
+        const int nplan = static_cast<int>(pairs * (P - 1));
+        cw_plan_kernel<<<static_cast<unsigned>((nplan + 127) / 128), 128, 0, stream>>>(dv, p.exact_flag);
+        dv.pass = 1;
+        cw_chain_kernel<false><<<static_cast<unsigned>(2 * pairs * P), 256, kChainSmem, stream>>>(dv);
+        e = launch_segment_combine(p.exact_flag, p.seg_state, pairs, P, kD, stream);
+        if (e != cudaSuccess) return e;
+        dv.pass = 0;
+    }
     if (p.y)
         cw_chain_kernel<true><<<static_cast<unsigned>(pairs * P), 256, kChainSmem, stream>>>(dv);
     else

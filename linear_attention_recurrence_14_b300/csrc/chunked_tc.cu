@@ -1301,6 +1301,18 @@ int plan_segments(int64_t pairs, int64_t nchunks, int num_sms, int requested) {
     return best;
 }
 
+cudaError_t launch_segment_combine(const int *flag, float *seg_state, int64_t pairs, int P, int d,
+                                   cudaStream_t stream) {
+    cudaError_t e = set_smem_attributes();
+    if (e != cudaSuccess) return e;
+    const size_t comb_smem = 2 * static_cast<size_t>(d) * d * sizeof(float);
+    if (d == 128)
+        segment_combine_kernel<128><<<static_cast<unsigned>(pairs), 512, comb_smem, stream>>>(flag, seg_state, P);
+    else
+        segment_combine_kernel<64><<<static_cast<unsigned>(pairs), 512, comb_smem, stream>>>(flag, seg_state, P);
+    return cudaGetLastError();
+}
+
 bool takes_exact_split(int64_t pairs, int64_t nchunks, int P, int d, size_t seg_state_bytes) {
     // Only for long sequences: below kExactSplitMinChunks chunks per head a
     // restart from token 0 costs less than the split's three extra launches.

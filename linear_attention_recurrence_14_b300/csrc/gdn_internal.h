@@ -57,6 +57,14 @@ constexpr int kExactSplitSmBound = 160;
 // Sequences of fewer chunks (of 64 tokens) per head never take the exact split.
 constexpr int kExactSplitMinChunks = 256;
 
+// Segments per head for which a workspace reserves the exact split's maps
+// (0: none needed).
+inline int64_t exact_split_segments(int64_t pairs, int64_t nchunks) {
+    if (pairs <= 0 || nchunks <= 1) return 0;
+    const int64_t segs = (2 * kExactSplitSmBound + pairs - 1) / pairs;
+    return segs > nchunks ? nchunks : segs;
+}
+
 // Number of sequence segments per (batch, value head) the chunked prefill uses
 // (requested > 0 is taken as is, capped at the chunk count).
 int plan_segments(int64_t pairs, int64_t nchunks, int num_sms, int requested);
@@ -65,6 +73,11 @@ int plan_segments(int64_t pairs, int64_t nchunks, int num_sms, int requested);
 // split (plan, transition pass, combine, then the output pass: four launches
 // instead of one), given segment-state room of seg_state_bytes.
 bool takes_exact_split(int64_t pairs, int64_t nchunks, int P, int d, size_t seg_state_bytes);
+
+// Entering states of the segments of every head with a flag set: S_1 = B_0,
+// S_{s+1} = M_s S_s + B_s, over seg_state [pairs][P][3][d][d] (slots B, M, In).
+cudaError_t launch_segment_combine(const int *flag, float *seg_state, int64_t pairs, int P, int d,
+                                   cudaStream_t stream);
 
 // Chunked tensor-core prefill (bf16).  Builds the TMA descriptors and launches.
 cudaError_t launch_chunked(const ChunkedParams &p, cudaStream_t stream, int num_sms);
@@ -86,6 +99,10 @@ struct ChunkedCwParams {
     uint8_t *ops;                // chunked_cw_ops_bytes(B, T, Hv) bytes, 16-byte aligned
     bool scalar_alpha;           // alpha is [B, T, Hv] (one decay for every channel)
     void *state_out;             // nullptr, or the state entering every chunk [B * Hv][nchunks][d][d] bf16
+    // Exact sequence split (optional, as in ChunkedParams): flags and segment maps.
+    int *exact_flag;
+    float *seg_state;
+    size_t seg_state_bytes;
 };
 
 // The per-chunk operand record the chunked pre-pass writes (bytes): -W, U~,

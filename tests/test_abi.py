@@ -259,10 +259,14 @@ def test_chunked_backward_workspace_and_arguments(L):
     r = lambda n: (n + 255) // 256 * 256  # noqa: E731
     # chunk records (74,240 bytes) and decay bounds (4 bytes) per (head, chunk); then the entering
     # states and the state gradients (bf16, 32 KB each per (head, chunk)); then dS0's staging
+    # and the exact split's flags and segment maps (segs = min(chunks, ceil(320 / (B Hv))) per head)
     for B, T, Hv in [(2, 1000, 4), (1, 64, 2), (1, 65, 1)]:
         s = shape(B=B, T=T, Hqk=1, Hv=Hv, d=128)
-        n = B * Hv * ((T + 63) // 64)
-        want = r(r(n * 74244) + 2 * n * 128 * 128 * 2) + B * Hv * 128 * 128 * 4
+        nc = (T + 63) // 64
+        n = B * Hv * nc
+        segs = min(nc, -(-320 // (B * Hv))) if nc > 1 else 0
+        split = r(B * Hv * segs * 4) + B * Hv * segs * 3 * 128 * 128 * 4
+        want = r(r(r(n * 74244) + 2 * n * 128 * 128 * 2) + split) + B * Hv * 128 * 128 * 4
         assert L.gdn_backward_chunked_workspace_bytes(ctypes.byref(s)) == want
     assert L.gdn_backward_chunked_workspace_bytes(ctypes.byref(shape(d=64))) == 0
     assert L.gdn_backward_chunked_workspace_bytes(ctypes.byref(shape(dtype=gdn.GDN_F32))) == 0
@@ -290,7 +294,10 @@ def test_channelwise_chunked_workspace_and_arguments(L):
     r = lambda n: (n + 255) // 256 * 256  # noqa: E731
     for B, T, Hv in [(2, 1000, 4), (1, 1, 2)]:
         s = shape(B=B, T=T, Hqk=2, Hv=Hv, d=128)
-        want = r(256 + B * Hv * 128 * 128 * 4) + B * Hv * ((T + 63) // 64) * 74244
+        nc = (T + 63) // 64
+        segs = min(nc, -(-320 // (B * Hv))) if nc > 1 else 0
+        split = r(B * Hv * segs * 4) + r(B * Hv * segs * 3 * 128 * 128 * 4)
+        want = r(256 + B * Hv * 128 * 128 * 4) + split + B * Hv * nc * 74244
         assert L.gdn_prefill_cw_workspace_bytes(ctypes.byref(s)) == want
     # shapes the token-sequential kernel takes need only the status area
     assert L.gdn_prefill_cw_workspace_bytes(ctypes.byref(shape(d=64))) == 256

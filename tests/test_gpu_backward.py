@@ -167,3 +167,17 @@ def test_backward_chunked_training_shape_sampled_heads():
         got = {n: sl(out[n]) for n in ("dq", "dk", "dv", "dlog_alpha", "dbeta")}
         got["dS0"] = out["dS0"][b:b + 1, heads]
         _check_chunked(got, ref)
+
+
+@pytest.mark.parametrize("decay", [0.0, 1.2e-4])   # alpha = 1 and alpha ~ 1 - 1e-4
+def test_backward_chunked_exact_split_for_gates_that_do_not_decay(decay):
+    # Over 256 chunks without any window, both state chains take the exact split; the result
+    # must agree with the fp32 token-sequential backward (itself pinned to the oracle).
+    T = 64 * 260 + 5
+    x = make_prefill_inputs(1, T, 1, 2, 128, "bf16", decay_scale=decay, s0_std=0.02, seed=97, device="cuda")
+    g = make_backward_grads(1, T, 2, 128, "bf16", ds_std=1.0, seed=97, device="cuda")
+    out = gdn.backward(x.q, x.k, x.v, x.alpha, x.beta, x.S0, g.dy, g.dS_T, algorithm=gdn.ALGO_CHUNKED)
+    seq = gdn.backward(x.q, x.k, x.v, x.alpha, x.beta, x.S0, g.dy, g.dS_T)
+    torch.cuda.synchronize()
+    for n in ("dq", "dk", "dv", "dlog_alpha", "dbeta", "dS0"):
+        assert rel_err(out[n], seq[n].double().cpu().numpy()) <= CHUNKED_TOL, n

@@ -150,3 +150,20 @@ def test_prefill_cw_chunked_grouped_shape_windows_match_oracle():
             if t1 == T:
                 errs.append(rel_err(S_T[0, h], So[0, i]))
     assert max(errs) <= TOL[torch.bfloat16], errs
+
+
+def test_prefill_cw_chunked_exact_split_for_channels_that_do_not_decay():
+    # A quarter of the channels keep alpha = 1, so no window of preceding chunks forgets the
+    # state: over 256 chunks the chain takes the exact split (segment maps and their combine).
+    T = 64 * 260 + 7
+    x = make_prefill_inputs(1, T, 1, 2, 128, "bf16", s0_std=0.02, seed=95, device="cuda")
+    a = make_channelwise_alpha(1, T, 2, 128, decay_scale=0.05, seed=96, device="cuda")
+    a[..., 96:] = 1.0
+    y, S_T = gdn.prefill_cw(x.q, x.k, x.v, a, x.beta, x.S0, segments=9)
+    yo, So = oracle.recurrence(x.q, x.k, x.v, a, x.beta, x.S0)
+    assert rel_err(y, yo) <= TOL[torch.bfloat16]
+    assert rel_err(S_T, So) <= TOL[torch.bfloat16]
+    # against one sequential pass of the same chain (segments = 1): only rounding order differs
+    y1, S1 = gdn.prefill_cw(x.q, x.k, x.v, a, x.beta, x.S0, segments=1)
+    assert rel_err(y, y1.double().cpu().numpy()) <= TOL[torch.bfloat16]
+    assert rel_err(S_T, S1.double().cpu().numpy()) <= TOL[torch.bfloat16]
