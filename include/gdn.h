@@ -243,8 +243,9 @@ gdn_status gdn_prefill_noalloc_status(void *stream);
  * path), the lower-triangular inverse and the chunk's W, U~ and P, then a
  * chain kernel runs the state over the chunks, split into segments with
  * warm-up windows as in gdn_prefill (the window bound uses the largest
- * channel's decay; a segment without a window restarts from token 0, which
- * is exact).  Every other shape runs the token-sequential kernel (bf16 or
+ * channel's decay), and the exact sequence split for the segments without
+ * a window on sequences of at least 256 chunks (else they restart from
+ * token 0, also exact).  Every other shape runs the token-sequential kernel (bf16 or
  * fp32, state in fp32 registers), as does the decode step.
  *
  * gdn_prefill_cw allocates the chunked path's workspace itself, in stream
