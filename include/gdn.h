@@ -353,8 +353,8 @@ gdn_status gdn_backward(const gdn_shape *shape,
  * lower-triangular inverse T = (I + A)^{-1}).  Products take bf16 operands
  * with fp32 accumulation, so results carry bf16-level rounding (about 1e-2
  * of the largest gradient), unlike gdn_backward's fp32 arithmetic; the state
- * chains split long sequences into segments with warm-up windows, as the
- * prefill does.  dq and dk are summed over the value heads of a group with
+ * chains split long sequences into segments with warm-up windows, and with
+ * the exact sequence split where gates do not decay, as the prefill does.  dq and dk are summed over the value heads of a group with
  * atomic additions (deterministic for up to two value heads per key head).
  * ws: device memory of gdn_backward_chunked_workspace_bytes(shape) bytes,
  * 256-byte aligned, no initial contents needed (74,244 bytes of chunk
