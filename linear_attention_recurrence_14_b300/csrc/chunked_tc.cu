@@ -563,7 +563,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int hk = hv / p.group;
     const int c_begin = seg * p.seg_chunks;
     const int c_end = min(p.nchunks, c_begin + p.seg_chunks);
-    const bool last_seg = seg == p.nseg - 1;
 
     if (tid == 0) {
         for (int s = 0; s < kStages; ++s) {

@@ -23,12 +23,6 @@ constexpr int kTile = 64;          // tokens per prologue warp
 constexpr int kMaxConv = 4;
 constexpr float kL2Eps = 1e-6f;
 
-__device__ __forceinline__ float warp_allsum(float v) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    return v;
-}
-
 // sigma(u) with the fast exponential and the approximate (MUFU) division:
 // about 2 ulp, far below the bf16 rounding of the outputs; the kernels are
 // otherwise limited by these per-element instructions, not by HBM.
