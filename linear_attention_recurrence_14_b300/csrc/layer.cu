@@ -324,6 +324,8 @@ struct EpiloguePlan {
 // 16-byte accesses: a lane handles 8 channels, a row of d channels takes
 // d/8 lanes (16 for d = 128, 8 for d = 64), so a warp covers 32*8/d rows per
 // access; two such row sets are in flight per iteration; grid-stride.
+constexpr int kEpiRows = 4;   // row sets in flight per warp
+
 template <int LPR>   // lanes per row
 __global__ void __launch_bounds__(256) epilogue_kernel(EpiloguePlan p) {
     constexpr int RPW = 32 / LPR;   // rows per warp access
@@ -337,11 +339,11 @@ __global__ void __launch_bounds__(256) epilogue_kernel(EpiloguePlan p) {
     const float inv_d = 1.f / static_cast<float>(p.d);
     const int64_t nsets = (p.rows + RPW - 1) / RPW;
 #pragma unroll 1
-    for (int64_t s0 = w0; s0 < nsets; s0 += 2 * warps) {
-        uint4 yr[2], zr[2];
-        int64_t r[2];
+    for (int64_t s0 = w0; s0 < nsets; s0 += kEpiRows * warps) {
+        uint4 yr[kEpiRows], zr[kEpiRows];
+        int64_t r[kEpiRows];
 #pragma unroll
-        for (int j = 0; j < 2; ++j) {
+        for (int j = 0; j < kEpiRows; ++j) {
             r[j] = (s0 + j * warps) * RPW + sub;
             if (r[j] < p.rows) {
                 yr[j] = *reinterpret_cast<const uint4 *>(p.y + r[j] * p.d + cl * 8);
@@ -351,7 +353,7 @@ __global__ void __launch_bounds__(256) epilogue_kernel(EpiloguePlan p) {
             }
         }
 #pragma unroll
-        for (int j = 0; j < 2; ++j) {
+        for (int j = 0; j < kEpiRows; ++j) {
             const __nv_bfloat162 *yh = reinterpret_cast<const __nv_bfloat162 *>(&yr[j]);
             const __nv_bfloat162 *zh = reinterpret_cast<const __nv_bfloat162 *>(&zr[j]);
             float y[8], z[8];
@@ -365,13 +367,13 @@ __global__ void __launch_bounds__(256) epilogue_kernel(EpiloguePlan p) {
             for (int e = 0; e < 8; ++e) ss = fmaf(y[e], y[e], ss);
 #pragma unroll
             for (int o = LPR / 2; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-            const float inv = rsqrtf(ss * inv_d + p.eps);
+            const float inv = rsqrt_ftz(ss * inv_d + p.eps);
             uint4 orow;
             uint32_t *ow = reinterpret_cast<uint32_t *>(&orow);
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                const __nv_bfloat162 v = __floats2bfloat162_rn(sigmoidf_(z[2 * e]) * y[2 * e] * inv * g[2 * e],
-                                                               sigmoidf_(z[2 * e + 1]) * y[2 * e + 1] * inv * g[2 * e + 1]);
+                const __nv_bfloat162 v = __floats2bfloat162_rn(sigmoid_ftz(z[2 * e]) * y[2 * e] * inv * g[2 * e],
+                                                               sigmoid_ftz(z[2 * e + 1]) * y[2 * e + 1] * inv * g[2 * e + 1]);
                 ow[e] = *reinterpret_cast<const uint32_t *>(&v);
             }
             if (r[j] < p.rows) *reinterpret_cast<uint4 *>(p.o + r[j] * p.d + cl * 8) = orow;
@@ -526,8 +528,8 @@ extern "C" gdn_status gdn_layer_epilogue(const gdn_layer_shape *shape, const voi
     int dev_id = 0, sms = 148;
     cudaGetDevice(&dev_id);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev_id);
-    // 8 resident CTAs of 8 warps per SM; each warp covers 2 * 256 / d rows per iteration
-    const int64_t rows_per_cta = 8 * 2 * (256 / s.d);
+    // 8 resident CTAs of 8 warps per SM; each warp covers kEpiRows * 256 / d rows per iteration
+    const int64_t rows_per_cta = 8 * kEpiRows * (256 / s.d);
     const int64_t want = (p.rows + rows_per_cta - 1) / rows_per_cta;
     const unsigned grid = static_cast<unsigned>(want < int64_t{sms} * 8 ? want : int64_t{sms} * 8);
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
