@@ -51,7 +51,6 @@ constexpr int kD = 128;            // head dimension (dk = dv)
 // Exponents are kept in base 2 (G holds cumulative log2 alpha): the largest
 // power of two taken through a bf16 operand is 2^115 (about e^80).
 constexpr float kMaxExp2 = 115.f;
-constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
 // Chunk record in the workspace, per (batch, value head, chunk); tiles are
@@ -208,7 +207,7 @@ __global__ void __launch_bounds__(256, 2) cw_prepass_kernel(const CwDev p) {
         float run = 0.f;
 #pragma unroll 8
         for (int t = 32 * h; t < 32 * h + 32; ++t) {
-            run += logf(G[t * kD + ch]) * kLog2e;
+            run += log2_approx(G[t * kD + ch]);
             G[t * kD + ch] = run;
         }
     }
@@ -235,22 +234,23 @@ __global__ void __launch_bounds__(256, 2) cw_prepass_kernel(const CwDev p) {
     }
     __syncthreads();
 
-    // ---- decay bound of the chunk: sum over tokens of max_c log alpha (natural log)
+    // ---- decay bound of the chunk: sum over tokens of max_c log alpha (natural log).
+    // Warp w: tokens 8w..8w+7; four lanes per token, each over 32 channels
+    // 32 (lane % 4) + i, visited from i = lane so that a step reads 32 banks.
     {
-        float part = 0.f;
-#pragma unroll 1
-        for (int i = 0; i < 8; ++i) {
-            const int t = warp * 8 + i;
-            float m = -INFINITY;
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const int ch = lane + 32 * j;
-                m = fmaxf(m, G[t * kD + ch] - (t > 0 ? G[(t - 1) * kD + ch] : 0.f));
-            }
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-            part += m;
+        const int t = warp * 8 + (lane >> 2), cb = 32 * (lane & 3);
+        float m = -INFINITY;
+#pragma unroll 8
+        for (int i = 0; i < 32; ++i) {
+            const int ch = cb + ((lane + i) & 31);
+            m = fmaxf(m, G[t * kD + ch] - (t > 0 ? G[(t - 1) * kD + ch] : 0.f));
         }
+        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+        float part = m;   // then the sum over the warp's 8 tokens
+        part += __shfl_xor_sync(0xffffffffu, part, 4);
+        part += __shfl_xor_sync(0xffffffffu, part, 8);
+        part += __shfl_xor_sync(0xffffffffu, part, 16);
         if (lane == 0) wred[warp] = part;
     }
     // ---- diagonal blocks past the bf16 range, element by element (t >= s in the block)
@@ -412,14 +412,14 @@ __global__ void __launch_bounds__(256, 2) cw_prepass_kernel(const CwDev p) {
                     }
                 }
             }
+        } else if (warp - ntask < 3 - I) {
+            // a block (I, np > I) of P above the diagonal blocks: zeros, 16 bytes per lane
+            const int np = I + 1 + (warp - ntask);
+            const int t = 16 * I + (lane >> 1), s = 16 * np + 8 * (lane & 1);
+            *reinterpret_cast<uint4 *>(rec + REC_P + t * 128 + s * 2) = zero4;
         }
     }
     __syncthreads();
-    // P above the diagonal blocks: zeros
-    for (int e = tid; e < 64 * 32; e += 256) {
-        const int t = e >> 5, s = 2 * (e & 31);
-        if (s >= 16 * ((t >> 4) + 1)) *reinterpret_cast<uint32_t *>(rec + REC_P + t * 128 + s * 2) = 0u;
-    }
 
     // ---- A into the block-packed solve layout (over the q/k tiles), V into the Kn tile
     float *At = reinterpret_cast<float *>(sm + PP_AT);
@@ -483,49 +483,57 @@ __global__ void __launch_bounds__(256, 2) cw_prepass_kernel(const CwDev p) {
     __syncthreads();
 
     // ---- W = sum_J (T2[:, J] Kloc[J]) (.) e^{R_J} (Kp = Kloc (.) e^{R_J} on block J)
-    // and U~ = T2 V: warp w takes rows 16 (w & 3) and columns 64 (w >> 2) .. + 63.
+    // and U~ = T2 V: warp w takes columns 16 w .. 16 w + 15 of every row block (the
+    // ten nonzero blocks of T2 give each warp the same work).
     {
-        const int mt = warp & 3, nh = warp >> 2;
-        float aw[8][4], au[8][4];
+        float aw[4][2][4], au[4][2][4];
 #pragma unroll
-        for (int nt = 0; nt < 8; ++nt)
+        for (int mt = 0; mt < 4; ++mt)
 #pragma unroll
-            for (int e = 0; e < 4; ++e) aw[nt][e] = au[nt][e] = 0.f;
+            for (int e = 0; e < 8; ++e) aw[mt][e >> 2][e & 3] = au[mt][e >> 2][e & 3] = 0.f;
 #pragma unroll
         for (int J = 0; J < 4; ++J) {
-            if (J > mt) break;   // T2 is zero above the diagonal blocks
-            uint32_t af[4];
-            ldsm_x4(af, sb + PP_T2 + sw128(16 * mt + a_row(lane), 2 * J + a_ch(lane)));
+            uint32_t bk[4], bv[4];
+            ldsm_x4_t(bk, sb + PP_KL + sw256(16 * J + bt_row(lane), 2 * warp + bt_ch(lane)));
+            ldsm_x4_t(bv, sb + PP_KN + sw256(16 * J + bt_row(lane), 2 * warp + bt_ch(lane)));
+            float e[2][2];
 #pragma unroll
-            for (int np = 0; np < 4; ++np) {
-                uint32_t bk[4], bv[4];
-                ldsm_x4_t(bk, sb + PP_KL + sw256(16 * J + bt_row(lane), 8 * nh + 2 * np + bt_ch(lane)));
-                ldsm_x4_t(bv, sb + PP_KN + sw256(16 * J + bt_row(lane), 8 * nh + 2 * np + bt_ch(lane)));
+            for (int jj = 0; jj < 2; ++jj) {
+                const int col = 16 * warp + 8 * jj + 2 * t4;
+                e[jj][0] = eR[J * kD + col];
+                e[jj][1] = eR[J * kD + col + 1];
+            }
+#pragma unroll
+            for (int mt = J; mt < 4; ++mt) {   // T2 is zero above the diagonal blocks
+                uint32_t af[4];
+                ldsm_x4(af, sb + PP_T2 + sw128(16 * mt + a_row(lane), 2 * J + a_ch(lane)));
                 float tw[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
                 mma16816(tw[0], af, bk[0], bk[1]);
                 mma16816(tw[1], af, bk[2], bk[3]);
-                mma16816(au[2 * np], af, bv[0], bv[1]);
-                mma16816(au[2 * np + 1], af, bv[2], bv[3]);
+                mma16816(au[mt][0], af, bv[0], bv[1]);
+                mma16816(au[mt][1], af, bv[2], bv[3]);
 #pragma unroll
                 for (int jj = 0; jj < 2; ++jj) {
-                    const int col = 64 * nh + 16 * np + 8 * jj + 2 * t4;
-                    const float e0 = eR[J * kD + col], e1 = eR[J * kD + col + 1];
-                    aw[2 * np + jj][0] = fmaf(tw[jj][0], e0, aw[2 * np + jj][0]);
-                    aw[2 * np + jj][1] = fmaf(tw[jj][1], e1, aw[2 * np + jj][1]);
-                    aw[2 * np + jj][2] = fmaf(tw[jj][2], e0, aw[2 * np + jj][2]);
-                    aw[2 * np + jj][3] = fmaf(tw[jj][3], e1, aw[2 * np + jj][3]);
+                    aw[mt][jj][0] = fmaf(tw[jj][0], e[jj][0], aw[mt][jj][0]);
+                    aw[mt][jj][1] = fmaf(tw[jj][1], e[jj][1], aw[mt][jj][1]);
+                    aw[mt][jj][2] = fmaf(tw[jj][2], e[jj][0], aw[mt][jj][2]);
+                    aw[mt][jj][3] = fmaf(tw[jj][3], e[jj][1], aw[mt][jj][3]);
                 }
             }
         }
 #pragma unroll
-        for (int nt = 0; nt < 8; ++nt) {
-            const int col = 64 * nh + 8 * nt + 2 * t4;
+        for (int mt = 0; mt < 4; ++mt) {
 #pragma unroll
-            for (int hr = 0; hr < 2; ++hr) {
-                const int t = 16 * mt + g + 8 * hr;
-                *reinterpret_cast<uint32_t *>(rec + REC_WN + t * 256 + col * 2) =
-                    pack2(-aw[nt][2 * hr], -aw[nt][2 * hr + 1]);
-                *reinterpret_cast<uint32_t *>(rec + REC_UT + t * 256 + col * 2) = pack2(au[nt][2 * hr], au[nt][2 * hr + 1]);
+            for (int nt = 0; nt < 2; ++nt) {
+                const int col = 16 * warp + 8 * nt + 2 * t4;
+#pragma unroll
+                for (int hr = 0; hr < 2; ++hr) {
+                    const int t = 16 * mt + g + 8 * hr;
+                    *reinterpret_cast<uint32_t *>(rec + REC_WN + t * 256 + col * 2) =
+                        pack2(-aw[mt][nt][2 * hr], -aw[mt][nt][2 * hr + 1]);
+                    *reinterpret_cast<uint32_t *>(rec + REC_UT + t * 256 + col * 2) =
+                        pack2(au[mt][nt][2 * hr], au[mt][nt][2 * hr + 1]);
+                }
             }
         }
     }

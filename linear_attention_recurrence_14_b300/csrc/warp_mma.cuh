@@ -65,6 +65,13 @@ __device__ __forceinline__ float exp2_ftz(float x) {
     return y;
 }
 
+// log2(x) with the PTX approximation (absolute error about 2^-22 near 1).
+__device__ __forceinline__ float log2_approx(float x) {
+    float y;
+    asm("lg2.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
     const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<const uint32_t *>(&v);
