@@ -167,3 +167,30 @@ def test_prefill_cw_chunked_exact_split_for_channels_that_do_not_decay():
     y1, S1 = gdn.prefill_cw(x.q, x.k, x.v, a, x.beta, x.S0, segments=1)
     assert rel_err(y, y1.double().cpu().numpy()) <= TOL[torch.bfloat16]
     assert rel_err(S_T, S1.double().cpu().numpy()) <= TOL[torch.bfloat16]
+
+
+def test_prefill_cw_chunk_decay_bounds():
+    # The pre-pass writes, per (batch, value head, chunk), the bound sum_t max_c log alpha_tc
+    # (natural log) that the warm-up windows and the exact split's plan compare with
+    # log_eps: the state's decay over the chunk is at most its exponential, since
+    # ||diag(alpha)(I - beta k k^T)|| <= max_c alpha_c for unit keys and beta in [0, 1].
+    # White-box: the bounds are the last B * Hv * nchunks floats of the chunked path's
+    # workspace.  Checked against a host computation from the same alpha on a ragged
+    # length with some channels at alpha = 1 and some strongly decaying.
+    B, T, Hqk, Hv, d = 2, 1000, 1, 2, 128
+    x = make_prefill_inputs(B, T, Hqk, Hv, d, "bf16", s0_std=0.02, seed=41, device="cuda")
+    a = make_channelwise_alpha(B, T, Hv, d, decay_scale=0.3, seed=41, device="cuda")
+    a[:, :, 0, :8] = 1.0
+    a[:, 500:, 1, 100:] = 1e-3
+    ws = gdn.new_cw_workspace(gdn.shape_of(x.q, x.v), "cuda")
+    _cw_chunked(x, a, workspace=ws)
+    torch.cuda.synchronize()
+    nchunks = (T + 63) // 64
+    n = B * Hv * nchunks
+    got = ws[ws.numel() - 4 * n:].view(torch.float32).reshape(B, Hv, nchunks).double().cpu()
+    la = torch.log(a.double().cpu()).amax(dim=3)                     # [B, T, Hv]
+    la = torch.cat([la, torch.zeros(B, nchunks * 64 - T, Hv, dtype=la.dtype)], 1)
+    want = la.reshape(B, nchunks, 64, Hv).sum(2).permute(0, 2, 1)   # [B, Hv, nchunks]
+    # base-2 cumulative sums in fp32 with an approximate log2 (about 2^-22 per token)
+    assert torch.allclose(got, want, rtol=1e-4, atol=2e-3), (got - want).abs().max()
+    assert (got[:, 0, :] > -1e-4).all()   # the head with channels at alpha = 1 never decays
