@@ -398,6 +398,26 @@ __device__ __forceinline__ void mma_run_t(uint32_t d, const MmaOperand &a, const
     }
 }
 
+// A product with a lower-triangular right factor over the chunk's tokens:
+// D[:, i] (+)= sum_{j <= i} A[:, j] B[i][j] with B stored K-major ([i rows][j],
+// 128-byte rows) and N = 64.  The K step over tokens 16 kk .. 16 kk + 15 only
+// reaches columns i >= 16 kk, so it is issued with N = 64 - 16 kk from column
+// 16 kk of D and row 16 kk of B: the zero blocks above B's block diagonal are
+// not multiplied.  idesc0: the instruction descriptor without its N field.
+template <bool TMEM_A>
+__device__ __forceinline__ void mma_run_tri(uint32_t d, const MmaOperand &a, const MmaOperand &b, uint32_t idesc0, uint32_t acc) {
+#pragma unroll 1
+    for (int kk = 0; kk < 4; ++kk) {
+        const uint32_t idesc = idesc0 | (static_cast<uint32_t>((64 - 16 * kk) >> 3) << 17);
+        const uint64_t bd = b.desc + ((operand_offset(b, kk) + 2048u * kk) >> 4);
+        const uint32_t accumulate = acc | (kk > 0 ? 1u : 0u);
+        if constexpr (TMEM_A)
+            mma_bf16_ts_w(d + 16u * kk, a.tmem + operand_offset(a, kk), bd, idesc, accumulate);
+        else
+            mma_bf16_w(d + 16u * kk, a.desc + (operand_offset(a, kk) >> 4), bd, idesc, accumulate);
+    }
+}
+
 // A rows of a chunk (gate warps): row i of K K^T is TMEM lane 64 + i.  Written
 // into the block-packed layout, A[i][j] at blk(i/16, j/16) + (j%16)*kBS + i%16,
 // for j < i.  Fast gates: A_ij = (beta_i gamma_i) (1/gamma_j) (k_i.k_j).
@@ -718,11 +738,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t a = kq_addr(j % kStages);
                 mma_run_t<8, false>(tb + TM_GW + (j & 1) * 64, smem_kmajor(a, 16384u), smem_kmajor(a + 8192, 16384u), ID_KK, 0u);
             };
+            // W^T = K^T T1^T and U~^T = V^T T2^T: T1, T2 are lower triangular by blocks
+            constexpr uint32_t ID_MK0 = idesc_bf16(128, 0, true, false);
+            constexpr uint32_t ID_TS0 = idesc_bf16(128, 0, false, false);
             auto wu = [&](int j) {
                 const int s = j % kStages;
-                mma_run_t<4, false>(tb + TM_GW + (j & 1) * 64, smem_mnmajor(kq_addr(s) + 8192, 16384u), smem_kmajor(t1, 0u), ID_MK, 0u);
+                mma_run_tri<false>(tb + TM_GW + (j & 1) * 64, smem_mnmajor(kq_addr(s) + 8192, 16384u), smem_kmajor(t1, 0u), ID_MK0, 0u);
                 if (!zero_v)
-                    mma_run_t<4, false>(tb + TM_ZU, smem_mnmajor(vw_addr(s), 8192u), smem_kmajor(t2, 0u), ID_MK, 0u);
+                    mma_run_tri<false>(tb + TM_ZU, smem_mnmajor(vw_addr(s), 8192u), smem_kmajor(t2, 0u), ID_MK0, 0u);
             };
             bool ok = true;
             do {
@@ -770,7 +793,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tc_fence_after();
                     // Y^T = S^T Q~^T + U^T P^T
                     mma_run_t<8, true>(tb + TM_Y, sa, smem_kmajor(kq_addr(s), 16384u), ID_TS, 0u);
-                    mma_run_t<4, true>(tb + TM_Y, ua, smem_kmajor(p_addr(s), 0u), ID_TS, 1u);
+                    mma_run_tri<true>(tb + TM_Y, ua, smem_kmajor(p_addr(s), 0u), ID_TS0, 1u);   // P^ lower triangular
                     mma_commit_w(&bars[B_YFULL]);
                     mma_commit_w(&bars[B_EMPTY + s]);
                     if (j + 1 < n) {
