@@ -720,7 +720,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t tb = __shfl_sync(0xffffffffu, tb_s, 0);
             const int n = __shfl_sync(0xffffffffu, n_s, 0);
             constexpr uint32_t ID_KK = idesc_bf16(128, 64, false, false);   // A, B K-major
-            constexpr uint32_t ID_MK = idesc_bf16(128, 64, true, false);    // A MN-major
             constexpr uint32_t ID_TS = idesc_bf16(128, 64, false, false);   // A in TMEM, B K-major
             constexpr uint32_t ID_TD = idesc_bf16(128, 128, false, true);   // A in TMEM, B MN-major
             constexpr uint32_t ID_TSM = idesc_bf16(128, 64, false, true);   // A in TMEM, B MN-major, N = 64
@@ -791,9 +790,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mma_commit_w(&bars[B_DFULL]);
                     if (j > 0 && !(ok = wait(&bars[B_YFREE], (j - 1) & 1))) break;
                     tc_fence_after();
-                    // Y^T = S^T Q~^T + U^T P^T
-                    mma_run_t<8, true>(tb + TM_Y, sa, smem_kmajor(kq_addr(s), 16384u), ID_TS, 0u);
-                    mma_run_tri<true>(tb + TM_Y, ua, smem_kmajor(p_addr(s), 0u), ID_TS0, 1u);   // P^ lower triangular
+                    // Y^T = S^T Q~^T + U^T P^T, for the chunks whose y is stored (not the
+                    // warm-up window, not a transition pass)
+                    if (p.pass == 0 && c_w + j >= c_begin) {
+                        mma_run_t<8, true>(tb + TM_Y, sa, smem_kmajor(kq_addr(s), 16384u), ID_TS, 0u);
+                        mma_run_tri<true>(tb + TM_Y, ua, smem_kmajor(p_addr(s), 0u), ID_TS0, 1u);   // P^ lower triangular
+                    }
                     mma_commit_w(&bars[B_YFULL]);
                     mma_commit_w(&bars[B_EMPTY + s]);
                     if (j + 1 < n) {
@@ -904,7 +906,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = ok && bwait(&bars[B_FULL + s], (j / kStages) & 1, abort_flag, p.status);
             ok = ok && bwait(&bars[B_GRAM + (j & 1)], (j >> 1) & 1, abort_flag, p.status);
             if (!bar_and(2, 128, ok)) return false;
-            if (l >= 64) return true;
+            if (l >= 64 || p.pass != 0 || c_w + j < c_begin) return true;   // P^ (and Q~) feed y only
             const uint32_t gw = tb + TM_GW + (j & 1) * 64;
             uint8_t *pbuf = sm + OFF_P + s * kPBytes;
             tc_fence_after();
