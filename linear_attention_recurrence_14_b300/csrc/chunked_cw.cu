@@ -279,6 +279,7 @@ __global__ void __launch_bounds__(256, 2) cw_prepass_kernel(const CwDev p) {
     }
 
     // ---- per-token operands: Qp, Kl to the record; Qloc (in place of q), Kloc
+    #pragma unroll 2
     for (int e = tid; e < kC * 16; e += 256) {
         const int t = e >> 4, pc = e & 15, I = t >> 4;
         const uint32_t off = sw256(t, pc);
@@ -346,6 +347,7 @@ __global__ void __launch_bounds__(256, 2) cw_prepass_kernel(const CwDev p) {
         fac[e] = exp2_ftz(R[I * kD + ch] - rj);
     }
     __syncthreads();
+    #pragma unroll 2
     for (int e = tid; e < 160 * 16; e += 256) {   // 16 + 32 + 48 + 64 rows
         const int row = e >> 4, pc = e & 15;
         const int I = row < 16 ? 0 : (row < 48 ? 1 : (row < 96 ? 2 : 3));
